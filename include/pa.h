@@ -1,0 +1,189 @@
+/*
+ * pa.h -- C ABI of the paged-KV GQA attention library for GB300 (sm_103a).
+ *
+ * Operations (each cites the page section that defines it):
+ *   pa_write_cache      reshape_and_cache scatter of new K/V rows into pages
+ *                       ("paged_attn.py", PagedAttention.write_to_paged_cache)
+ *   pa_decode           single-pass paged GQA decode
+ *                       ("paged_attn.py", PagedAttention._forward_decode_pytorch
+ *                        and the paged_attention_v1 call in forward_decode)
+ *   pa_decode_split     split-KV decode: 512-token partitions with fp32
+ *                       per-partition max / sum / partial output, then a
+ *                       log-sum-exp merge ("paged_attn.py", forward_decode, V2
+ *                       branch; "libmir-cuda attention/mod.rs",
+ *                       SplitPagedAttention and its workspace)
+ *   pa_ragged_prefill   ragged (varlen) causal prefill of many requests in one
+ *                       launch through qo_indptr / kv_indptr, over contiguous
+ *                       or paged K/V ("spark_runtime/flashinfer.rs",
+ *                       ragged_prefill_bf16_hd256; "paged_attn.py",
+ *                       _forward_prefix_pytorch)
+ *
+ * Conventions shared by every entry point:
+ *  - All data pointers are DEVICE pointers of the current CUDA device unless
+ *    the name ends in _h (host).  The caller owns all memory; no entry point
+ *    allocates, frees or synchronises (except pa_get_device_status, which
+ *    synchronises `stream`).  Work is enqueued on `stream` (a cudaStream_t,
+ *    NULL = legacy default stream) and returns immediately.
+ *  - bf16 tensors are passed as void pointers to IEEE bfloat16 data.
+ *  - KV pools are addressed by element strides (stride_block, stride_head,
+ *    stride_token); the head_dim axis is contiguous.  The default layout is
+ *    HND per page, [num_blocks][num_kv_heads][block_size][head_dim], i.e.
+ *    strides (nkv*bs*hd, bs*hd, hd).  The NHD page layout
+ *    [num_blocks][block_size][num_kv_heads][head_dim] is (bs*nkv*hd, hd, nkv*hd).
+ *    K and V pools share one set of strides.
+ *  - Supported shapes: head_dim in {64, 128, 256}; block_size == 16;
+ *    num_q_heads % num_kv_heads == 0 with group size in {1, 2, 4, 8}.
+ *    Pointers must be 16-byte aligned and strides multiples of 8 elements.
+ *  - Return value: PA_OK or an error status; on error nothing was enqueued and
+ *    pa_last_error() (thread-local) describes the problem.
+ *  - Device-side guards: a block-table entry outside [0, num_blocks), a
+ *    seq_len larger than max_blocks_per_seq * block_size, or a slot outside
+ *    the pool is never dereferenced: the affected tokens contribute nothing and
+ *    a device status word records PA_ERR_DEVICE_BOUNDS.  Every pipeline wait
+ *    is bounded; a wait that runs out records PA_ERR_TIMEOUT and the kernel
+ *    returns.  Read (and clear) that word with pa_get_device_status().
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,       /* bad argument (null pointer, negative size, ...) */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but unsupported shape or layout */
+    PA_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+    PA_ERR_WORKSPACE = 4,     /* workspace too small or misaligned */
+    PA_ERR_TIMEOUT = 5,       /* device-side bounded wait ran out */
+    PA_ERR_DEVICE_BOUNDS = 6  /* device-side index guard fired */
+} pa_status;
+
+/* Tokens per split-KV partition ("paged_attn.py", _PARTITION_SIZE). */
+#define PA_PARTITION_TOKENS 512
+
+/*
+ * pa_write_cache -- reshape_and_cache.
+ * For each token t in [0, num_tokens) with slot = slot_mapping[t] >= 0, copies
+ * k[t][h][:] into k_cache at page slot / block_size, head h, row
+ * slot % block_size (and v likewise), bit for bit.  slot < 0 skips the token
+ * (padding).  Slots >= num_blocks * block_size are not written and set
+ * PA_ERR_DEVICE_BOUNDS in the device status word.  Two tokens with the same
+ * slot in one call give an unspecified winner.
+ *   k, v          [num_tokens][num_kv_heads][head_dim] bf16, contiguous
+ *   k_cache, v_cache  pools addressed by the strides (see conventions)
+ *   slot_mapping  [num_tokens] int64
+ */
+int pa_write_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                   const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                   int head_dim, int block_size, int64_t num_blocks,
+                   int64_t stride_block, int64_t stride_head, int64_t stride_token,
+                   void *stream);
+
+/*
+ * pa_decode -- single-pass paged GQA decode (one query token per sequence).
+ * For sequence b and query head h (kv head kh = h / (num_q_heads/num_kv_heads)):
+ *   out[b][h] = softmax(sm_scale * q[b][h] . K_j) weighted sum of V_j over
+ *   j < seq_lens[b], with token j at page block_tables[b][j / block_size],
+ *   row j % block_size.  seq_lens[b] == 0 gives a zero row.
+ *   out, q        [num_seqs][num_q_heads][head_dim] bf16
+ *   block_tables  [num_seqs][max_blocks_per_seq] int32 (entries past
+ *                 ceil(seq_len / block_size) are never read)
+ *   seq_lens      [num_seqs] int32
+ * One CTA walks the whole sequence of its (b, kv head); suited to short
+ * contexts or large batches.  Allocates nothing.
+ */
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+              int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
+              int64_t stride_head, int64_t stride_token, float sm_scale, void *stream);
+
+/*
+ * Bytes of workspace pa_decode_split needs (256-byte aligned sub-buffers):
+ *   P = ceil(max_seq_len / 512) partitions
+ *   partial_out [num_seqs][num_q_heads][P][head_dim] fp32   at offset 0
+ *   partial_max [num_seqs][num_q_heads][P] fp32  (natural-log units)  next
+ *   partial_sum [num_seqs][num_q_heads][P] fp32                         next
+ * Offsets are given by pa_decode_split_workspace_offsets().
+ */
+size_t pa_decode_split_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                      int max_seq_len);
+void pa_decode_split_workspace_offsets(int num_seqs, int num_q_heads, int head_dim,
+                                       int max_seq_len, size_t *off_out, size_t *off_max,
+                                       size_t *off_sum);
+
+/*
+ * pa_decode_split -- split-KV paged GQA decode.  Same result as pa_decode.
+ * Pass 1: one CTA per (partition p, kv head, sequence) computes for its group
+ * of query heads m_p = max of the scaled scores over tokens
+ * [512 p, min(512 (p+1), L)), l_p = sum exp(s - m_p) and
+ * o_p = sum exp(s - m_p) V / l_p, into the workspace (fp32).  Partitions at or
+ * past ceil(L / 512) are neither written nor read.
+ * Pass 2 (merge): M = max_p m_p, w_p = l_p exp(m_p - M),
+ * out = sum_p w_p o_p / sum_p w_p, rounded to bf16; L == 0 gives zeros.
+ * max_seq_len must be >= every seq_lens[b]; a larger seq_len is clamped to it
+ * and flagged PA_ERR_DEVICE_BOUNDS.  workspace is caller-owned device memory
+ * of at least pa_decode_split_workspace_size() bytes, 256-byte aligned.
+ */
+int pa_decode_split(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                    int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
+                    int64_t stride_head, int64_t stride_token, float sm_scale,
+                    int max_seq_len, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/*
+ * Bytes of workspace pa_ragged_prefill needs (a device-built tile schedule).
+ */
+size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_heads,
+                                        int head_dim);
+
+/*
+ * pa_ragged_prefill -- ragged causal (or full) prefill, N requests, one launch.
+ * Request r owns query rows [qo_indptr[r], qo_indptr[r+1]) and
+ * kv_len_r = kv_indptr[r+1] - kv_indptr[r] keys.  Query row i of request r,
+ * head h, attends to keys j < kv_len_r of kv head h / (num_q_heads/num_kv_heads)
+ * and, if causal != 0, only to j <= i + (kv_len_r - qo_len_r) (bottom-right
+ * alignment: the query rows are the LAST qo_len_r positions).  A row with no
+ * visible key is written as zeros.
+ *   o, q  [total_qo_rows][num_q_heads][head_dim] bf16
+ *   Contiguous mode (block_tables == NULL): k, v are
+ *         [total_kv_rows][num_kv_heads][head_dim] bf16 and key j of request r
+ *         is row kv_indptr[r] + j; the stride arguments are ignored.
+ *   Paged mode (block_tables != NULL): k, v are the paged pools, key j of
+ *         request r is token j of block_tables[r] (as in pa_decode); the
+ *         kv_indptr values only give the lengths.
+ *   qo_indptr_h, kv_indptr_h  [batch+1] int32 HOST copies (used to size and
+ *         order the launch); qo_indptr_d, kv_indptr_d the same on the device.
+ *   workspace  >= pa_ragged_prefill_workspace_size() bytes, 256-byte aligned.
+ */
+int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
+                      const int32_t *qo_indptr_h, const int32_t *kv_indptr_h,
+                      const int32_t *qo_indptr_d, const int32_t *kv_indptr_d,
+                      const int32_t *block_tables, int max_blocks_per_seq, int block_size,
+                      int64_t num_blocks, int64_t stride_block, int64_t stride_head,
+                      int64_t stride_token, int batch, int total_qo_rows,
+                      int total_kv_rows, int num_q_heads, int num_kv_heads, int head_dim,
+                      float sm_scale, int causal, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word: *status_h receives PA_OK or the OR-ed PA_ERR_* bits recorded by the
+ * device-side guards (bit (1 << code)).  Returns PA_OK or PA_ERR_CUDA.
+ */
+int pa_get_device_status(int *status_h, void *stream);
+
+/* Thread-local description of the last error returned on this thread. */
+const char *pa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

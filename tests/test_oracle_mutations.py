@@ -1,0 +1,121 @@
+"""Planted mistakes: each mutation of a COPY of the oracle source must be caught.
+
+A plausible slip anywhere in the oracle (a dropped term, a wrong index or
+sign, a transposed operand) has to fail at least one pin, otherwise the pins
+do not really tie the oracle down.  The copies are compiled into a temporary
+directory on the CPU; the committed oracle is never modified.
+"""
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_gqa_15_gb300 import workloads as W
+from tests import brute
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "pa_oracle.c")
+
+MUTATIONS = {
+    "dropped_scale": ("        s *= scale;\n        scores[j] = s;", "        scores[j] = s;"),
+    "gqa_modulo": ("int kh = h / g; /* contiguous GQA groups */", "int kh = h % c->nkv;"),
+    "top_left_causal": ("int64_t lim = i + (kv - qo) + 1;", "int64_t lim = i + 1;"),
+    "page_row_swapped": ("(j % c->bs) * c->s_token;\n}", "(j / c->bs) * c->s_token;\n}"),
+    "merge_without_lp": ("double w = l[bh * max_parts + p] * exp(m[bh * max_parts + p] - M);",
+                         "double w = exp(m[bh * max_parts + p] - M);"),
+    "slot_div_mod_swapped": ("int64_t page = slot / bs, row = slot % bs;",
+                             "int64_t page = slot % bs, row = slot / bs;"),
+    "unnormalised_output": ("    for (int d = 0; d < hd; ++d) out[d] /= den;\n", ""),
+    "partition_unnormalised": ("for (int e = 0; e < d->hd; ++e) op[e] /= lsum;", ""),
+    "max_not_subtracted": ("double p = exp(scores[j] - mx);", "double p = exp(scores[j]);"),
+    "wrong_exp_sign": ("double w = exp(sc[j - j0] - mx);", "double w = exp(mx - sc[j - j0]);"),
+}
+
+
+def _check_decode():
+    w = W.make_decode("mut", [17, 33, 64, 100], 4, 2, 64, seed=1000, num_blocks=64)
+    t = w.tensors("cpu")
+    q, kc, vc = (W.to_bits(t[n]) for n in ("q", "k_cache", "v_cache"))
+    got = oracle.decode(q, kc, vc, w.block_tables, w.seq_lens, 2, 16, w.scale)
+    ref = brute.brute_decode(q, kc, vc, w.block_tables, w.seq_lens, 2, 16, w.scale,
+                             oracle.hnd_strides(2, 16, 64))
+    np.testing.assert_allclose(got, ref, atol=1e-12, rtol=0)
+
+
+def _check_prefill():
+    qo, kv = np.array([6, 10, 3]), np.array([6, 14, 9])
+    w = W.make_prefill("mut", qo, kv, 4, 2, 64, seed=7)
+    t = w.tensors("cpu")
+    q, k, v = (W.to_bits(t[n]) for n in ("q", "k", "v"))
+    got = oracle.prefill(q, k, v, w.qo_indptr, w.kv_indptr, 2, w.scale, causal=True)
+    ref = brute.brute_prefill_contiguous(q, k, v, w.qo_indptr, w.kv_indptr, 2, w.scale, True)
+    np.testing.assert_allclose(got, ref, atol=1e-12, rtol=0)
+
+
+def _check_split():
+    w = W.make_decode("mut", [300, 1100, 2000], 4, 2, 64, seed=13)
+    t = w.tensors("cpu")
+    q, kc, vc = (W.to_bits(t[n]) for n in ("q", "k_cache", "v_cache"))
+    strides = oracle.hnd_strides(2, 16, 64)
+    ref = brute.brute_decode(q, kc, vc, w.block_tables, w.seq_lens, 2, 16, w.scale, strides)
+    m, l, o = oracle.decode_partitions(q, kc, vc, w.block_tables, w.seq_lens, 2, 16, w.scale, 4)
+    merged = oracle.merge_partitions(m, l, o, w.seq_lens)
+    np.testing.assert_allclose(merged, ref, atol=1e-12, rtol=0)
+
+
+def _check_write():
+    rng = np.random.default_rng(3)
+    kc = np.zeros((8, 2, 16, 64), np.uint16)
+    vc = np.zeros_like(kc)
+    k = rng.integers(1, 0x7F00, size=(20, 2, 64)).astype(np.uint16)
+    v = rng.integers(1, 0x7F00, size=(20, 2, 64)).astype(np.uint16)
+    slots = rng.choice(8 * 16, size=20, replace=False).astype(np.int64)
+    oracle.write_cache(k, v, kc, vc, slots, 16)
+    for t, s in enumerate(slots):
+        np.testing.assert_array_equal(kc[s // 16, :, s % 16], k[t])
+        np.testing.assert_array_equal(vc[s // 16, :, s % 16], v[t])
+
+
+def _check_large_logits():
+    # scores of several hundred: exp() overflows unless the row max is subtracted
+    w = W.make_decode("mut", [40, 90], 2, 1, 64, seed=21)
+    t = w.tensors("cpu")
+    q, kc, vc = (W.to_bits(t[n]) for n in ("q", "k_cache", "v_cache"))
+    got = oracle.decode(q, kc, vc, w.block_tables, w.seq_lens, 1, 16, 100.0)
+    ref = brute.brute_decode(q, kc, vc, w.block_tables, w.seq_lens, 1, 16, 100.0,
+                             oracle.hnd_strides(1, 16, 64))
+    np.testing.assert_allclose(got, ref, atol=1e-12, rtol=0)
+
+
+CHECKS = [_check_decode, _check_prefill, _check_split, _check_write, _check_large_logits]
+
+
+def test_unmutated_copy_passes_every_check(tmp_path):
+    lib = tmp_path / "clean.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", SRC,
+                           "-o", str(lib), "-lm"])
+    with oracle.using_library(str(lib)):
+        for chk in CHECKS:
+            chk()
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    mutated = tmp_path / "mut.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "mut.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                           str(mutated), "-o", str(lib), "-lm"])
+    caught = []
+    with oracle.using_library(str(lib)):
+        for chk in CHECKS:
+            try:
+                chk()
+            except AssertionError:
+                caught.append(chk.__name__)
+    assert caught, f"planted mistake {name} passed every pin"
