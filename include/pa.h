@@ -139,6 +139,23 @@ int pa_decode_split(void *out, const void *q, const void *k_cache, const void *v
                     void *stream);
 
 /*
+ * The two passes of pa_decode_split as separate calls (same arguments and
+ * workspace): pa_decode_partitions writes the per-partition (m_p, l_p, o_p)
+ * into the workspace; pa_decode_merge reads them and writes out.
+ * pa_decode_split == pa_decode_partitions followed by pa_decode_merge.
+ */
+int pa_decode_partitions(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
+                         int64_t stride_head, int64_t stride_token, float sm_scale,
+                         int max_seq_len, void *workspace, size_t workspace_bytes,
+                         void *stream);
+int pa_decode_merge(void *out, const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                    int head_dim, int max_seq_len, const void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of workspace pa_ragged_prefill needs (a device-built tile schedule).
  */
 size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_heads,

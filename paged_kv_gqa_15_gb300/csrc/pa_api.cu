@@ -1,0 +1,348 @@
+// pa_api.cu -- the C ABI (include/pa.h): argument validation, workspace
+// layout, the device status word, and kernel dispatch.  No entry point here
+// allocates memory or synchronises (pa_get_device_status excepted).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "no error";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device status word (OR of 1 << PA_ERR_* bits), one per device.
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices] = {nullptr};
+
+int status_ptr(int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device %d", dev);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    *out = g_status_ptr[dev];
+    return PA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_heads(int head_dim, int num_q_heads, int num_kv_heads) {
+    if (num_q_heads <= 0 || num_kv_heads <= 0)
+        return fail(PA_ERR_INVALID, "head counts must be positive (nq=%d, nkv=%d)", num_q_heads,
+                    num_kv_heads);
+    if (num_q_heads % num_kv_heads != 0)
+        return fail(PA_ERR_INVALID, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                    num_q_heads, num_kv_heads);
+    const int g = num_q_heads / num_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return fail(PA_ERR_UNSUPPORTED, "GQA group size %d not in {1, 2, 4, 8}", g);
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", head_dim);
+    return PA_OK;
+}
+
+int check_pool(int head_dim, int block_size, int64_t num_blocks, int num_kv_heads,
+               int64_t sb, int64_t sh, int64_t st) {
+    if (block_size != 16)
+        return fail(PA_ERR_UNSUPPORTED, "block_size %d: only 16-token blocks", block_size);
+    if (num_blocks <= 0) return fail(PA_ERR_INVALID, "num_blocks %lld", (long long)num_blocks);
+    if (sb <= 0 || sh <= 0 || st <= 0 || sb % 8 || sh % 8 || st % 8)
+        return fail(PA_ERR_INVALID,
+                    "pool strides (%lld, %lld, %lld) must be positive multiples of 8 elements",
+                    (long long)sb, (long long)sh, (long long)st);
+    if (st < head_dim)
+        return fail(PA_ERR_INVALID, "token stride %lld < head_dim %d", (long long)st, head_dim);
+    (void)num_kv_heads;
+    return PA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int decode_common(pa::DecodeParams &p, void *out, const void *q, const void *k_cache,
+                  const void *v_cache, const int32_t *block_tables, const int32_t *seq_lens,
+                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int max_blocks_per_seq, int64_t num_blocks, int64_t sb, int64_t sh, int64_t st,
+                  float sm_scale) {
+    if (num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs %d", num_seqs);
+    int rc = check_heads(head_dim, num_q_heads, num_kv_heads);
+    if (rc) return rc;
+    rc = check_pool(head_dim, block_size, num_blocks, num_kv_heads, sb, sh, st);
+    if (rc) return rc;
+    if (max_blocks_per_seq <= 0)
+        return fail(PA_ERR_INVALID, "max_blocks_per_seq %d", max_blocks_per_seq);
+    if (num_seqs > 0 && (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens))
+        return fail(PA_ERR_INVALID, "null pointer argument");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID, "out, q and the KV pools must be 16-byte aligned");
+    if (!(sm_scale == sm_scale)) return fail(PA_ERR_INVALID, "sm_scale is NaN");
+    std::memset(&p, 0, sizeof p);
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.num_blocks = num_blocks;
+    p.s_block = sb;
+    p.s_head = sh;
+    p.s_token = st;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.max_blocks = max_blocks_per_seq;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    p.rows_contiguous = (st == head_dim) ? 1 : 0;
+    p.max_seq_len = max_blocks_per_seq * 16;
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_last_error(void) { return g_last_error; }
+
+int pa_get_device_status(int *status_h, void *stream) {
+    if (!status_h) return fail(PA_ERR_INVALID, "status_h is NULL");
+    int *ptr = nullptr;
+    int rc = status_ptr(&ptr);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaMemcpy(status_h, ptr, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read status");
+    e = cudaMemset(ptr, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear status");
+    return PA_OK;
+}
+
+int pa_write_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                   const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                   int head_dim, int block_size, int64_t num_blocks, int64_t stride_block,
+                   int64_t stride_head, int64_t stride_token, void *stream) {
+    if (num_tokens < 0) return fail(PA_ERR_INVALID, "num_tokens %lld", (long long)num_tokens);
+    if (num_kv_heads <= 0) return fail(PA_ERR_INVALID, "num_kv_heads %d", num_kv_heads);
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", head_dim);
+    int rc = check_pool(head_dim, block_size, num_blocks, num_kv_heads, stride_block,
+                        stride_head, stride_token);
+    if (rc) return rc;
+    if (num_tokens > 0 && (!k || !v || !k_cache || !v_cache || !slot_mapping))
+        return fail(PA_ERR_INVALID, "null pointer argument");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID, "k, v and the caches must be 16-byte aligned");
+    pa::WriteCacheParams p;
+    p.k = k;
+    p.v = v;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.slot_mapping = slot_mapping;
+    p.num_tokens = num_tokens;
+    p.num_blocks = num_blocks;
+    p.s_block = stride_block;
+    p.s_head = stride_head;
+    p.s_token = stride_token;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    rc = status_ptr(&p.status);
+    if (rc) return rc;
+    cudaError_t e = pa::launch_write_cache(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "write_cache launch");
+    return PA_OK;
+}
+
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+              int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
+              int64_t stride_head, int64_t stride_token, float sm_scale, void *stream) {
+    pa::DecodeParams p;
+    int rc = decode_common(p, out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                           num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                           num_blocks, stride_block, stride_head, stride_token, sm_scale);
+    if (rc) return rc;
+    rc = status_ptr(&p.status);
+    if (rc) return rc;
+    cudaError_t e = pa::launch_decode(p, head_dim, false, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return PA_OK;
+}
+
+void pa_decode_split_workspace_offsets(int num_seqs, int num_q_heads, int head_dim,
+                                       int max_seq_len, size_t *off_out, size_t *off_max,
+                                       size_t *off_sum) {
+    const size_t parts = max_seq_len > 0 ? (static_cast<size_t>(max_seq_len) + 511) / 512 : 0;
+    const size_t rows = static_cast<size_t>(num_seqs > 0 ? num_seqs : 0) *
+                        static_cast<size_t>(num_q_heads > 0 ? num_q_heads : 0) * parts;
+    const size_t o_bytes = round256(rows * static_cast<size_t>(head_dim > 0 ? head_dim : 0) * 4);
+    const size_t s_bytes = round256(rows * 4);
+    if (off_out) *off_out = 0;
+    if (off_max) *off_max = o_bytes;
+    if (off_sum) *off_sum = o_bytes + s_bytes;
+}
+
+size_t pa_decode_split_workspace_size(int num_seqs, int num_q_heads, int head_dim,
+                                      int max_seq_len) {
+    size_t o, m, l;
+    pa_decode_split_workspace_offsets(num_seqs, num_q_heads, head_dim, max_seq_len, &o, &m, &l);
+    return l + (l - m);  // partial_out, then partial_max and partial_sum of equal size
+}
+
+namespace {
+
+int split_setup(pa::DecodeParams &p, int num_seqs, int num_q_heads, int head_dim,
+                int max_blocks_per_seq, int max_seq_len, const void *workspace,
+                size_t workspace_bytes) {
+    if (max_seq_len < 0) return fail(PA_ERR_INVALID, "max_seq_len %d", max_seq_len);
+    if (max_blocks_per_seq > 0 && max_seq_len > max_blocks_per_seq * 16)
+        return fail(PA_ERR_INVALID, "max_seq_len %d exceeds max_blocks_per_seq * 16 = %d",
+                    max_seq_len, max_blocks_per_seq * 16);
+    const size_t need =
+        pa_decode_split_workspace_size(num_seqs, num_q_heads, head_dim, max_seq_len);
+    if (workspace_bytes < need)
+        return fail(PA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+    if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return fail(PA_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+    size_t oo, om, ol;
+    pa_decode_split_workspace_offsets(num_seqs, num_q_heads, head_dim, max_seq_len, &oo, &om,
+                                      &ol);
+    char *ws = static_cast<char *>(const_cast<void *>(workspace));
+    p.part_o = reinterpret_cast<float *>(ws + oo);
+    p.part_m = reinterpret_cast<float *>(ws + om);
+    p.part_l = reinterpret_cast<float *>(ws + ol);
+    p.max_parts = (max_seq_len + 511) / 512;
+    p.max_seq_len = max_seq_len;
+    return PA_OK;
+}
+
+}  // namespace
+
+int pa_decode_partitions(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
+                         int64_t stride_head, int64_t stride_token, float sm_scale,
+                         int max_seq_len, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+    pa::DecodeParams p;
+    // `out` is not written by this pass; q stands in for the alignment check.
+    int rc = decode_common(p, const_cast<void *>(q), q, k_cache, v_cache, block_tables,
+                           seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_blocks_per_seq, num_blocks, stride_block, stride_head,
+                           stride_token, sm_scale);
+    if (rc) return rc;
+    p.out = nullptr;
+    rc = split_setup(p, num_seqs, num_q_heads, head_dim, max_blocks_per_seq, max_seq_len,
+                     workspace, workspace_bytes);
+    if (rc) return rc;
+    if (num_seqs == 0 || p.max_parts == 0) return PA_OK;
+    rc = status_ptr(&p.status);
+    if (rc) return rc;
+    cudaError_t e = pa::launch_decode(p, head_dim, true, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode partition launch");
+    return PA_OK;
+}
+
+int pa_decode_merge(void *out, const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                    int head_dim, int max_seq_len, const void *workspace,
+                    size_t workspace_bytes, void *stream) {
+    if (num_seqs < 0 || num_q_heads <= 0)
+        return fail(PA_ERR_INVALID, "num_seqs %d, num_q_heads %d", num_seqs, num_q_heads);
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", head_dim);
+    if (num_seqs > 0 && (!out || !seq_lens)) return fail(PA_ERR_INVALID, "null pointer argument");
+    if (!aligned16(out)) return fail(PA_ERR_INVALID, "out must be 16-byte aligned");
+    pa::DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.out = out;
+    p.seq_lens = seq_lens;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    int rc = split_setup(p, num_seqs, num_q_heads, head_dim, 0, max_seq_len, workspace,
+                         workspace_bytes);
+    if (rc) return rc;
+    if (num_seqs == 0) return PA_OK;
+    rc = status_ptr(&p.status);
+    if (rc) return rc;
+    cudaError_t e = pa::launch_merge(p, head_dim, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return PA_OK;
+}
+
+int pa_decode_split(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                    int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
+                    int64_t stride_head, int64_t stride_token, float sm_scale,
+                    int max_seq_len, void *workspace, size_t workspace_bytes, void *stream) {
+    pa::DecodeParams p;
+    int rc = decode_common(p, out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                           num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                           num_blocks, stride_block, stride_head, stride_token, sm_scale);
+    if (rc) return rc;
+    rc = split_setup(p, num_seqs, num_q_heads, head_dim, max_blocks_per_seq, max_seq_len,
+                     workspace, workspace_bytes);
+    if (rc) return rc;
+    if (num_seqs == 0) return PA_OK;
+    rc = status_ptr(&p.status);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.max_parts > 0) {
+        cudaError_t e = pa::launch_decode(p, head_dim, true, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decode partition launch");
+    }
+    cudaError_t e = pa::launch_merge(p, head_dim, s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return PA_OK;
+}
+
+size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_heads,
+                                        int head_dim) {
+    (void)batch;
+    (void)total_qo_rows;
+    (void)num_q_heads;
+    (void)head_dim;
+    return 256;
+}
+
+int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
+                      const int32_t *qo_indptr_h, const int32_t *kv_indptr_h,
+                      const int32_t *qo_indptr_d, const int32_t *kv_indptr_d,
+                      const int32_t *block_tables, int max_blocks_per_seq, int block_size,
+                      int64_t num_blocks, int64_t stride_block, int64_t stride_head,
+                      int64_t stride_token, int batch, int total_qo_rows, int total_kv_rows,
+                      int num_q_heads, int num_kv_heads, int head_dim, float sm_scale,
+                      int causal, void *workspace, size_t workspace_bytes, void *stream) {
+    (void)o; (void)q; (void)k; (void)v; (void)qo_indptr_h; (void)kv_indptr_h;
+    (void)qo_indptr_d; (void)kv_indptr_d; (void)block_tables; (void)max_blocks_per_seq;
+    (void)block_size; (void)num_blocks; (void)stride_block; (void)stride_head;
+    (void)stride_token; (void)batch; (void)total_qo_rows; (void)total_kv_rows;
+    (void)num_q_heads; (void)num_kv_heads; (void)head_dim; (void)sm_scale; (void)causal;
+    (void)workspace; (void)workspace_bytes; (void)stream;
+    return fail(PA_ERR_UNSUPPORTED, "pa_ragged_prefill: not built yet");
+}
+
+}  // extern "C"

@@ -1,0 +1,45 @@
+// pa_internal.h -- launch parameter blocks and launcher declarations shared
+// between the C ABI layer (pa_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct WriteCacheParams {
+    const void *k, *v;
+    void *k_cache, *v_cache;
+    const int64_t *slot_mapping;
+    int64_t num_tokens, num_blocks;
+    int64_t s_block, s_head, s_token;
+    int num_kv_heads, head_dim, block_size;
+    int *status;
+};
+
+struct DecodeParams {
+    void *out;                    // bf16 [B][nq][hd]        (single pass)
+    const void *q;                // bf16 [B][nq][hd]
+    const void *k_cache, *v_cache;
+    const int32_t *block_tables;  // [B][max_blocks]
+    const int32_t *seq_lens;      // [B]
+    float *part_o, *part_m, *part_l;  // split partials (split pass only)
+    int64_t num_blocks;
+    int64_t s_block, s_head, s_token;
+    int num_seqs, num_q_heads, num_kv_heads, max_blocks;
+    int max_parts;                // split: partitions per (b, h) in the workspace
+    int max_seq_len;              // split: clamp for seq_lens
+    float scale_log2;             // sm_scale * log2(e)
+    int rows_contiguous;          // s_token == head_dim: one bulk copy per page
+    int *status;
+};
+
+struct PrefillParams;  // defined in pa_prefill.cu
+
+cudaError_t launch_write_cache(const WriteCacheParams &p, cudaStream_t stream);
+// Returns cudaErrorNotSupported for an unsupported (head_dim, group) pair.
+cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeParams &p, int head_dim, cudaStream_t stream);
+
+}  // namespace pa

@@ -3,11 +3,15 @@
 A plausible slip anywhere in the oracle (a dropped term, a wrong index or
 sign, a transposed operand) has to fail at least one pin, otherwise the pins
 do not really tie the oracle down.  The copies are compiled into a temporary
-directory on the CPU; the committed oracle is never modified.
+directory on the CPU and exercised in a child process (a mutated index can
+read or write out of bounds, which must not corrupt the test process); a
+failed check or a crash of the child both count as caught.  The committed
+oracle is never modified.
 """
 import math
 import os
 import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -92,13 +96,34 @@ def _check_large_logits():
 CHECKS = [_check_decode, _check_prefill, _check_split, _check_write, _check_large_logits]
 
 
+def _run_checks_in_child(lib_path):
+    """Returns (exit code, stdout) of a child running every check against lib_path."""
+    code = ("import sys; sys.path.insert(0, %r); import oracle; "
+            "from tests import test_oracle_mutations as m; "
+            "failed = []\n"
+            "with oracle.using_library(%r):\n"
+            "    for chk in m.CHECKS:\n"
+            "        try:\n"
+            "            chk()\n"
+            "        except AssertionError:\n"
+            "            failed.append(chk.__name__)\n"
+            "print('FAILED', failed); sys.exit(1 if failed else 0)")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, "-c", code % (root, lib_path)], capture_output=True,
+                         text=True, timeout=300, cwd=root)
+    return res.returncode, res.stdout + res.stderr
+
+
+def _compile(src_path, lib_path):
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                           str(src_path), "-o", str(lib_path), "-lm"])
+
+
 def test_unmutated_copy_passes_every_check(tmp_path):
     lib = tmp_path / "clean.so"
-    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", SRC,
-                           "-o", str(lib), "-lm"])
-    with oracle.using_library(str(lib)):
-        for chk in CHECKS:
-            chk()
+    _compile(SRC, lib)
+    rc, out = _run_checks_in_child(str(lib))
+    assert rc == 0, out
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
@@ -109,13 +134,6 @@ def test_planted_mistake_is_caught(tmp_path, name):
     mutated = tmp_path / "mut.c"
     mutated.write_text(src.replace(old, new))
     lib = tmp_path / "mut.so"
-    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-                           str(mutated), "-o", str(lib), "-lm"])
-    caught = []
-    with oracle.using_library(str(lib)):
-        for chk in CHECKS:
-            try:
-                chk()
-            except AssertionError:
-                caught.append(chk.__name__)
-    assert caught, f"planted mistake {name} passed every pin"
+    _compile(mutated, lib)
+    rc, out = _run_checks_in_child(str(lib))
+    assert rc != 0, f"planted mistake {name} passed every pin:\n{out}"
