@@ -1,0 +1,557 @@
+"""Benchmark of the paged-KV GQA attention hot path on GB300.
+
+One step = one pass of the hot path over one batch of synthetic input:
+  pa_write_cache (the batch's new tokens) -> pa_decode_partitions -> pa_decode_merge
+on the Llama-3-8B-shaped decode workload (64 sequences, 32 q / 8 kv heads,
+head_dim 128, 16-token pages, seq_lens U[512, 4096], shuffled block tables).
+The metric is decode KV-bytes GB/s (K and V of every visible token per step).
+The other workloads (long-context split decode, tiny decode, ragged prefill,
+chunked paged prefill) are measured in the same run and reported under
+"workloads", each with its own roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (no
+data-path collective); the step time is the max over ranks and `value` is the
+bytes all ranks processed divided by it.  `--impl reference` times the fp64 CPU
+oracle on a bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV HBM GB/s & ragged prefill TFLOP/s, as fraction of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (read + write) per launch from ncu captures, keyed by kernel, valid only
+# for the source file hash they were measured on (otherwise reported as null).
+TRAFFIC = {}
+
+
+# ---------------------------------------------------------------------------------------
+# host-side helpers (also exercised by the CPU tests)
+# ---------------------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, \
+            "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_gqa_15_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, src_files, launches_bytes=None):
+    rec = TRAFFIC.get(kernel)
+    if not rec or rec.get("src") != source_hash(*src_files):
+        return None
+    return rec["bytes_per_launch"]
+
+
+def roofline(bound, achieved, peak, unit, traffic, peak_kind):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4) if peak else None, "traffic": traffic,
+            "peak_source": peak_kind}
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a float over all ranks (identity without torch.distributed)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, device=None) -> float:
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_step_local: float, ms_per_step_local: float, device=None):
+    """(whole-job units per second, max-over-ranks ms per step)."""
+    ms = reduce_max(ms_per_step_local, device)
+    units = reduce_sum(units_per_step_local, device)
+    return units / (ms / 1e3), ms
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None, interval_ms=50):
+        self.gpu_id = gpu_id
+        self.interval_ms = interval_ms
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               f"--loop-ms={self.interval_ms}"]
+        if self.gpu_id:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(self.interval_ms / 1000.0 * 2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        return self.summary(self.lines)
+
+    @staticmethod
+    def summary(lines):
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------------------
+# GPU arms
+# ---------------------------------------------------------------------------------------
+
+def decode_setup(w, dev, split=True):
+    import paged_kv_gqa_15_gb300 as pa
+    t = w.tensors(dev)
+    s = {"t": t,
+         "bt": torch.from_numpy(w.block_tables).to(dev),
+         "sl": torch.from_numpy(w.seq_lens).to(dev),
+         "out": torch.empty_like(t["q"])}
+    if w.new_token_write:
+        s["slots"] = torch.from_numpy(w.slot_mapping).to(dev)
+    s["ws"] = pa.alloc_workspace(pa.decode_split_workspace_size(
+        w.batch, w.num_q_heads, w.head_dim, max(w.max_seq_len, 1)), dev)
+    return s
+
+
+def decode_step(w, s, stream, evs=None):
+    """One hot-path step; records an event after each kernel when evs is a list."""
+    import paged_kv_gqa_15_gb300 as pa
+    t = s["t"]
+    n = 0
+    if evs is not None:
+        evs.append(_ev(stream))
+    if w.new_token_write:
+        pa.pa_write_cache(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], s["slots"],
+                          stream=stream)
+        n += 1
+        if evs is not None:
+            evs.append(_ev(stream))
+    L = max(w.max_seq_len, 1)
+    pa.pa_decode_partitions(t["q"], t["k_cache"], t["v_cache"], s["bt"], s["sl"], w.scale, L,
+                            s["ws"], stream=stream)
+    if evs is not None:
+        evs.append(_ev(stream))
+    pa.pa_decode_merge(s["out"], s["sl"], L, s["ws"], stream=stream)
+    if evs is not None:
+        evs.append(_ev(stream))
+    return n + 2
+
+
+def _ev(stream):
+    e = torch.cuda.Event(enable_timing=True)
+    e.record(stream)
+    return e
+
+
+def time_steps(step, steps, warmup, stream, device, labels):
+    """Warm up, then time exactly `steps` steps with CUDA events on `stream`.
+    Returns (ms per step, {label: avg ms}, launches)."""
+    import torch.distributed as dist
+    for _ in range(warmup):
+        step(None)
+    torch.cuda.synchronize()
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+    torch.cuda.synchronize()
+    all_evs = []
+    launches = 0
+    start = _ev(stream)
+    for _ in range(steps):
+        evs = []
+        launches += step(evs)
+        all_evs.append(evs)
+    end = _ev(stream)
+    torch.cuda.synchronize()
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+    ms = start.elapsed_time(end) / steps
+    per = {l: 0.0 for l in labels}
+    for evs in all_evs:
+        for i, l in enumerate(labels):
+            per[l] += evs[i].elapsed_time(evs[i + 1])
+    per = {l: v / steps for l, v in per.items()}
+    return ms, per, launches
+
+
+def bench_decode(w, steps, warmup, dev, stream, peaks, peak_kind):
+    s = decode_setup(w, dev)
+    labels = (["write_cache"] if w.new_token_write else []) + ["decode_partitions",
+                                                               "decode_merge"]
+
+    def step(evs):
+        return decode_step(w, s, stream, evs)
+
+    ms, per, launches = time_steps(step, steps, warmup, stream, dev, labels)
+    kv = w.kv_bytes()
+    value, ms_max = aggregate_throughput(kv, ms, dev)
+    kern_ms = per["decode_partitions"]
+    src = ("pa_decode.cu", "pa_device.cuh")
+    res = {
+        "value": value / 1e9, "unit": "GB/s", "ms_per_step": ms_max,
+        "kv_bytes_per_step": kv, "launches": launches,
+        "kernels_ms": {k: round(v, 5) for k, v in per.items()},
+        "roofline": roofline("hbm", kv / (kern_ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s",
+                             traffic_for("decode_partitions:" + w.name, src), peak_kind),
+        "roofline_nominal_frac": round(kv / (kern_ms / 1e3) / 1e9 / 8000.0, 4),
+    }
+    return res, s
+
+
+def bench_decode_e2e(w, s, steps, warmup, dev, stream):
+    """Same step through the public calls with pinned host inputs copied in and the
+    output copied out inside the timed region."""
+    t = s["t"]
+    host = {"q": t["q"].cpu().pin_memory(),
+            "bt": s["bt"].cpu().pin_memory(), "sl": s["sl"].cpu().pin_memory()}
+    if w.new_token_write:
+        host.update({"k_new": t["k_new"].cpu().pin_memory(),
+                     "v_new": t["v_new"].cpu().pin_memory(),
+                     "slots": s["slots"].cpu().pin_memory()})
+    out_h = torch.empty(s["out"].shape, dtype=s["out"].dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step(evs):
+        with torch.cuda.stream(stream):
+            t["q"].copy_(host["q"], non_blocking=True)
+            s["bt"].copy_(host["bt"], non_blocking=True)
+            s["sl"].copy_(host["sl"], non_blocking=True)
+            if w.new_token_write:
+                t["k_new"].copy_(host["k_new"], non_blocking=True)
+                t["v_new"].copy_(host["v_new"], non_blocking=True)
+                s["slots"].copy_(host["slots"], non_blocking=True)
+        n = decode_step(w, s, stream, None)
+        with torch.cuda.stream(stream):
+            out_h.copy_(s["out"], non_blocking=True)
+        if evs is not None:
+            evs.extend([_ev(stream), _ev(stream)])
+        return n
+
+    ms, _, _ = time_steps(step, steps, warmup, stream, dev, ["step"])
+    value, ms_max = aggregate_throughput(w.kv_bytes(), ms, dev)
+    return {"value": round(value / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms_max, 5),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def bench_prefill(w, steps, warmup, dev, stream, peaks, peak_kind):
+    import paged_kv_gqa_15_gb300 as pa
+    t = w.tensors(dev)
+    qo_d = torch.from_numpy(w.qo_indptr).to(dev)
+    kv_d = torch.from_numpy(w.kv_indptr).to(dev)
+    o = torch.empty_like(t["q"])
+    ws = pa.alloc_workspace(pa.ragged_prefill_workspace_size(w.batch, w.total_qo, w.num_q_heads,
+                                                             w.head_dim), dev)
+    bt = torch.from_numpy(w.block_tables).to(dev) if w.paged else None
+    slots = torch.from_numpy(w.chunk_slot_mapping).to(dev) if w.chunk_write else None
+    labels = (["write_cache"] if w.chunk_write else []) + ["ragged_prefill"]
+
+    def step(evs):
+        n = 0
+        if evs is not None:
+            evs.append(_ev(stream))
+        if w.chunk_write:
+            pa.pa_write_cache(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], slots,
+                              stream=stream)
+            n += 1
+            if evs is not None:
+                evs.append(_ev(stream))
+        k = t["k_cache"] if w.paged else t["k"]
+        v = t["v_cache"] if w.paged else t["v"]
+        pa.pa_ragged_prefill(o, t["q"], k, v, w.qo_indptr, w.kv_indptr, qo_d, kv_d, w.scale,
+                             causal=w.causal, block_tables=bt, workspace=ws, stream=stream)
+        if evs is not None:
+            evs.append(_ev(stream))
+        return n + 1
+
+    ms, per, launches = time_steps(step, steps, warmup, stream, dev, labels)
+    flops = w.flops()
+    value, ms_max = aggregate_throughput(flops, ms, dev)
+    kern_ms = per["ragged_prefill"]
+    achieved = flops / (kern_ms / 1e3) / 1e12
+    return {"value": value / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_max,
+            "flops_per_step": flops, "launches": launches,
+            "kernels_ms": {k: round(v, 5) for k, v in per.items()},
+            "roofline": roofline("tensor", achieved, peaks["bf16_tflops"], "TFLOP/s",
+                                 traffic_for("ragged_prefill:" + w.name,
+                                             ("pa_prefill.cu", "pa_device.cuh")), peak_kind),
+            "roofline_nominal_frac": round(achieved / 2250.0, 4)}
+
+
+# ---------------------------------------------------------------------------------------
+# oracle (CPU) arm
+# ---------------------------------------------------------------------------------------
+
+def oracle_decode_time(w, t_host, seqs, nthreads):
+    """Runs the fp64 oracle on the given sequences; returns (seconds, KV bytes)."""
+    import oracle
+    q, kc, vc = t_host
+    seqs = np.asarray(seqs)
+    t0 = time.perf_counter()
+    oracle.decode(q[seqs], kc, vc, w.block_tables[seqs], w.seq_lens[seqs], w.num_kv_heads,
+                  w.block_size, w.scale, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    kv = int(w.seq_lens[seqs].astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 4
+    return dt, kv
+
+
+def oracle_decode_sample(w, t_host, target_s=15.0, nthreads=None):
+    """Times the fp64 oracle on the first n sequences of the workload, n chosen so the
+    run takes about target_s seconds.  Returns (GB/s, seconds, n, threads)."""
+    import oracle
+    nthreads = nthreads or oracle.default_threads()
+    one, _ = oracle_decode_time(w, t_host, [0], nthreads)
+    n = int(max(1, min(w.batch, math.floor(target_s / max(one, 1e-4)))))
+    dt, kv = oracle_decode_time(w, t_host, np.arange(n), nthreads)
+    return kv / dt / 1e9, dt, n, nthreads
+
+
+def host_decode_inputs(w, t):
+    from paged_kv_gqa_15_gb300 import workloads as W
+    return W.to_bits(t["q"]), W.to_bits(t["k_cache"]), W.to_bits(t["v_cache"])
+
+
+def run_reference(args, w, rank):
+    """The oracle as the reference arm: each step is a bounded sample (n of the
+    workload's sequences, cycling through the batch) sized so that the whole
+    --warmup + --steps run takes about 90 s of host time."""
+    if rank != 0:
+        return None
+    import oracle
+    from paged_kv_gqa_15_gb300 import workloads as W
+    t = w.tensors("cpu")
+    host = (W.to_bits(t["q"]), W.to_bits(t["k_cache"]), W.to_bits(t["v_cache"]))
+    th = oracle.default_threads()
+    per_step = 90.0 / max(args.steps + args.warmup, 1)
+    one, _ = oracle_decode_time(w, host, [0], th)
+    n = int(max(1, min(w.batch, math.floor(per_step / max(one, 1e-4)))))
+    cursor = 0
+
+    def next_seqs():
+        nonlocal cursor
+        seqs = [(cursor + i) % w.batch for i in range(n)]
+        cursor = (cursor + n) % w.batch
+        return seqs
+
+    for _ in range(args.warmup):
+        oracle_decode_time(w, host, next_seqs(), th)
+    tot_s, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, kv = oracle_decode_time(w, host, next_seqs(), th)
+        tot_s += dt
+        tot_b += kv
+    value = tot_b / tot_s / 1e9
+    sample = (f"fp64 oracle decode of {n} of the {w.batch} sequences per step (all "
+              f"{w.num_q_heads} heads, cycling through the batch), {tot_s:.1f} s over "
+              f"{args.steps} steps")
+    return {"metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_s / max(args.steps, 1) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": th,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def workload_config(w):
+    from paged_kv_gqa_15_gb300 import workloads as W
+    if isinstance(w, W.DecodeWorkload):
+        return {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                "block_size": w.block_size,
+                "seq_lens": f"U[{int(w.seq_lens.min())},{int(w.seq_lens.max())}] seed {w.seed}",
+                "num_blocks": w.num_blocks, "kv_bytes_per_step": w.kv_bytes(),
+                "l2": "inputs larger than L2 (KV pool %.0f MB > 129 MB); no flush" % (
+                    2 * w.num_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2 / 1e6)}
+    return {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "causal": w.causal,
+            "paged": w.paged, "total_qo": w.total_qo, "total_kv": w.total_kv,
+            "flops_per_step": w.flops()}
+
+
+# ---------------------------------------------------------------------------------------
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b_decode")
+    ap.add_argument("--extra", default="long_context_decode,tiny_decode,ragged_prefill,"
+                                       "chunked_paged_prefill",
+                    help="other workloads measured in the same run (N=1 only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    from paged_kv_gqa_15_gb300 import workloads as W
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = W.WORKLOADS[args.workload]()
+
+    if args.impl == "reference":
+        res = run_reference(args, w, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+
+    import __graft_entry__
+    import paged_kv_gqa_15_gb300 as pa
+    if not os.path.exists(pa.LIB_PATH):
+        __graft_entry__.build_library()
+    pa.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.Stream(device=dev)
+    peaks, peak_kind = load_peaks()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    res, state = bench_decode(w, args.steps, args.warmup, dev, stream, peaks, peak_kind)
+    clk_main = clocks.stop()
+    e2e = bench_decode_e2e(w, state, args.steps, args.warmup, dev, stream)
+    status = pa.device_status(stream)
+    clocks_all = ClockSampler(uuid)
+    clocks_all.start()
+
+    extra = {}
+    if world == 1 and args.extra:
+        for name in [x for x in args.extra.split(",") if x and x != args.workload]:
+            wx = W.WORKLOADS[name]()
+            try:
+                if isinstance(wx, W.DecodeWorkload):
+                    steps = max(3, min(args.steps, 50)) if wx.kv_bytes() > 1e9 else args.steps
+                    r, _ = bench_decode(wx, steps, args.warmup, dev, stream, peaks, peak_kind)
+                else:
+                    r = bench_prefill(wx, max(3, min(args.steps, 50)), args.warmup, dev, stream,
+                                      peaks, peak_kind)
+                r["config"] = workload_config(wx)
+                extra[name] = r
+            except pa.PaError as e:
+                extra[name] = {"unavailable": str(e)}
+            torch.cuda.empty_cache()
+        status |= pa.device_status(stream)
+    clk_all = clocks_all.stop()
+    clk = dict(clk_main)
+    clk["extra_workloads"] = clk_all
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t = state["t"]
+        host = host_decode_inputs(w, t)
+        gbs, dt, n, th = oracle_decode_sample(w, host, target_s=15.0)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": th, "kind": "oracle",
+               "sample": f"fp64 oracle decode of {n} of {w.batch} sequences (all "
+                         f"{w.num_q_heads} heads, {dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(res["value"], 3), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(res["ms_per_step"], 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
+            "data": "synthetic", "config": workload_config(w),
+            "roofline": res["roofline"], "roofline_nominal_frac": res["roofline_nominal_frac"],
+            "kernels_ms": res["kernels_ms"], "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": res["launches"], "clocks": clk, "device_status": status,
+            "workloads": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

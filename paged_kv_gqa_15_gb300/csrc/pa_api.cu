@@ -321,11 +321,11 @@ int pa_decode_split(void *out, const void *q, const void *k_cache, const void *v
 
 size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_heads,
                                         int head_dim) {
-    (void)batch;
-    (void)total_qo_rows;
     (void)num_q_heads;
     (void)head_dim;
-    return 256;
+    const size_t tiles = static_cast<size_t>(total_qo_rows > 0 ? total_qo_rows : 0) / 128 +
+                         static_cast<size_t>(batch > 0 ? batch : 0) + 1;
+    return round256(tiles * 8);
 }
 
 int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
@@ -336,13 +336,88 @@ int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
                       int64_t stride_token, int batch, int total_qo_rows, int total_kv_rows,
                       int num_q_heads, int num_kv_heads, int head_dim, float sm_scale,
                       int causal, void *workspace, size_t workspace_bytes, void *stream) {
-    (void)o; (void)q; (void)k; (void)v; (void)qo_indptr_h; (void)kv_indptr_h;
-    (void)qo_indptr_d; (void)kv_indptr_d; (void)block_tables; (void)max_blocks_per_seq;
-    (void)block_size; (void)num_blocks; (void)stride_block; (void)stride_head;
-    (void)stride_token; (void)batch; (void)total_qo_rows; (void)total_kv_rows;
-    (void)num_q_heads; (void)num_kv_heads; (void)head_dim; (void)sm_scale; (void)causal;
-    (void)workspace; (void)workspace_bytes; (void)stream;
-    return fail(PA_ERR_UNSUPPORTED, "pa_ragged_prefill: not built yet");
+    if (batch < 0 || total_qo_rows < 0 || total_kv_rows < 0)
+        return fail(PA_ERR_INVALID, "negative size (batch %d, qo %d, kv %d)", batch,
+                    total_qo_rows, total_kv_rows);
+    int rc = check_heads(head_dim, num_q_heads, num_kv_heads);
+    if (rc) return rc;
+    if (batch == 0) return PA_OK;
+    if (!qo_indptr_h || !kv_indptr_h || !qo_indptr_d || !kv_indptr_d)
+        return fail(PA_ERR_INVALID, "null indptr");
+    if (!(sm_scale == sm_scale)) return fail(PA_ERR_INVALID, "sm_scale is NaN");
+    const bool paged = block_tables != nullptr;
+    if (paged) {
+        rc = check_pool(head_dim, block_size, num_blocks, num_kv_heads, stride_block,
+                        stride_head, stride_token);
+        if (rc) return rc;
+        if (max_blocks_per_seq <= 0)
+            return fail(PA_ERR_INVALID, "max_blocks_per_seq %d", max_blocks_per_seq);
+        if (num_blocks >= (int64_t(1) << 31) - 1)
+            return fail(PA_ERR_UNSUPPORTED, "num_blocks %lld too large", (long long)num_blocks);
+    }
+    if (qo_indptr_h[0] != 0 || kv_indptr_h[0] != 0)
+        return fail(PA_ERR_INVALID, "indptr must start at 0");
+    int64_t n_tiles = 0;
+    for (int r = 0; r < batch; ++r) {
+        const int qo = qo_indptr_h[r + 1] - qo_indptr_h[r];
+        const int kv = kv_indptr_h[r + 1] - kv_indptr_h[r];
+        if (qo < 0 || kv < 0) return fail(PA_ERR_INVALID, "indptr not monotone at request %d", r);
+        if (paged && kv > max_blocks_per_seq * 16)
+            return fail(PA_ERR_INVALID, "request %d: %d keys exceed its block table (%d pages)", r,
+                        kv, max_blocks_per_seq);
+        n_tiles += (qo + 127) / 128;
+    }
+    if (qo_indptr_h[batch] != total_qo_rows)
+        return fail(PA_ERR_INVALID, "qo_indptr[batch] %d != total_qo_rows %d", qo_indptr_h[batch],
+                    total_qo_rows);
+    if (!paged && kv_indptr_h[batch] != total_kv_rows)
+        return fail(PA_ERR_INVALID, "kv_indptr[batch] %d != total_kv_rows %d", kv_indptr_h[batch],
+                    total_kv_rows);
+    if (n_tiles > 65535)
+        return fail(PA_ERR_UNSUPPORTED, "%lld query tiles exceed one launch", (long long)n_tiles);
+    if (total_qo_rows == 0) return PA_OK;
+    if (!o || !q || !k || !v) return fail(PA_ERR_INVALID, "null pointer argument");
+    if (!aligned16(o) || !aligned16(q) || !aligned16(k) || !aligned16(v))
+        return fail(PA_ERR_INVALID, "o, q, k and v must be 16-byte aligned");
+    const size_t need =
+        pa_ragged_prefill_workspace_size(batch, total_qo_rows, num_q_heads, head_dim);
+    if (workspace_bytes < need)
+        return fail(PA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(PA_ERR_WORKSPACE, "workspace must be non-null and 256-byte aligned");
+
+    pa::PrefillParams p;
+    std::memset(&p, 0, sizeof p);
+    p.o = o;
+    p.qo_indptr = qo_indptr_d;
+    p.kv_indptr = kv_indptr_d;
+    p.block_tables = block_tables;
+    p.tiles = static_cast<const int2 *>(workspace);
+    p.num_blocks = paged ? num_blocks : 0;
+    p.batch = batch;
+    p.nq = num_q_heads;
+    p.nkv = num_kv_heads;
+    p.max_blocks = paged ? max_blocks_per_seq : 0;
+    p.n_tiles = static_cast<int>(n_tiles);
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;
+    rc = status_ptr(&p.status);
+    if (rc) return rc;
+    pa::PrefillLaunch L;
+    L.q = q;
+    L.k = k;
+    L.v = v;
+    L.total_qo = total_qo_rows;
+    L.total_kv = total_kv_rows;
+    L.s_block = stride_block;
+    L.s_head = stride_head;
+    L.s_token = stride_token;
+    L.head_dim = head_dim;
+    cudaError_t e = pa::launch_prefill(p, L, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue)
+        return fail(PA_ERR_CUDA, "tensor map encoding failed (cuTensorMapEncodeTiled)");
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return PA_OK;
 }
 
 }  // extern "C"

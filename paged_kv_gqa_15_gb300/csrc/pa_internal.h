@@ -2,6 +2,7 @@
 // between the C ABI layer (pa_api.cu) and the kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -35,11 +36,31 @@ struct DecodeParams {
     int *status;
 };
 
-struct PrefillParams;  // defined in pa_prefill.cu
+struct PrefillParams {
+    CUtensorMap tm_q;   // q [total_qo][nq][hd] as (hd, nq, rows), 128-row boxes
+    CUtensorMap tm_k;   // ragged: (hd, nkv, rows); paged: (hd, 16, nkv, blocks)
+    CUtensorMap tm_v;
+    void *o;
+    const int32_t *qo_indptr, *kv_indptr;  // device [batch + 1]
+    const int32_t *block_tables;           // paged mode, else nullptr
+    const int2 *tiles;                     // (request, q tile), heaviest first
+    int64_t num_blocks;
+    int batch, nq, nkv, max_blocks, n_tiles, causal;
+    float scale_log2;
+    int *status;
+};
+
+struct PrefillLaunch {
+    const void *q, *k, *v;
+    int64_t total_qo, total_kv;
+    int64_t s_block, s_head, s_token;
+    int head_dim;
+};
 
 cudaError_t launch_write_cache(const WriteCacheParams &p, cudaStream_t stream);
 // Returns cudaErrorNotSupported for an unsupported (head_dim, group) pair.
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams &p, int head_dim, cudaStream_t stream);
+cudaError_t launch_prefill(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream);
 
 }  // namespace pa

@@ -1,0 +1,555 @@
+// pa_prefill.cu -- ragged (varlen) causal prefill on the Blackwell tensor cores.
+//
+// What it computes ("spark_runtime/flashinfer.rs", ragged_prefill_bf16_hd256
+// and its CPU reference; "paged_attn.py", _forward_prefix_pytorch): request r
+// owns query rows [qo_indptr[r], qo_indptr[r+1]) and kv_len keys; query row i,
+// head h attends to keys j < kv_len of kv head h / g, and under the causal mask
+// only to j <= i + (kv_len - qo_len).  Keys come from contiguous rows
+// kv_indptr[r] + j (ragged mode) or from token j of block_tables[r] (paged
+// mode, 16-token pages).
+//
+// GB300 design (FlashAttention-style, not the pages' SM80 design):
+//  * CTA = one (request, 128-row query tile, query head); 6 warps:
+//      warp 0   TMA producer: Q once, then K_j / V_j tiles (128-byte swizzle)
+//               into a 2-stage ring; paged mode issues one box per 16-token page
+//      warp 1   TMEM allocator + single-thread tcgen05.mma issuer:
+//               S_j = Q K_j^T (M=128, N=BN, K=head_dim) into TMEM buffer j%2,
+//               then O += P_{j-1} V_{j-1} with P read straight from TMEM
+//      warps 2-5  softmax: one query row per thread, read S from TMEM, mask,
+//               exp2, write P (bf16) over S in TMEM; epilogue O / l -> bf16
+//  * Online softmax with lazy rescaling: O is rescaled (in TMEM) only when a
+//    row max grows by more than 2^8, so the correction is rare; the final
+//    normalisation uses the same running max, which keeps the result exact.
+//  * Causal tile skipping: a query tile stops at the last key tile any of its
+//    rows can see; per-element masking only on tiles that cross the diagonal
+//    or the end of the keys.
+//  * A one-CTA prologue kernel sorts the (request, q-tile) work items by their
+//    number of key tiles, heaviest first, into the caller's workspace.
+//  * Every mbarrier wait is bounded (PA_ERR_TIMEOUT instead of a hang).
+#include <cuda.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr int kBM = 128;              // query rows per tile (MMA M)
+constexpr int kThreads = 192;         // 6 warps
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;        // S / P buffers at columns 0 and 128
+constexpr uint32_t kTmemO = 256;      // O accumulator at columns 256 .. 256 + head_dim
+constexpr int kSchedBuckets = 2048;
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+template <int HD, int BN>
+struct PrefillCfg {
+    static constexpr int QCH = HD / 64;                       // 128-byte column chunks
+    static constexpr uint32_t Q_BYTES = QCH * kBM * 128;
+    static constexpr uint32_t KV_CHUNK = BN * 128;            // one chunk of a K / V tile
+    static constexpr uint32_t KV_BYTES = QCH * KV_CHUNK;
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
+    static constexpr uint32_t SMEM_USED = OFF_BAR + 256;
+    // + alignment slack; at least ~116 KB so that one CTA (and its 512 TMEM
+    // columns) owns an SM
+    static constexpr uint32_t SMEM = (SMEM_USED + 1024 > 118 * 1024) ? SMEM_USED + 1024 : 118 * 1024;
+    static_assert(HD % 64 == 0 && BN % 16 == 0 && BN <= 128, "tile shape");
+    static_assert(kTmemO + HD <= kTmemCols, "TMEM budget");
+};
+
+// Number of key tiles a query tile needs (its work), bottom-right causal.
+__device__ __forceinline__ int key_tiles(int q0, int qo_len, int kv_len, int causal, int bn) {
+    int kv_end = kv_len;
+    if (causal) kv_end = min(kv_len, max(0, q0 + kBM + (kv_len - qo_len)));
+    return (kv_end + bn - 1) / bn;
+}
+
+// Heaviest-first order of the (request, query tile) work items.
+__global__ void __launch_bounds__(1024) prefill_schedule_kernel(
+    const int32_t *qo_indptr, const int32_t *kv_indptr, int batch, int causal, int bn,
+    int n_tiles, int2 *tiles, int *status) {
+    __shared__ int hist[kSchedBuckets];
+    __shared__ int total_sh;
+    const int tid = threadIdx.x;
+    for (int i = tid; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
+    if (tid == 0) total_sh = 0;
+    __syncthreads();
+    for (int r = tid; r < batch; r += blockDim.x) {
+        const int qo_len = qo_indptr[r + 1] - qo_indptr[r];
+        const int kv_len = kv_indptr[r + 1] - kv_indptr[r];
+        const int nt = (max(qo_len, 0) + kBM - 1) / kBM;
+        for (int t = 0; t < nt; ++t) {
+            const int key = min(key_tiles(t * kBM, qo_len, kv_len, causal, bn), kSchedBuckets - 1);
+            atomicAdd(&hist[kSchedBuckets - 1 - key], 1);
+        }
+        atomicAdd(&total_sh, nt);
+    }
+    __syncthreads();
+    if (tid < 32) {  // exclusive scan of the histogram by one warp
+        constexpr int PER = kSchedBuckets / 32;
+        int local = 0;
+        for (int i = 0; i < PER; ++i) local += hist[tid * PER + i];
+        int incl = local;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(kFullMask, incl, off);
+            if (tid >= off) incl += v;
+        }
+        int run = incl - local;
+        for (int i = 0; i < PER; ++i) {
+            const int c = hist[tid * PER + i];
+            hist[tid * PER + i] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    const int total = total_sh;
+    if (tid == 0 && total != n_tiles) atomicOr(status, kStatusBounds);
+    for (int r = tid; r < batch; r += blockDim.x) {
+        const int qo_len = qo_indptr[r + 1] - qo_indptr[r];
+        const int kv_len = kv_indptr[r + 1] - kv_indptr[r];
+        const int nt = (max(qo_len, 0) + kBM - 1) / kBM;
+        for (int t = 0; t < nt; ++t) {
+            const int key = min(key_tiles(t * kBM, qo_len, kv_len, causal, bn), kSchedBuckets - 1);
+            const int pos = atomicAdd(&hist[kSchedBuckets - 1 - key], 1);
+            if (pos < n_tiles) tiles[pos] = make_int2(r, t);
+        }
+    }
+    for (int i = total + tid; i < n_tiles; i += blockDim.x) tiles[i] = make_int2(-1, -1);
+}
+
+template <int HD, int BN, bool PAGED>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+    using C = PrefillCfg<HD, BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *q_full = bars + 0;
+    uint64_t *k_full = bars + 1;   // [2]
+    uint64_t *k_empty = bars + 3;  // [2]
+    uint64_t *v_full = bars + 5;   // [2]
+    uint64_t *v_empty = bars + 7;  // [2]
+    uint64_t *s_full = bars + 9;   // [2]
+    uint64_t *p_full = bars + 11;  // [2]
+    uint64_t *o_done = bars + 13;  // one phase per P.V
+    uint64_t *drain = bars + 14;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 16);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int h = blockIdx.x;
+    const int2 tile = p.tiles[blockIdx.y];
+    const int r = tile.x;
+    const bool tile_ok = r >= 0 && r < p.batch;
+    int qo_start = 0, qo_len = 0, kv_start = 0, kv_len = 0;
+    if (tile_ok) {
+        qo_start = p.qo_indptr[r];
+        qo_len = p.qo_indptr[r + 1] - qo_start;
+        kv_start = p.kv_indptr[r];
+        kv_len = p.kv_indptr[r + 1] - kv_start;
+        if (PAGED && kv_len > p.max_blocks * kBlockSize) {
+            if (threadIdx.x == 0) atomicOr(p.status, kStatusBounds);
+            kv_len = p.max_blocks * kBlockSize;
+        }
+    }
+    const int q0 = tile_ok ? tile.y * kBM : 0;
+    const bool work = tile_ok && q0 < qo_len;
+    const int off = kv_len - qo_len;
+    const int kh = h / (p.nq / p.nkv);
+    const int n_kv = work ? key_tiles(q0, qo_len, kv_len, p.causal, BN) : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_full[s], 128);
+        }
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------- TMA producer -------------------------------
+        if (n_kv > 0) {
+            if (lane == 0) {
+                prefetch_tensormap(&p.tm_q);
+                prefetch_tensormap(&p.tm_k);
+                prefetch_tensormap(&p.tm_v);
+                mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+                for (int c = 0; c < C::QCH; ++c)
+                    tma_load_3d(smem + C::OFF_Q + c * kBM * 128, &p.tm_q, c * 64, h, qo_start + q0,
+                                q_full);
+            }
+            const int pages_seq = (kv_len + kBlockSize - 1) / kBlockSize;
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = ((j >> 1) & 1) ^ 1u;
+                int page = 0;
+                if constexpr (PAGED) {
+                    const int pidx = j * (BN / kBlockSize) + lane;
+                    const bool in_seq = lane < BN / kBlockSize && pidx < pages_seq;
+                    page = in_seq ? p.block_tables[static_cast<int64_t>(r) * p.max_blocks + pidx]
+                                  : -1;
+                    const bool bad = in_seq && (page < 0 || page >= p.num_blocks);
+                    if (__any_sync(kFullMask, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
+                    // pages past the sequence (or bad ids) read as zeros: out-of-range box
+                    if (!in_seq || bad) page = static_cast<int>(p.num_blocks);
+                }
+                for (int kv = 0; kv < 2; ++kv) {
+                    uint64_t *full = kv ? &v_full[s] : &k_full[s];
+                    uint64_t *empty = kv ? &v_empty[s] : &k_empty[s];
+                    const CUtensorMap *tm = kv ? &p.tm_v : &p.tm_k;
+                    uint8_t *dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::KV_BYTES;
+                    int stop = 0;
+                    if (lane == 0) {
+                        if (!mbar_wait(empty, ph, p.status, abort_flag)) {
+                            stop = 1;
+                        } else {
+                            mbar_arrive_expect_tx(full, C::KV_BYTES);
+                            if constexpr (!PAGED) {
+                                for (int c = 0; c < C::QCH; ++c)
+                                    tma_load_3d(dst + c * C::KV_CHUNK, tm, c * 64, kh,
+                                                kv_start + j * BN, full);
+                            }
+                        }
+                    }
+                    stop = __shfl_sync(kFullMask, stop, 0);
+                    if (stop) break;
+                    if constexpr (PAGED) {
+#pragma unroll
+                        for (int i = 0; i < BN / kBlockSize; ++i) {
+                            const int pg = __shfl_sync(kFullMask, page, i);
+                            if (lane == 0) {
+                                for (int c = 0; c < C::QCH; ++c)
+                                    tma_load_4d(dst + c * C::KV_CHUNK + i * kBlockSize * 128, tm,
+                                                c * 64, 0, kh, pg, full);
+                            }
+                        }
+                    }
+                }
+                if (*abort_flag) break;
+            }
+        }
+    } else if (warp == 1) {
+        // -------------------------------- MMA issuer --------------------------------
+        if (n_kv > 0 && lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, HD, false, true);
+            const uint32_t q_base = smem_addr(smem + C::OFF_Q);
+            bool ok = mbar_wait(q_full, 0, p.status, abort_flag);
+            tc_fence_after_sync();
+            auto issue_pv = [&](int i) {
+                const int s = i & 1;
+                const uint32_t ph = (i >> 1) & 1;
+                if (!ok) return;
+                ok = mbar_wait(&p_full[s], ph, p.status, abort_flag) &&
+                     mbar_wait(&v_full[s], ph, p.status, abort_flag);
+                if (!ok) return;
+                tc_fence_after_sync();
+                const uint32_t v_base = smem_addr(smem + C::OFF_V + s * C::KV_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t bdesc =
+                        smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
+                    mma_bf16_ts(tmem + kTmemO, tmem + kTmemS + s * 128 + kk * 8, bdesc, idesc_o,
+                                (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(&v_empty[s]);
+                tc_commit(o_done);
+            };
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1;
+                ok = mbar_wait(&k_full[s], ph, p.status, abort_flag);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t k_base = smem_addr(smem + C::OFF_K + s * C::KV_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t c = kk / 4, inner = (kk % 4) * 32;
+                    const uint64_t adesc = smem_desc_sw128(q_base + c * kBM * 128 + inner, 16, 1024);
+                    const uint64_t bdesc =
+                        smem_desc_sw128(k_base + c * C::KV_CHUNK + inner, 16, 1024);
+                    mma_bf16_ss(tmem + kTmemS + s * 128, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&k_empty[s]);
+                tc_commit(&s_full[s]);
+                if (j >= 1) issue_pv(j - 1);
+            }
+            issue_pv(n_kv - 1);
+            // never release TMEM / smem with tensor-core work still in flight
+            tc_commit(drain);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(drain, 0)) {
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(p.status, kStatusTimeout);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ----------------------------- softmax + epilogue -----------------------------
+        const int quad = warp & 3;                  // TMEM lane quadrant of this warp
+        const int row = quad * 32 + lane;           // query row within the tile
+        const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+        const int q_pos = q0 + row + off;           // last key this row may see (causal)
+        const float scale = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kv && ok; ++j) {
+            const int s = j & 1;
+            const uint32_t ph = (j >> 1) & 1;
+            ok = mbar_wait(&s_full[s], ph, p.status, abort_flag);
+            if (!ok) break;
+            tc_fence_after_sync();
+            uint32_t sr[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[c * 32]);
+                tmem_load_32(tmem + t_lane + kTmemS + s * 128 + c * 32, chunk);
+            }
+            const bool need_mask =
+                (j + 1) * BN > kv_len || (p.causal && (j + 1) * BN - 1 > q0 + off);
+            float tmax = -INFINITY;
+            if (need_mask) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    const int kj = j * BN + c;
+                    float v = __uint_as_float(sr[c]) * scale;
+                    if (kj >= kv_len || (p.causal && kj > q_pos)) v = -INFINITY;
+                    sr[c] = __float_as_uint(v);
+                    tmax = fmaxf(tmax, v);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    const float v = __uint_as_float(sr[c]) * scale;
+                    sr[c] = __float_as_uint(v);
+                    tmax = fmaxf(tmax, v);
+                }
+            }
+            const float m_new = fmaxf(m, tmax);
+            const bool grow = m_new > m + 8.0f;     // lazy rescale threshold: 2^8
+            const float m_use = grow ? m_new : m;
+            const float corr = (m == -INFINITY) ? 0.f : fast_exp2(m - m_use);
+            if (j > 0 && __any_sync(kFullMask, grow)) {
+                // O holds P_0..P_{j-1} V: wait for the last P.V, then rescale in TMEM
+                ok = mbar_wait(o_done, (j - 1) & 1, p.status, abort_flag);
+                if (__any_sync(kFullMask, !ok)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const float f = grow ? corr : 1.f;
+#pragma unroll
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_load_32(tmem + t_lane + kTmemO + c * 32, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                    tmem_store_32(tmem + t_lane + kTmemO + c * 32, o);
+                }
+                tmem_store_wait();
+            }
+            if (grow) {
+                l *= corr;
+                m = m_use;
+            }
+            uint32_t pk[BN / 2];
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN / 2; ++c) {
+                float p0 = 0.f, p1 = 0.f;
+                if (m != -INFINITY) {
+                    p0 = fast_exp2(__uint_as_float(sr[2 * c]) - m);
+                    p1 = fast_exp2(__uint_as_float(sr[2 * c + 1]) - m);
+                }
+                lsum += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l += lsum;
+            if constexpr (BN == 128) {
+                tmem_store_64(tmem + t_lane + kTmemS + s * 128, pk);
+            } else {
+                tmem_store_32(tmem + t_lane + kTmemS + s * 128,
+                              *reinterpret_cast<uint32_t (*)[32]>(pk));
+            }
+            tmem_store_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&p_full[s]);
+        }
+        if (n_kv > 0 && ok) {
+            ok = mbar_wait(o_done, (n_kv - 1) & 1, p.status, abort_flag);
+            tc_fence_after_sync();
+        }
+        const bool any_bad = __any_sync(kFullMask, !ok);
+        if (work && !any_bad) {
+            const bool row_ok = q0 + row < qo_len;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
+                                  (static_cast<int64_t>(qo_start + q0 + row) * p.nq + h) * HD;
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t o[32];
+                if (n_kv > 0) {
+                    tmem_load_32(tmem + t_lane + kTmemO + c * 32, o);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv,
+                                       __uint_as_float(o[2 * e + 1]) * inv);
+                if (row_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                }
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---- host side ----------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+bool encode(CUtensorMap *tm, const void *base, int rank, const cuuint64_t *dims,
+            const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
+              strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HD, int BN, bool PAGED>
+cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream) {
+    using C = PrefillCfg<HD, BN>;
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(p.nq),
+                                    static_cast<cuuint64_t>(L.total_qo)};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(HD) * 2,
+                                   static_cast<cuuint64_t>(p.nq) * HD * 2};
+        const cuuint32_t box[3] = {64, 1, kBM};
+        if (!encode(&p.tm_q, L.q, 3, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    if constexpr (!PAGED) {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(p.nkv),
+                                    static_cast<cuuint64_t>(L.total_kv > 0 ? L.total_kv : 1)};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(HD) * 2,
+                                   static_cast<cuuint64_t>(p.nkv) * HD * 2};
+        const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(BN)};
+        if (!encode(&p.tm_k, L.k, 3, dims, str, box)) return cudaErrorInvalidValue;
+        if (!encode(&p.tm_v, L.v, 3, dims, str, box)) return cudaErrorInvalidValue;
+    } else {
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(HD), 16,
+                                    static_cast<cuuint64_t>(p.nkv),
+                                    static_cast<cuuint64_t>(p.num_blocks)};
+        const cuuint64_t str[3] = {static_cast<cuuint64_t>(L.s_token) * 2,
+                                   static_cast<cuuint64_t>(L.s_head) * 2,
+                                   static_cast<cuuint64_t>(L.s_block) * 2};
+        const cuuint32_t box[4] = {64, 16, 1, 1};
+        if (!encode(&p.tm_k, L.k, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!encode(&p.tm_v, L.v, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    prefill_schedule_kernel<<<1, 1024, 0, stream>>>(p.qo_indptr, p.kv_indptr, p.batch, p.causal,
+                                                    BN, p.n_tiles, const_cast<int2 *>(p.tiles),
+                                                    p.status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto kern = prefill_kernel<HD, BN, PAGED>;
+    static int configured_device = -1;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    const dim3 grid(p.nq, p.n_tiles);
+    kern<<<grid, kThreads, C::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream) {
+    if (p.n_tiles == 0) return cudaSuccess;
+    const bool paged = p.block_tables != nullptr;
+    switch (L.head_dim) {
+        case 64:
+            return paged ? launch_prefill_t<64, 128, true>(p, L, stream)
+                         : launch_prefill_t<64, 128, false>(p, L, stream);
+        case 128:
+            return paged ? launch_prefill_t<128, 128, true>(p, L, stream)
+                         : launch_prefill_t<128, 128, false>(p, L, stream);
+        case 256:
+            return paged ? launch_prefill_t<256, 64, true>(p, L, stream)
+                         : launch_prefill_t<256, 64, false>(p, L, stream);
+        default:
+            return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace pa
