@@ -156,6 +156,34 @@ int pa_decode_merge(void *out, const int32_t *seq_lens, int num_seqs, int num_q_
                     size_t workspace_bytes, void *stream);
 
 /*
+ * pa_decode_split_static -- pa_decode_split for callers that cannot allocate.
+ * (Not an operation from the reference pages: it has no counterpart there.)
+ * Some callers may not call cudaMalloc and have no workspace to pass: e.g. a
+ * plugin inside an engine that owns all device memory, or a latency-critical
+ * decode loop where an allocation could synchronise the device or fail with
+ * out-of-memory mid-step.  This entry point allocates nothing: the split
+ * partials live in a device array of PA_STATIC_SCRATCH_BYTES compiled into the
+ * library (every GPU that loads the library holds it until the process exits).
+ * Arguments and result are those of pa_decode_split without the workspace.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address with cudaGetSymbolAddress; make that first call
+ *    before any stream capture.
+ *  - A batch whose pa_decode_split_workspace_size() exceeds
+ *    PA_STATIC_SCRATCH_BYTES is rejected with PA_ERR_WORKSPACE.
+ *  - All calls on a device share the array, which keeps the last call's
+ *    partials; nothing in it needs clearing (each call writes every partition
+ *    it later merges).  Calls that overlap on the GPU (e.g. on two streams of
+ *    one device) race on the array: order them on one stream or with events.
+ */
+#define PA_STATIC_SCRATCH_BYTES (16 * 1024 * 1024)
+int pa_decode_split_static(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
+                           int64_t stride_head, int64_t stride_token, float sm_scale,
+                           int max_seq_len, void *stream);
+
+/*
  * Bytes of workspace pa_ragged_prefill needs (a device-built tile schedule).
  */
 size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_heads,

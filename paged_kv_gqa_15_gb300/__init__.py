@@ -50,6 +50,9 @@ def load():
     lib.pa_decode_split.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, P, Z, P]
     lib.pa_decode_partitions.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, P, Z, P]
     lib.pa_decode_merge.argtypes = [P, P, I, I, I, I, P, Z, P]
+    lib.pa_decode_split_static.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I,
+                                           P]
+    lib.pa_decode_split_static.restype = I
     lib.pa_ragged_prefill_workspace_size.argtypes = [I, I, I, I]
     lib.pa_ragged_prefill_workspace_size.restype = Z
     lib.pa_ragged_prefill.argtypes = [P, P, P, P, P, P, P, P, P, I, I, L, L, L, L, I, I, I, I, I,
@@ -157,6 +160,23 @@ def pa_decode_split(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale, 
                                   block_tables.shape[1], nb, sb, sh, st, float(sm_scale),
                                   int(max_seq_len), _ptr(workspace), workspace.numel(),
                                   _stream(stream)))
+
+
+STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # PA_STATIC_SCRATCH_BYTES in include/pa.h
+
+
+def pa_decode_split_static(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale,
+                           max_seq_len, layout="HND", stream=None):
+    """pa_decode_split with the library's fixed device scratch instead of a workspace,
+    for callers that cannot allocate device memory.  Batches needing more than
+    STATIC_SCRATCH_BYTES of partials are rejected; concurrent calls on one device race."""
+    nb, nkv, bs, hd = _pool_geometry(k_cache, layout)
+    sb, sh, st = pool_strides(k_cache, layout)
+    B, nq, _ = q.shape
+    _check(load().pa_decode_split_static(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(block_tables), _ptr(seq_lens), B, nq, nkv, hd, bs,
+                                         block_tables.shape[1], nb, sb, sh, st, float(sm_scale),
+                                         int(max_seq_len), _stream(stream)))
 
 
 def pa_decode_partitions(q, k_cache, v_cache, block_tables, seq_lens, sm_scale, max_seq_len,

@@ -119,6 +119,8 @@ int decode_common(pa::DecodeParams &p, void *out, const void *q, const void *k_c
 
 }  // namespace
 
+int pa::set_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
 extern "C" {
 
 const char *pa_last_error(void) { return g_last_error; }

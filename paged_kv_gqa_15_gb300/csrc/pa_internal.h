@@ -63,4 +63,7 @@ cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaS
 cudaError_t launch_merge(const DecodeParams &p, int head_dim, cudaStream_t stream);
 cudaError_t launch_prefill(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream);
 
+// Records `msg` as this thread's pa_last_error() text and returns `code`.
+int set_error(int code, const char *msg);
+
 }  // namespace pa
