@@ -38,10 +38,13 @@ namespace {
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr int kBM = 128;              // query rows per tile (MMA M)
 constexpr int kThreads = 192;         // 6 warps
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;        // S / P buffers at columns 0 and 128
-constexpr uint32_t kTmemO = 256;      // O accumulator at columns 256 .. 256 + head_dim
 constexpr int kSchedBuckets = 2048;
+
+constexpr uint32_t pow2_at_least(uint32_t x) {
+    uint32_t v = 32;
+    while (v < x) v <<= 1;
+    return v;
+}
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -65,11 +68,19 @@ struct PrefillCfg {
     static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
     static constexpr uint32_t SMEM_USED = OFF_BAR + 256;
-    // + alignment slack; at least ~116 KB so that one CTA (and its 512 TMEM
-    // columns) owns an SM
-    static constexpr uint32_t SMEM = (SMEM_USED + 1024 > 118 * 1024) ? SMEM_USED + 1024 : 118 * 1024;
+    // TMEM: S / P double buffer at columns [0, BN) and [BN, 2 BN), O after them
+    static constexpr uint32_t TM_S = 0;
+    static constexpr uint32_t TM_O = 2 * BN;
+    static constexpr uint32_t TMEM_COLS = pow2_at_least(2 * BN + HD);
+    // Two CTAs share an SM when both fit in its 512 TMEM columns (and in shared
+    // memory): their MMA and softmax phases then interleave on the tensor core.
+    // A CTA that needs all 512 columns asks for enough shared memory to be alone.
+    static constexpr int CTAS_PER_SM = TMEM_COLS <= 256 ? 2 : 1;
+    static constexpr uint32_t SMEM_MIN = CTAS_PER_SM == 2 ? 0 : 118 * 1024;
+    static constexpr uint32_t SMEM = (SMEM_USED + 1024 > SMEM_MIN) ? SMEM_USED + 1024 : SMEM_MIN;
     static_assert(HD % 64 == 0 && BN % 16 == 0 && BN <= 128, "tile shape");
-    static_assert(kTmemO + HD <= kTmemCols, "TMEM budget");
+    static_assert(TMEM_COLS <= 512, "TMEM budget");
+    static_assert(CTAS_PER_SM == 1 || 2 * SMEM <= 227 * 1024, "two CTAs per SM");
 };
 
 // Number of key tiles a query tile needs (its work), bottom-right causal.
@@ -133,7 +144,8 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(
 }
 
 template <int HD, int BN, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
+    prefill_kernel(const __grid_constant__ PrefillParams p) {
     using C = PrefillCfg<HD, BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -146,10 +158,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint64_t *v_empty = bars + 7;  // [2]
     uint64_t *s_full = bars + 9;   // [2]
     uint64_t *p_full = bars + 11;  // [2]
-    uint64_t *o_done = bars + 13;  // one phase per P.V
+    // o_done completes one phase per P.V.  While softmax works on tile j only
+    // P_{j-1} V can be pending (S_j completing implies P_{j-2} V completed), so a
+    // parity wait on it is unambiguous there; after the last tile two P.V may be
+    // pending, so the epilogue waits on o_final (committed after the last P.V).
+    uint64_t *o_done = bars + 13;
     uint64_t *drain = bars + 14;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 16);
+    uint64_t *o_final = bars + 15;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -186,11 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
+        mbar_init(o_final, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -281,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint64_t bdesc =
                         smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
-                    mma_bf16_ts(tmem + kTmemO, tmem + kTmemS + s * 128 + kk * 8, bdesc, idesc_o,
+                    mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + s * BN + kk * 8, bdesc, idesc_o,
                                 (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&v_empty[s]);
@@ -300,13 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     const uint64_t adesc = smem_desc_sw128(q_base + c * kBM * 128 + inner, 16, 1024);
                     const uint64_t bdesc =
                         smem_desc_sw128(k_base + c * C::KV_CHUNK + inner, 16, 1024);
-                    mma_bf16_ss(tmem + kTmemS + s * 128, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                    mma_bf16_ss(tmem + C::TM_S + s * BN, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&k_empty[s]);
                 tc_commit(&s_full[s]);
                 if (j >= 1) issue_pv(j - 1);
             }
             issue_pv(n_kv - 1);
+            if (ok) tc_commit(o_final);
             // never release TMEM / smem with tensor-core work still in flight
             tc_commit(drain);
             const uint64_t t0 = global_timer_ns();
@@ -337,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[c * 32]);
-                tmem_load_32(tmem + t_lane + kTmemS + s * 128 + c * 32, chunk);
+                tmem_load_32(tmem + t_lane + C::TM_S + s * BN + c * 32, chunk);
             }
             const bool need_mask =
                 (j + 1) * BN > kv_len || (p.causal && (j + 1) * BN - 1 > q0 + off);
@@ -375,10 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                 for (int c = 0; c < HD / 32; ++c) {
                     uint32_t o[32];
-                    tmem_load_32(tmem + t_lane + kTmemO + c * 32, o);
+                    tmem_load_32(tmem + t_lane + C::TM_O + c * 32, o);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tmem_store_32(tmem + t_lane + kTmemO + c * 32, o);
+                    tmem_store_32(tmem + t_lane + C::TM_O + c * 32, o);
                 }
                 tmem_store_wait();
             }
@@ -400,9 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             l += lsum;
             if constexpr (BN == 128) {
-                tmem_store_64(tmem + t_lane + kTmemS + s * 128, pk);
+                tmem_store_64(tmem + t_lane + C::TM_S + s * BN, pk);
             } else {
-                tmem_store_32(tmem + t_lane + kTmemS + s * 128,
+                tmem_store_32(tmem + t_lane + C::TM_S + s * BN,
                               *reinterpret_cast<uint32_t (*)[32]>(pk));
             }
             tmem_store_wait();
@@ -410,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             mbar_arrive(&p_full[s]);
         }
         if (n_kv > 0 && ok) {
-            ok = mbar_wait(o_done, (n_kv - 1) & 1, p.status, abort_flag);
+            ok = mbar_wait(o_final, 0, p.status, abort_flag);
             tc_fence_after_sync();
         }
         const bool any_bad = __any_sync(kFullMask, !ok);
@@ -423,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
                 if (n_kv > 0) {
-                    tmem_load_32(tmem + t_lane + kTmemO + c * 32, o);
+                    tmem_load_32(tmem + t_lane + C::TM_O + c * 32, o);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
@@ -447,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
@@ -539,11 +558,11 @@ cudaError_t launch_prefill(PrefillParams &p, const PrefillLaunch &L, cudaStream_
     const bool paged = p.block_tables != nullptr;
     switch (L.head_dim) {
         case 64:
-            return paged ? launch_prefill_t<64, 128, true>(p, L, stream)
-                         : launch_prefill_t<64, 128, false>(p, L, stream);
+            return paged ? launch_prefill_t<64, 64, true>(p, L, stream)
+                         : launch_prefill_t<64, 64, false>(p, L, stream);
         case 128:
-            return paged ? launch_prefill_t<128, 128, true>(p, L, stream)
-                         : launch_prefill_t<128, 128, false>(p, L, stream);
+            return paged ? launch_prefill_t<128, 64, true>(p, L, stream)
+                         : launch_prefill_t<128, 64, false>(p, L, stream);
         case 256:
             return paged ? launch_prefill_t<256, 64, true>(p, L, stream)
                          : launch_prefill_t<256, 64, false>(p, L, stream);

@@ -1,0 +1,74 @@
+"""Host-side logic of bench.py on the CPU: multi-rank aggregation over gloo
+(world size 2), clock-sample parsing and the oracle reference arm."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # rank r processed (r + 1) GB in (10 + 5 r) ms per step
+    value, ms = bench.aggregate_throughput((rank + 1) * 1e9, 10.0 + 5.0 * rank)
+    q.put((rank, value, ms, bench.reduce_max(float(rank))))
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_over_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, value, ms, mx in res:
+        assert ms == pytest.approx(15.0)                  # max over ranks
+        assert value == pytest.approx(3e9 / 0.015)        # all ranks' units / max time
+        assert mx == 1.0
+
+
+def test_single_process_aggregation_is_identity():
+    value, ms = bench.aggregate_throughput(2e9, 4.0)
+    assert ms == 4.0 and value == pytest.approx(5e11)
+
+
+def test_clock_summary_parsing():
+    lines = ["1965, 2070, 610.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "2070, 2070, 900.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+             "garbage line"]
+    s = bench.ClockSampler.summary(lines)
+    assert s["sm_mhz"] == pytest.approx((1965 + 2070) / 2)
+    assert s["sm_max_mhz"] == 2070 and s["samples"] == 2
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                          "tiny_decode", "--steps", "2", "--warmup", "3"], cwd=ROOT,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
