@@ -41,7 +41,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) per launch from ncu captures, keyed by kernel, valid only
 # for the source file hash they were measured on (otherwise reported as null).
-TRAFFIC = {}
+TRAFFIC = {
+    # ncu capture of one decode_kernel<128,4,persistent> launch on the Llama-8B decode
+    # workload: dram__bytes_read.sum 568.39 MB + dram__bytes_write.sum 5.43 MB
+    "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
+        "src": "b593ae57d3f2f152", "bytes_per_launch": 573817344},
+}
 
 
 # ---------------------------------------------------------------------------------------
@@ -536,9 +541,14 @@ def main(argv=None):
 
     clocks = ClockSampler(uuid)
     clocks.start()
-    res, state = bench_decode(w, args.steps, args.warmup, dev, stream, peaks, peak_kind)
+    is_decode = isinstance(w, W.DecodeWorkload)
+    if is_decode:
+        res, state = bench_decode(w, args.steps, args.warmup, dev, stream, peaks, peak_kind)
+    else:
+        res, state = bench_prefill(w, args.steps, args.warmup, dev, stream, peaks,
+                                   peak_kind), None
     clk_main = clocks.stop()
-    e2e = bench_decode_e2e(w, state, args.steps, args.warmup, dev, stream)
+    e2e = bench_decode_e2e(w, state, args.steps, args.warmup, dev, stream) if is_decode else None
     status = pa.device_status(stream)
     clocks_all = ClockSampler(uuid)
     clocks_all.start()
@@ -565,7 +575,7 @@ def main(argv=None):
     clk["extra_workloads"] = clk_all
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and is_decode:
         t = state["t"]
         host = host_decode_inputs(w, t)
         gbs, dt, n, th = oracle_decode_sample(w, host, target_s=15.0)
@@ -575,7 +585,7 @@ def main(argv=None):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(res["value"], 3), "unit": "GB/s",
+            "metric": METRIC, "value": round(res["value"], 3), "unit": res["unit"],
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(res["ms_per_step"], 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",

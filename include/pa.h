@@ -207,6 +207,7 @@ size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_
  *   qo_indptr_h, kv_indptr_h  [batch+1] int32 HOST copies (used to size and
  *         order the launch); qo_indptr_d, kv_indptr_d the same on the device.
  *   workspace  >= pa_ragged_prefill_workspace_size() bytes, 256-byte aligned.
+ *   sm_scale must be positive and finite (PA_ERR_INVALID otherwise).
  */
 int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
                       const int32_t *qo_indptr_h, const int32_t *kv_indptr_h,

@@ -346,7 +346,8 @@ int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
     if (batch == 0) return PA_OK;
     if (!qo_indptr_h || !kv_indptr_h || !qo_indptr_d || !kv_indptr_d)
         return fail(PA_ERR_INVALID, "null indptr");
-    if (!(sm_scale == sm_scale)) return fail(PA_ERR_INVALID, "sm_scale is NaN");
+    if (!(sm_scale > 0.f) || sm_scale == INFINITY)
+        return fail(PA_ERR_INVALID, "sm_scale must be positive and finite for prefill");
     const bool paged = block_tables != nullptr;
     if (paged) {
         rc = check_pool(head_dim, block_size, num_blocks, num_kv_heads, stride_block,

@@ -649,6 +649,9 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     if (configured_device != dev) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
+        // ask for the largest shared-memory carveout so two CTAs fit per SM
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern, C::NT, C::SMEM);
         if (e != cudaSuccess) return e;
         configured_device = dev;

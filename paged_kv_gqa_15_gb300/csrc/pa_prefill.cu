@@ -52,6 +52,29 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// 2^x for a pair, on the FMA / ALU pipes instead of the MUFU unit (so the two
+// can share the softmax's exponentials).  Range reduction 2^x = 2^n * 2^f with
+// n = round(x) taken from the low mantissa bits of x + 1.5 * 2^23, f in
+// [-0.5, 0.5]; 2^f by a cubic minimax fit on that interval (max relative error
+// 7.5e-5, far below the bf16 rounding that P gets next); 2^n added straight to
+// the exponent bits.  x is clamped at -125 so the exponent never underflows:
+// masked scores (-inf) come out as ~2e-38 instead of 0, which no bf16 sum of P
+// or P.V can see.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    x.x = fmaxf(x.x, -125.f);
+    x.y = fmaxf(x.y, -125.f);
+    const float2 t = __fadd2_rn(x, make_float2(kMagic, kMagic));
+    const float2 n = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
+    const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
+    float2 pv = __ffma2_rn(f, make_float2(0.055171505f, 0.055171505f),
+                           make_float2(0.24261115f, 0.24261115f));
+    pv = __ffma2_rn(f, pv, make_float2(0.693261f, 0.693261f));
+    pv = __ffma2_rn(f, pv, make_float2(0.99992806f, 0.99992806f));
+    return make_float2(__int_as_float(__float_as_int(pv.x) + (__float_as_int(t.x) << 23)),
+                       __int_as_float(__float_as_int(pv.y) + (__float_as_int(t.y) << 23)));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
@@ -294,6 +317,21 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                      mbar_wait(&v_full[s], ph, p.status, abort_flag);
                 if (!ok) return;
                 tc_fence_after_sync();
+                if constexpr (PAGED) {
+                    // Rows past kv_len in the sequence's last page hold whatever the pool
+                    // held; P is 0 there, but 0 x NaN would still poison O, so zero them.
+                    const int first_stale = kv_len - i * BN;
+                    if (first_stale < BN) {
+                        uint8_t *vt = smem + C::OFF_V + s * C::KV_BYTES;
+                        for (int c = 0; c < C::QCH; ++c)
+                            for (int row = max(first_stale, 0); row < BN; ++row) {
+                                uint4 *dst = reinterpret_cast<uint4 *>(vt + c * C::KV_CHUNK + row * 128);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+                            }
+                        fence_proxy_async_smem();
+                    }
+                }
                 const uint32_t v_base = smem_addr(smem + C::OFF_V + s * C::KV_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
@@ -353,32 +391,34 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             if (!ok) break;
             tc_fence_after_sync();
             uint32_t sr[BN];
+            if constexpr (BN == 64) {
+                tmem_load_64(tmem + t_lane + C::TM_S + s * BN, sr);
+            } else {
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[c * 32]);
-                tmem_load_32(tmem + t_lane + C::TM_S + s * BN + c * 32, chunk);
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t (&chunk)[64] = *reinterpret_cast<uint32_t (*)[64]>(&sr[c * 64]);
+                    tmem_load_64(tmem + t_lane + C::TM_S + s * BN + c * 64, chunk);
+                }
             }
             const bool need_mask =
                 (j + 1) * BN > kv_len || (p.causal && (j + 1) * BN - 1 > q0 + off);
-            float tmax = -INFINITY;
             if (need_mask) {
 #pragma unroll
                 for (int c = 0; c < BN; ++c) {
                     const int kj = j * BN + c;
-                    float v = __uint_as_float(sr[c]) * scale;
-                    if (kj >= kv_len || (p.causal && kj > q_pos)) v = -INFINITY;
-                    sr[c] = __float_as_uint(v);
-                    tmax = fmaxf(tmax, v);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const float v = __uint_as_float(sr[c]) * scale;
-                    sr[c] = __float_as_uint(v);
-                    tmax = fmaxf(tmax, v);
+                    if (kj >= kv_len || (p.causal && kj > q_pos)) sr[c] = __float_as_uint(-INFINITY);
                 }
             }
-            const float m_new = fmaxf(m, tmax);
+            // row max of the raw scores (sm_scale > 0, so it scales to the max of s * scale);
+            // eight independent partial maxima keep the dependency chain short
+            float pmax[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pmax[e] = __uint_as_float(sr[e]);
+#pragma unroll
+            for (int c = 8; c < BN; ++c) pmax[c & 7] = fmaxf(pmax[c & 7], __uint_as_float(sr[c]));
+            const float tmax = fmaxf(fmaxf(fmaxf(pmax[0], pmax[1]), fmaxf(pmax[2], pmax[3])),
+                                     fmaxf(fmaxf(pmax[4], pmax[5]), fmaxf(pmax[6], pmax[7])));
+            const float m_new = fmaxf(m, tmax * scale);   // -inf stays -inf
             const bool grow = m_new > m + 8.0f;     // lazy rescale threshold: 2^8
             const float m_use = grow ? m_new : m;
             const float corr = (m == -INFINITY) ? 0.f : fast_exp2(m - m_use);
@@ -405,19 +445,35 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 l *= corr;
                 m = m_use;
             }
+            // P = 2^(s * scale - m): three pairs in four on the MUFU unit, one on the
+            // FMA pipe (exp2_poly2), so neither unit alone bounds the softmax
             uint32_t pk[BN / 2];
-            float lsum = 0.f;
+            float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                              make_float2(0.f, 0.f)};
+            if (m != -INFINITY) {
+                const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-m, -m);
 #pragma unroll
-            for (int c = 0; c < BN / 2; ++c) {
-                float p0 = 0.f, p1 = 0.f;
-                if (m != -INFINITY) {
-                    p0 = fast_exp2(__uint_as_float(sr[2 * c]) - m);
-                    p1 = fast_exp2(__uint_as_float(sr[2 * c + 1]) - m);
+                for (int c = 0; c < BN / 2; ++c) {
+                    const float2 x = __ffma2_rn(
+                        make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
+                        sc2, nm2);
+                    float2 e;
+                    if ((c & 3) == 3) {
+                        e = exp2_poly2(x);
+                    } else {
+                        e.x = fast_exp2(x.x);
+                        e.y = fast_exp2(x.y);
+                    }
+                    lsum[c & 3] = __fadd2_rn(lsum[c & 3], e);
+                    pk[c] = pack_bf16x2(e.x, e.y);
                 }
-                lsum += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;
             }
-            l += lsum;
+            const float2 ls01 = __fadd2_rn(lsum[0], lsum[1]), ls23 = __fadd2_rn(lsum[2], lsum[3]);
+            const float2 lsum_t = __fadd2_rn(ls01, ls23);
+            l += lsum_t.x + lsum_t.y;
             if constexpr (BN == 128) {
                 tmem_store_64(tmem + t_lane + C::TM_S + s * BN, pk);
             } else {
@@ -543,6 +599,8 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }

@@ -244,3 +244,37 @@ def test_chunked_paged_prefill_config_sampled():
                          block_tables=w.block_tables, block_size=16, rows=rows)
     assert_close_bf16(bf16_out(o)[rows], ref[rows], what="config chunked paged prefill")
     assert pa.device_status() == 0
+
+
+def test_paged_stale_nan_rows_do_not_leak():
+    """Rows of a request's last page past its kv length may hold anything (here NaN):
+    they are masked out and must not reach the output."""
+    w = W.make_prefill("stale", [20, 7], [37, 70], 4, 2, 128, seed=40, paged=True)
+    t = w.tensors("cpu")
+    q = W.to_bits(t["q"])
+    kc, vc = W.to_bits(t["k_cache"]), W.to_bits(t["v_cache"])
+    nan = np.uint16(0x7FC0)
+    for r, kv in enumerate(w.kv_lens):
+        if kv % 16:
+            page = w.block_tables[r, kv // 16]
+            kc[page, :, kv % 16:, :] = nan
+            vc[page, :, kv % 16:, :] = nan
+    o = torch.empty(t["q"].shape, dtype=torch.bfloat16, device=DEV)
+    pa.pa_ragged_prefill(o, _to_dev(q), _to_dev(kc), _to_dev(vc), w.qo_indptr, w.kv_indptr,
+                         torch.from_numpy(w.qo_indptr).to(DEV),
+                         torch.from_numpy(w.kv_indptr).to(DEV), w.scale, causal=True,
+                         block_tables=torch.from_numpy(w.block_tables).to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.prefill(q, kc, vc, w.qo_indptr, w.kv_indptr, 2, w.scale, causal=True,
+                         block_tables=w.block_tables, block_size=16)
+    assert_close_bf16(o, ref, what="stale NaN rows")
+
+
+def test_rejects_non_positive_scale():
+    w = W.make_prefill("s", [4], [4], 2, 1, 64, seed=41)
+    t = w.tensors("cpu")
+    o = torch.empty(t["q"].shape, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(pa.PaError):
+        pa.pa_ragged_prefill(o, t["q"].to(DEV), t["k"].to(DEV), t["v"].to(DEV), w.qo_indptr,
+                             w.kv_indptr, torch.from_numpy(w.qo_indptr).to(DEV),
+                             torch.from_numpy(w.kv_indptr).to(DEV), 0.0)
