@@ -327,7 +327,7 @@ size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_
     (void)head_dim;
     const size_t tiles = static_cast<size_t>(total_qo_rows > 0 ? total_qo_rows : 0) / 128 +
                          static_cast<size_t>(batch > 0 ? batch : 0) + 1;
-    return round256(tiles * 8);
+    return 256 + round256(tiles * 8);  // work-item counter, then the tile schedule
 }
 
 int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
@@ -395,7 +395,8 @@ int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
     p.qo_indptr = qo_indptr_d;
     p.kv_indptr = kv_indptr_d;
     p.block_tables = block_tables;
-    p.tiles = static_cast<const int2 *>(workspace);
+    p.item_counter = static_cast<int *>(workspace);
+    p.tiles = reinterpret_cast<const int2 *>(static_cast<char *>(workspace) + 256);
     p.num_blocks = paged ? num_blocks : 0;
     p.batch = batch;
     p.nq = num_q_heads;

@@ -44,6 +44,7 @@ struct PrefillParams {
     const int32_t *qo_indptr, *kv_indptr;  // device [batch + 1]
     const int32_t *block_tables;           // paged mode, else nullptr
     const int2 *tiles;                     // (request, q tile), heaviest first
+    int *item_counter;                     // next unclaimed work item (zeroed per call)
     int64_t num_blocks;
     int batch, nq, nkv, max_blocks, n_tiles, causal;
     float scale_log2;

@@ -9,7 +9,9 @@
 // mode, 16-token pages).
 //
 // GB300 design (FlashAttention-style, not the pages' SM80 design):
-//  * CTA = one (request, 128-row query tile, query head); 6 warps:
+//  * Persistent CTAs (two per SM at head_dim <= 128) claim work items -- one
+//    (request, 128-row query tile, query head) each -- from a heaviest-first
+//    list through a global counter; 6 warps per CTA:
 //      warp 0   TMA producer: Q once, then K_j / V_j tiles (128-byte swizzle)
 //               into a 2-stage ring; paged mode issues one box per 16-token page
 //      warp 1   TMEM allocator + single-thread tcgen05.mma issuer:
@@ -116,10 +118,11 @@ __device__ __forceinline__ int key_tiles(int q0, int qo_len, int kv_len, int cau
 // Heaviest-first order of the (request, query tile) work items.
 __global__ void __launch_bounds__(1024) prefill_schedule_kernel(
     const int32_t *qo_indptr, const int32_t *kv_indptr, int batch, int causal, int bn,
-    int n_tiles, int2 *tiles, int *status) {
+    int n_tiles, int2 *tiles, int *item_counter, int *status) {
     __shared__ int hist[kSchedBuckets];
     __shared__ int total_sh;
     const int tid = threadIdx.x;
+    if (tid == 0) *item_counter = 0;  // the prefill kernel claims items from here
     for (int i = tid; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
     if (tid == 0) total_sh = 0;
     __syncthreads();
@@ -166,6 +169,37 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(
     for (int i = total + tid; i < n_tiles; i += blockDim.x) tiles[i] = make_int2(-1, -1);
 }
 
+// One work item: a 128-row query tile of one request for one query head.
+struct PrefillItem {
+    int r, h, qo_start, qo_len, kv_start, kv_len, q0, n_kv;
+    bool work;  // the tile holds query rows (it is written, possibly with zeros)
+};
+
+template <bool PAGED, int BN>
+__device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, long long i) {
+    PrefillItem w;
+    const int2 tile = p.tiles[i / p.nq];
+    w.h = static_cast<int>(i % p.nq);
+    w.r = tile.x;
+    w.qo_start = w.qo_len = w.kv_start = w.kv_len = 0;
+    const bool ok = w.r >= 0 && w.r < p.batch;
+    if (ok) {
+        w.qo_start = p.qo_indptr[w.r];
+        w.qo_len = p.qo_indptr[w.r + 1] - w.qo_start;
+        w.kv_start = p.kv_indptr[w.r];
+        w.kv_len = p.kv_indptr[w.r + 1] - w.kv_start;
+        if (PAGED && w.kv_len > p.max_blocks * kBlockSize) w.kv_len = p.max_blocks * kBlockSize;
+    }
+    w.q0 = ok ? tile.y * kBM : 0;
+    w.work = ok && w.q0 < w.qo_len;
+    w.n_kv = w.work ? key_tiles(w.q0, w.qo_len, w.kv_len, p.causal, BN) : 0;
+    return w;
+}
+
+// Persistent: each CTA claims items of the heaviest-first list (item i = query
+// tile i / nq, head i % nq) one at a time from a global counter, so the load
+// balances itself; TMEM and barriers are set up once and the next item's
+// Q / K / V loads overlap the current item's tail.
 template <int HD, int BN, bool PAGED>
 __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
@@ -175,47 +209,38 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *q_full = bars + 0;
-    uint64_t *k_full = bars + 1;   // [2]
-    uint64_t *k_empty = bars + 3;  // [2]
-    uint64_t *v_full = bars + 5;   // [2]
-    uint64_t *v_empty = bars + 7;  // [2]
-    uint64_t *s_full = bars + 9;   // [2]
-    uint64_t *p_full = bars + 11;  // [2]
-    // o_done completes one phase per P.V.  While softmax works on tile j only
-    // P_{j-1} V can be pending (S_j completing implies P_{j-2} V completed), so a
-    // parity wait on it is unambiguous there; after the last tile two P.V may be
-    // pending, so the epilogue waits on o_final (committed after the last P.V).
-    uint64_t *o_done = bars + 13;
-    uint64_t *drain = bars + 14;
+    uint64_t *q_empty = bars + 1;   // committed after an item's last S = Q K^T
+    uint64_t *k_full = bars + 2;    // [2]
+    uint64_t *k_empty = bars + 4;   // [2]
+    uint64_t *v_full = bars + 6;    // [2]
+    uint64_t *v_empty = bars + 8;   // [2]
+    uint64_t *s_full = bars + 10;   // [2]
+    uint64_t *p_full = bars + 12;   // [2]
+    // o_done completes one phase per P.V (counted over all items).  While softmax
+    // works on key tile j only P_{j-1} V can be pending (S_j completing implies
+    // P_{j-2} V completed, and the previous item finished before), so a parity wait
+    // on it is unambiguous; an item's epilogue waits on o_final instead (committed
+    // after the item's last P.V), and hands O back with o_free.
+    uint64_t *o_done = bars + 14;
     uint64_t *o_final = bars + 15;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
+    uint64_t *o_free = bars + 16;
+    uint64_t *drain = bars + 17;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 19);
+    // Work items are claimed dynamically (atomicAdd on a global counter) by the
+    // producer and handed to the MMA and softmax warps through a 4-deep queue.
+    uint64_t *item_full = bars + 20;   // [4]
+    uint64_t *item_empty = bars + 24;  // [4]: released by the MMA thread + 4 softmax warps
+    volatile int *item_q = reinterpret_cast<volatile int *>(bars + 28);  // [4]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int h = blockIdx.x;
-    const int2 tile = p.tiles[blockIdx.y];
-    const int r = tile.x;
-    const bool tile_ok = r >= 0 && r < p.batch;
-    int qo_start = 0, qo_len = 0, kv_start = 0, kv_len = 0;
-    if (tile_ok) {
-        qo_start = p.qo_indptr[r];
-        qo_len = p.qo_indptr[r + 1] - qo_start;
-        kv_start = p.kv_indptr[r];
-        kv_len = p.kv_indptr[r + 1] - kv_start;
-        if (PAGED && kv_len > p.max_blocks * kBlockSize) {
-            if (threadIdx.x == 0) atomicOr(p.status, kStatusBounds);
-            kv_len = p.max_blocks * kBlockSize;
-        }
-    }
-    const int q0 = tile_ok ? tile.y * kBM : 0;
-    const bool work = tile_ok && q0 < qo_len;
-    const int off = kv_len - qo_len;
-    const int kh = h / (p.nq / p.nkv);
-    const int n_kv = work ? key_tiles(q0, qo_len, kv_len, p.causal, BN) : 0;
+    const long long n_items = static_cast<long long>(p.n_tiles) * p.nq;
+    const int group = p.nq / p.nkv;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -225,8 +250,13 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             mbar_init(&p_full[s], 128);
         }
         mbar_init(o_done, 1);
-        mbar_init(drain, 1);
         mbar_init(o_final, 1);
+        mbar_init(o_free, 128);
+        mbar_init(drain, 1);
+        for (int k = 0; k < 4; ++k) {
+            mbar_init(&item_full[k], 1);
+            mbar_init(&item_empty[k], 5);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -241,37 +271,74 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
 
     if (warp == 0) {
         // ------------------------------- TMA producer -------------------------------
-        if (n_kv > 0) {
+        if (lane == 0) {
+            prefetch_tensormap(&p.tm_q);
+            prefetch_tensormap(&p.tm_k);
+            prefetch_tensormap(&p.tm_v);
+        }
+        uint32_t kv_it = 0, q_it = 0;
+        int stop = 0;
+        // Claims the k-th item of this CTA and publishes it to the MMA and softmax
+        // warps; returns the item index, or -1 when the list is exhausted.
+        auto claim = [&](uint32_t k) -> int {
+            int i = -1;
             if (lane == 0) {
-                prefetch_tensormap(&p.tm_q);
-                prefetch_tensormap(&p.tm_k);
-                prefetch_tensormap(&p.tm_v);
-                mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-                for (int c = 0; c < C::QCH; ++c)
-                    tma_load_3d(smem + C::OFF_Q + c * kBM * 128, &p.tm_q, c * 64, h, qo_start + q0,
-                                q_full);
-            }
-            const int pages_seq = (kv_len + kBlockSize - 1) / kBlockSize;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j & 1;
-                const uint32_t ph = ((j >> 1) & 1) ^ 1u;
-                int page = 0;
-                if constexpr (PAGED) {
-                    const int pidx = j * (BN / kBlockSize) + lane;
-                    const bool in_seq = lane < BN / kBlockSize && pidx < pages_seq;
-                    page = in_seq ? p.block_tables[static_cast<int64_t>(r) * p.max_blocks + pidx]
-                                  : -1;
-                    const bool bad = in_seq && (page < 0 || page >= p.num_blocks);
-                    if (__any_sync(kFullMask, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
-                    // pages past the sequence (or bad ids) read as zeros: out-of-range box
-                    if (!in_seq || bad) page = static_cast<int>(p.num_blocks);
+                const int slot = k & 3;
+                if (!mbar_wait(&item_empty[slot], ((k >> 2) & 1) ^ 1u, p.status, abort_flag)) {
+                    stop = 1;
+                } else {
+                    const long long claimed = atomicAdd(p.item_counter, 1);
+                    i = claimed < n_items ? static_cast<int>(claimed) : -1;
+                    item_q[slot] = i;
+                    mbar_arrive(&item_full[slot]);
                 }
+            }
+            stop = __shfl_sync(kFullMask, stop, 0);
+            return stop ? -1 : __shfl_sync(kFullMask, i, 0);
+        };
+        // Page id of page `pidx` of request r for lanes that ask (pages past the
+        // sequence or bad ids -> num_blocks, an out-of-range box that reads zeros).
+        auto page_of = [&](int r, int pidx, int pages_seq, bool ask) -> int {
+            int page = -1;
+            const bool in_seq = ask && pidx < pages_seq;
+            if (in_seq) page = p.block_tables[static_cast<int64_t>(r) * p.max_blocks + pidx];
+            const bool bad = in_seq && (page < 0 || page >= p.num_blocks);
+            if (__any_sync(kFullMask, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
+            return (!in_seq || bad) ? static_cast<int>(p.num_blocks) : page;
+        };
+        for (uint32_t k = 0; !stop; ++k) {
+            const int cur = claim(k);
+            if (stop || cur < 0) break;
+            const PrefillItem w = prefill_item<PAGED, BN>(p, cur);
+            if (w.n_kv == 0) continue;
+            const int kh = w.h / group;
+
+            if (lane == 0) {
+                if (!mbar_wait(q_empty, (q_it & 1) ^ 1u, p.status, abort_flag)) {
+                    stop = 1;
+                } else {
+                    mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+                    for (int c = 0; c < C::QCH; ++c)
+                        tma_load_3d(smem + C::OFF_Q + c * kBM * 128, &p.tm_q, c * 64, w.h,
+                                    w.qo_start + w.q0, q_full);
+                }
+            }
+            stop = __shfl_sync(kFullMask, stop, 0);
+            if (stop) break;
+            ++q_it;
+            const int pages_seq = (w.kv_len + kBlockSize - 1) / kBlockSize;
+            for (int j = 0; j < w.n_kv && !stop; ++j, ++kv_it) {
+                const int s = kv_it & 1;
+                const uint32_t ph = ((kv_it >> 1) & 1) ^ 1u;
+                int page = 0;
+                if constexpr (PAGED)
+                    page = page_of(w.r, j * (BN / kBlockSize) + lane, pages_seq,
+                                   lane < BN / kBlockSize);
                 for (int kv = 0; kv < 2; ++kv) {
                     uint64_t *full = kv ? &v_full[s] : &k_full[s];
                     uint64_t *empty = kv ? &v_empty[s] : &k_empty[s];
                     const CUtensorMap *tm = kv ? &p.tm_v : &p.tm_k;
                     uint8_t *dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::KV_BYTES;
-                    int stop = 0;
                     if (lane == 0) {
                         if (!mbar_wait(empty, ph, p.status, abort_flag)) {
                             stop = 1;
@@ -280,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                             if constexpr (!PAGED) {
                                 for (int c = 0; c < C::QCH; ++c)
                                     tma_load_3d(dst + c * C::KV_CHUNK, tm, c * 64, kh,
-                                                kv_start + j * BN, full);
+                                                w.kv_start + j * BN, full);
                             }
                         }
                     }
@@ -288,44 +355,47 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                     if (stop) break;
                     if constexpr (PAGED) {
 #pragma unroll
-                        for (int i = 0; i < BN / kBlockSize; ++i) {
-                            const int pg = __shfl_sync(kFullMask, page, i);
+                        for (int e = 0; e < BN / kBlockSize; ++e) {
+                            const int pg = __shfl_sync(kFullMask, page, e);
                             if (lane == 0) {
                                 for (int c = 0; c < C::QCH; ++c)
-                                    tma_load_4d(dst + c * C::KV_CHUNK + i * kBlockSize * 128, tm,
+                                    tma_load_4d(dst + c * C::KV_CHUNK + e * kBlockSize * 128, tm,
                                                 c * 64, 0, kh, pg, full);
                             }
                         }
                     }
                 }
-                if (*abort_flag) break;
             }
         }
     } else if (warp == 1) {
         // -------------------------------- MMA issuer --------------------------------
-        if (n_kv > 0 && lane == 0) {
+        if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, HD, false, true);
             const uint32_t q_base = smem_addr(smem + C::OFF_Q);
-            bool ok = mbar_wait(q_full, 0, p.status, abort_flag);
-            tc_fence_after_sync();
-            auto issue_pv = [&](int i) {
-                const int s = i & 1;
-                const uint32_t ph = (i >> 1) & 1;
+            uint32_t kv_it = 0, q_it = 0, o_items = 0;
+            bool ok = true;
+            // O += P_g V_g for global key tile g (tile jj of an item with kv_len keys)
+            auto issue_pv = [&](uint32_t g, int jj, int kv_len) {
                 if (!ok) return;
-                ok = mbar_wait(&p_full[s], ph, p.status, abort_flag) &&
+                const int s = g & 1;
+                const uint32_t ph = (g >> 1) & 1;
+                if (jj == 0 && o_items > 0)  // the previous item's epilogue has read O
+                    ok = mbar_wait(o_free, (o_items - 1) & 1, p.status, abort_flag);
+                ok = ok && mbar_wait(&p_full[s], ph, p.status, abort_flag) &&
                      mbar_wait(&v_full[s], ph, p.status, abort_flag);
                 if (!ok) return;
                 tc_fence_after_sync();
                 if constexpr (PAGED) {
                     // Rows past kv_len in the sequence's last page hold whatever the pool
                     // held; P is 0 there, but 0 x NaN would still poison O, so zero them.
-                    const int first_stale = kv_len - i * BN;
+                    const int first_stale = kv_len - jj * BN;
                     if (first_stale < BN) {
                         uint8_t *vt = smem + C::OFF_V + s * C::KV_BYTES;
                         for (int c = 0; c < C::QCH; ++c)
                             for (int row = max(first_stale, 0); row < BN; ++row) {
-                                uint4 *dst = reinterpret_cast<uint4 *>(vt + c * C::KV_CHUNK + row * 128);
+                                uint4 *dst =
+                                    reinterpret_cast<uint4 *>(vt + c * C::KV_CHUNK + row * 128);
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
                             }
@@ -338,32 +408,52 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                     const uint64_t bdesc =
                         smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
                     mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + s * BN + kk * 8, bdesc, idesc_o,
-                                (i > 0 || kk > 0) ? 1u : 0u);
+                                (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&v_empty[s]);
                 tc_commit(o_done);
             };
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                ok = mbar_wait(&k_full[s], ph, p.status, abort_flag);
+            for (uint32_t k = 0; ok; ++k) {
+                const int slot = k & 3;
+                ok = mbar_wait(&item_full[slot], (k >> 2) & 1, p.status, abort_flag);
+                if (!ok) break;
+                const int i = item_q[slot];
+                mbar_arrive(&item_empty[slot]);
+                if (i < 0) break;
+                const PrefillItem w = prefill_item<PAGED, BN>(p, i);
+                if (w.n_kv == 0) continue;
+                ok = mbar_wait(q_full, q_it & 1, p.status, abort_flag);
                 if (!ok) break;
                 tc_fence_after_sync();
-                const uint32_t k_base = smem_addr(smem + C::OFF_K + s * C::KV_BYTES);
+                const uint32_t base = kv_it;
+                for (int j = 0; j < w.n_kv && ok; ++j) {
+                    const uint32_t g = base + j;
+                    const int s = g & 1;
+                    ok = mbar_wait(&k_full[s], (g >> 1) & 1, p.status, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint32_t k_base = smem_addr(smem + C::OFF_K + s * C::KV_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t c = kk / 4, inner = (kk % 4) * 32;
-                    const uint64_t adesc = smem_desc_sw128(q_base + c * kBM * 128 + inner, 16, 1024);
-                    const uint64_t bdesc =
-                        smem_desc_sw128(k_base + c * C::KV_CHUNK + inner, 16, 1024);
-                    mma_bf16_ss(tmem + C::TM_S + s * BN, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const uint32_t c = kk / 4, inner = (kk % 4) * 32;
+                        const uint64_t adesc =
+                            smem_desc_sw128(q_base + c * kBM * 128 + inner, 16, 1024);
+                        const uint64_t bdesc =
+                            smem_desc_sw128(k_base + c * C::KV_CHUNK + inner, 16, 1024);
+                        mma_bf16_ss(tmem + C::TM_S + s * BN, adesc, bdesc, idesc_s,
+                                    kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&k_empty[s]);
+                    tc_commit(&s_full[s]);
+                    if (j == w.n_kv - 1) tc_commit(q_empty);  // Q is no longer read
+                    if (j >= 1) issue_pv(g - 1, j - 1, w.kv_len);
                 }
-                tc_commit(&k_empty[s]);
-                tc_commit(&s_full[s]);
-                if (j >= 1) issue_pv(j - 1);
+                issue_pv(base + w.n_kv - 1, w.n_kv - 1, w.kv_len);
+                if (ok) tc_commit(o_final);
+                kv_it += w.n_kv;
+                ++q_it;
+                ++o_items;
             }
-            issue_pv(n_kv - 1);
-            if (ok) tc_commit(o_final);
             // never release TMEM / smem with tensor-core work still in flight
             tc_commit(drain);
             const uint64_t t0 = global_timer_ns();
@@ -380,141 +470,166 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
         const int quad = warp & 3;                  // TMEM lane quadrant of this warp
         const int row = quad * 32 + lane;           // query row within the tile
         const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
-        const int q_pos = q0 + row + off;           // last key this row may see (causal)
         const float scale = p.scale_log2;
-        float m = -INFINITY, l = 0.f;
+        uint32_t kv_it = 0, o_items = 0;
         bool ok = true;
-        for (int j = 0; j < n_kv && ok; ++j) {
-            const int s = j & 1;
-            const uint32_t ph = (j >> 1) & 1;
-            ok = mbar_wait(&s_full[s], ph, p.status, abort_flag);
-            if (!ok) break;
-            tc_fence_after_sync();
-            uint32_t sr[BN];
-            if constexpr (BN == 64) {
-                tmem_load_64(tmem + t_lane + C::TM_S + s * BN, sr);
-            } else {
-#pragma unroll
-                for (int c = 0; c < BN / 64; ++c) {
-                    uint32_t (&chunk)[64] = *reinterpret_cast<uint32_t (*)[64]>(&sr[c * 64]);
-                    tmem_load_64(tmem + t_lane + C::TM_S + s * BN + c * 64, chunk);
-                }
-            }
-            const bool need_mask =
-                (j + 1) * BN > kv_len || (p.causal && (j + 1) * BN - 1 > q0 + off);
-            if (need_mask) {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const int kj = j * BN + c;
-                    if (kj >= kv_len || (p.causal && kj > q_pos)) sr[c] = __float_as_uint(-INFINITY);
-                }
-            }
-            // row max of the raw scores (sm_scale > 0, so it scales to the max of s * scale);
-            // eight independent partial maxima keep the dependency chain short
-            float pmax[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) pmax[e] = __uint_as_float(sr[e]);
-#pragma unroll
-            for (int c = 8; c < BN; ++c) pmax[c & 7] = fmaxf(pmax[c & 7], __uint_as_float(sr[c]));
-            const float tmax = fmaxf(fmaxf(fmaxf(pmax[0], pmax[1]), fmaxf(pmax[2], pmax[3])),
-                                     fmaxf(fmaxf(pmax[4], pmax[5]), fmaxf(pmax[6], pmax[7])));
-            const float m_new = fmaxf(m, tmax * scale);   // -inf stays -inf
-            const bool grow = m_new > m + 8.0f;     // lazy rescale threshold: 2^8
-            const float m_use = grow ? m_new : m;
-            const float corr = (m == -INFINITY) ? 0.f : fast_exp2(m - m_use);
-            if (j > 0 && __any_sync(kFullMask, grow)) {
-                // O holds P_0..P_{j-1} V: wait for the last P.V, then rescale in TMEM
-                ok = mbar_wait(o_done, (j - 1) & 1, p.status, abort_flag);
+        for (uint32_t k = 0; ok; ++k) {
+            const int slot = k & 3;
+            ok = mbar_wait(&item_full[slot], (k >> 2) & 1, p.status, abort_flag);
+            if (__any_sync(kFullMask, !ok)) break;
+            const int i = item_q[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[slot]);
+            if (i < 0) break;
+            const PrefillItem w = prefill_item<PAGED, BN>(p, i);
+            if (!w.work) continue;
+            const int off = w.kv_len - w.qo_len;
+            const int q_pos = w.q0 + row + off;     // last key this row may see (causal)
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < w.n_kv && ok; ++j) {
+                const uint32_t g = kv_it + j;
+                const int s = g & 1;
+                ok = mbar_wait(&s_full[s], (g >> 1) & 1, p.status, abort_flag);
                 if (__any_sync(kFullMask, !ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const float f = grow ? corr : 1.f;
+                uint32_t sr[BN];
+                if constexpr (BN == 64) {
+                    tmem_load_64(tmem + t_lane + C::TM_S + s * BN, sr);
+                } else {
 #pragma unroll
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_load_32(tmem + t_lane + C::TM_O + c * 32, o);
+                    for (int c = 0; c < BN / 64; ++c) {
+                        uint32_t (&chunk)[64] = *reinterpret_cast<uint32_t (*)[64]>(&sr[c * 64]);
+                        tmem_load_64(tmem + t_lane + C::TM_S + s * BN + c * 64, chunk);
+                    }
+                }
+                const bool need_mask =
+                    (j + 1) * BN > w.kv_len || (p.causal && (j + 1) * BN - 1 > w.q0 + off);
+                if (need_mask) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tmem_store_32(tmem + t_lane + C::TM_O + c * 32, o);
+                    for (int c = 0; c < BN; ++c) {
+                        const int kj = j * BN + c;
+                        if (kj >= w.kv_len || (p.causal && kj > q_pos))
+                            sr[c] = __float_as_uint(-INFINITY);
+                    }
+                }
+                // row max of the raw scores (sm_scale > 0, so it scales to the max of
+                // s * scale); eight partial maxima keep the dependency chain short
+                float pmax[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pmax[e] = __uint_as_float(sr[e]);
+#pragma unroll
+                for (int c = 8; c < BN; ++c) pmax[c & 7] = fmaxf(pmax[c & 7], __uint_as_float(sr[c]));
+                const float tmax = fmaxf(fmaxf(fmaxf(pmax[0], pmax[1]), fmaxf(pmax[2], pmax[3])),
+                                         fmaxf(fmaxf(pmax[4], pmax[5]), fmaxf(pmax[6], pmax[7])));
+                const float m_new = fmaxf(m, tmax * scale);   // -inf stays -inf
+                const bool grow = m_new > m + 8.0f;     // lazy rescale threshold: 2^8
+                const float m_use = grow ? m_new : m;
+                const float corr = (m == -INFINITY) ? 0.f : fast_exp2(m - m_use);
+                if (j > 0 && __any_sync(kFullMask, grow)) {
+                    // O holds P_0..P_{j-1} V: wait for the last P.V, then rescale in TMEM
+                    ok = mbar_wait(o_done, (g - 1) & 1, p.status, abort_flag);
+                    if (__any_sync(kFullMask, !ok)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const float f = grow ? corr : 1.f;
+#pragma unroll
+                    for (int c = 0; c < HD / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_load_32(tmem + t_lane + C::TM_O + c * 32, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tmem_store_32(tmem + t_lane + C::TM_O + c * 32, o);
+                    }
+                    tmem_store_wait();
+                }
+                if (grow) {
+                    l *= corr;
+                    m = m_use;
+                }
+                // P = 2^(s * scale - m): three pairs in four on the MUFU unit, one on the
+                // FMA pipe (exp2_poly2), so neither unit alone bounds the softmax
+                uint32_t pk[BN / 2];
+                float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                  make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                if (m != -INFINITY) {
+                    const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-m, -m);
+#pragma unroll
+                    for (int c = 0; c < BN / 2; ++c) {
+                        const float2 x = __ffma2_rn(
+                            make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
+                            sc2, nm2);
+                        float2 e;
+                        if ((c & 3) == 3) {
+                            e = exp2_poly2(x);
+                        } else {
+                            e.x = fast_exp2(x.x);
+                            e.y = fast_exp2(x.y);
+                        }
+                        lsum[c & 3] = __fadd2_rn(lsum[c & 3], e);
+                        pk[c] = pack_bf16x2(e.x, e.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;
+                }
+                const float2 ls01 = __fadd2_rn(lsum[0], lsum[1]), ls23 = __fadd2_rn(lsum[2], lsum[3]);
+                const float2 lsum_t = __fadd2_rn(ls01, ls23);
+                l += lsum_t.x + lsum_t.y;
+                if constexpr (BN == 128) {
+                    tmem_store_64(tmem + t_lane + C::TM_S + s * BN, pk);
+                } else {
+                    tmem_store_32(tmem + t_lane + C::TM_S + s * BN,
+                                  *reinterpret_cast<uint32_t (*)[32]>(pk));
                 }
                 tmem_store_wait();
+                tc_fence_before_sync();
+                mbar_arrive(&p_full[s]);
             }
-            if (grow) {
-                l *= corr;
-                m = m_use;
-            }
-            // P = 2^(s * scale - m): three pairs in four on the MUFU unit, one on the
-            // FMA pipe (exp2_poly2), so neither unit alone bounds the softmax
-            uint32_t pk[BN / 2];
-            float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                              make_float2(0.f, 0.f)};
-            if (m != -INFINITY) {
-                const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-m, -m);
-#pragma unroll
-                for (int c = 0; c < BN / 2; ++c) {
-                    const float2 x = __ffma2_rn(
-                        make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
-                        sc2, nm2);
-                    float2 e;
-                    if ((c & 3) == 3) {
-                        e = exp2_poly2(x);
-                    } else {
-                        e.x = fast_exp2(x.x);
-                        e.y = fast_exp2(x.y);
-                    }
-                    lsum[c & 3] = __fadd2_rn(lsum[c & 3], e);
-                    pk[c] = pack_bf16x2(e.x, e.y);
+            if (!ok) break;
+            kv_it += w.n_kv;
+            if (w.n_kv > 0) {
+                ok = mbar_wait(o_final, o_items & 1, p.status, abort_flag);
+                if (__any_sync(kFullMask, !ok)) {
+                    ok = false;
+                    break;
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;
+                tc_fence_after_sync();
             }
-            const float2 ls01 = __fadd2_rn(lsum[0], lsum[1]), ls23 = __fadd2_rn(lsum[2], lsum[3]);
-            const float2 lsum_t = __fadd2_rn(ls01, ls23);
-            l += lsum_t.x + lsum_t.y;
-            if constexpr (BN == 128) {
-                tmem_store_64(tmem + t_lane + C::TM_S + s * BN, pk);
-            } else {
-                tmem_store_32(tmem + t_lane + C::TM_S + s * BN,
-                              *reinterpret_cast<uint32_t (*)[32]>(pk));
-            }
-            tmem_store_wait();
-            tc_fence_before_sync();
-            mbar_arrive(&p_full[s]);
-        }
-        if (n_kv > 0 && ok) {
-            ok = mbar_wait(o_final, 0, p.status, abort_flag);
-            tc_fence_after_sync();
-        }
-        const bool any_bad = __any_sync(kFullMask, !ok);
-        if (work && !any_bad) {
-            const bool row_ok = q0 + row < qo_len;
+            const bool row_ok = w.q0 + row < w.qo_len;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
-                                  (static_cast<int64_t>(qo_start + q0 + row) * p.nq + h) * HD;
+                                  (static_cast<int64_t>(w.qo_start + w.q0 + row) * p.nq + w.h) * HD;
 #pragma unroll
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
-                if (n_kv > 0) {
+                if (w.n_kv > 0) {
                     tmem_load_32(tmem + t_lane + C::TM_O + c * 32, o);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
                 }
-                uint32_t w[16];
+                uint32_t wv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv,
-                                       __uint_as_float(o[2 * e + 1]) * inv);
+                    wv[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv,
+                                        __uint_as_float(o[2 * e + 1]) * inv);
                 if (row_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                    dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+                    dst[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
+                    dst[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
                 }
+            }
+            if (w.n_kv > 0) {
+                tc_fence_before_sync();
+                mbar_arrive(o_free);   // O may be overwritten by the next item
+                ++o_items;
             }
         }
     }
@@ -589,7 +704,7 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
     }
     prefill_schedule_kernel<<<1, 1024, 0, stream>>>(p.qo_indptr, p.kv_indptr, p.batch, p.causal,
                                                     BN, p.n_tiles, const_cast<int2 *>(p.tiles),
-                                                    p.status);
+                                                    p.item_counter, p.status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kern = prefill_kernel<HD, BN, PAGED>;
@@ -604,8 +719,13 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    const dim3 grid(p.nq, p.n_tiles);
-    kern<<<grid, kThreads, C::SMEM, stream>>>(p);
+    static int sms = 0;
+    if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 152;
+    const long long items = static_cast<long long>(p.n_tiles) * p.nq;
+    long long ctas = static_cast<long long>(sms) * C::CTAS_PER_SM;
+    if (items < ctas) ctas = items;
+    kern<<<static_cast<unsigned>(ctas), kThreads, C::SMEM, stream>>>(p);
     return cudaGetLastError();
 }
 
