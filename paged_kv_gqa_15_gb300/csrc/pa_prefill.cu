@@ -77,6 +77,15 @@ __device__ __forceinline__ float2 exp2_poly2(float2 x) {
                        __int_as_float(__float_as_int(pv.y) + (__float_as_int(t.y) << 23)));
 }
 
+// 32-byte store (one full L2 sector per thread); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32B(void *ptr, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                              uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(a0), "r"(a1),
+                 "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
@@ -601,6 +610,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 tc_fence_after_sync();
             }
             const bool row_ok = w.q0 + row < w.qo_len;
+            const bool o_32B = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;  // rows are 32B multiples
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
                                   (static_cast<int64_t>(w.qo_start + w.q0 + row) * p.nq + w.h) * HD;
@@ -618,7 +628,14 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 for (int e = 0; e < 16; ++e)
                     wv[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv,
                                         __uint_as_float(o[2 * e + 1]) * inv);
-                if (row_ok) {
+                // each thread owns one output row, so a warp's store touches 32 rows:
+                // 32-byte stores fill whole sectors (half the sector writes of 16-byte ones)
+                if (row_ok && o_32B) {
+                    st_global_32B(orow + c * 32, wv[0], wv[1], wv[2], wv[3], wv[4], wv[5], wv[6],
+                                  wv[7]);
+                    st_global_32B(orow + c * 32 + 16, wv[8], wv[9], wv[10], wv[11], wv[12], wv[13],
+                                  wv[14], wv[15]);
+                } else if (row_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
                     dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                     dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);

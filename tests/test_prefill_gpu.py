@@ -81,6 +81,40 @@ def test_ragged_multi_tile(hd):
     assert_close_bf16(o, ref, what=f"ragged hd{hd}")
 
 
+@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_query_block_boundaries(hd, causal):
+    # query lengths on both sides of the 128- and 256-row boundaries: a block whose
+    # second tile is empty, partial or full, and keys shorter than the queries
+    qo = [255, 256, 257, 383, 384, 385, 513, 129]
+    kv = [255, 300, 257, 383, 900, 385, 513, 60]
+    o, ref, _ = _contig_case(qo, kv, 4, 2, hd, seed=200 + hd + causal, causal=causal)
+    assert_close_bf16(o, ref, what=f"block boundaries hd{hd} causal={causal}")
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+def test_paged_query_block_boundaries(hd):
+    o, ref, _ = _paged_case([257, 384, 100], [400, 384, 1000], 4, 1, hd, seed=210 + hd)
+    assert_close_bf16(o, ref, what=f"paged block boundaries hd{hd}")
+
+
+def test_output_only_16_byte_aligned():
+    # an output buffer that is 16- but not 32-byte aligned takes the 16-byte store path
+    w = W.make_prefill("al", [200, 70], [200, 300], 4, 2, 128, seed=220)
+    t = w.tensors("cpu")
+    q, k, v = (W.to_bits(t[n]) for n in ("q", "k", "v"))
+    n = q.size
+    backing = torch.full((n + 8,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    o = backing[8:].view(q.shape)
+    assert o.data_ptr() % 32 == 16
+    pa.pa_ragged_prefill(o, _to_dev(q), _to_dev(k), _to_dev(v), w.qo_indptr, w.kv_indptr,
+                         torch.from_numpy(w.qo_indptr).to(DEV), torch.from_numpy(w.kv_indptr).to(DEV),
+                         w.scale, causal=True)
+    torch.cuda.synchronize()
+    ref = oracle.prefill(q, k, v, w.qo_indptr, w.kv_indptr, 2, w.scale, causal=True)
+    assert_close_bf16(o, ref, what="16-byte aligned output")
+
+
 @pytest.mark.parametrize("nq,nkv", [(4, 4), (8, 4), (16, 4), (32, 4)])
 def test_group_sizes(nq, nkv):
     o, ref, _ = _contig_case([200, 77], [200, 300], nq, nkv, 128, seed=nq)
