@@ -11,12 +11,18 @@
 // GB300 design (FlashAttention-style, not the pages' SM80 design):
 //  * Persistent CTAs (two per SM at head_dim <= 128) claim work items -- one
 //    (request, 128-row query tile, query head) each -- from a heaviest-first
-//    list through a global counter; 6 warps per CTA:
-//      warp 0   TMA producer: Q once, then K_j / V_j tiles (128-byte swizzle)
-//               into a 2-stage ring; paged mode issues one box per 16-token page
+//    list through a global counter; the producer decodes each claimed item once
+//    and hands it to the other warps through a 4-deep shared-memory queue.
+//    6 warps per CTA:
+//      warp 0   TMA producer: Q once per item, then K_j / V_j tiles (128-byte
+//               swizzle) into 2-stage rings, K one tile ahead of V (the order the
+//               MMA warp consumes them); paged mode issues one box per 16-token
+//               page and looks each page id up once per tile, a tile early
 //      warp 1   TMEM allocator + single-thread tcgen05.mma issuer:
 //               S_j = Q K_j^T (M=128, N=BN, K=head_dim) into TMEM buffer j%2,
-//               then O += P_{j-1} V_{j-1} with P read straight from TMEM
+//               then O += P_{j-1} V_{j-1} with P read straight from TMEM; two
+//               tcgen05.commits per key tile (S done, P.V done), everything else
+//               (K / Q reuse, O rescale, O final) is read off those two barriers
 //      warps 2-5  softmax: one query row per thread, read S from TMEM, mask,
 //               exp2, write P (bf16) over S in TMEM; epilogue O / l -> bf16
 //  * Online softmax with lazy rescaling: O is rescaled (in TMEM) only when a
@@ -97,11 +103,13 @@ struct PrefillCfg {
     static constexpr uint32_t Q_BYTES = QCH * kBM * 128;
     static constexpr uint32_t KV_CHUNK = BN * 128;            // one chunk of a K / V tile
     static constexpr uint32_t KV_BYTES = QCH * KV_CHUNK;
+    static constexpr int KS = 2;   // K ring stages: one per S buffer (K_j is free once S_j is)
+    static constexpr int VS = 2;                              // V ring stages
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-    static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
-    static constexpr uint32_t SMEM_USED = OFF_BAR + 256;
+    static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
+    static constexpr uint32_t SMEM_USED = OFF_BAR + 512;   // barriers + item queue
     // TMEM: S / P double buffer at columns [0, BN) and [BN, 2 BN), O after them
     static constexpr uint32_t TM_S = 0;
     static constexpr uint32_t TM_O = 2 * BN;
@@ -109,12 +117,16 @@ struct PrefillCfg {
     // Two CTAs share an SM when both fit in its 512 TMEM columns (and in shared
     // memory): their MMA and softmax phases then interleave on the tensor core.
     // A CTA that needs all 512 columns asks for enough shared memory to be alone.
+    // 1024 bytes of slack realign the base for the 128-byte-swizzled tiles.
     static constexpr int CTAS_PER_SM = TMEM_COLS <= 256 ? 2 : 1;
     static constexpr uint32_t SMEM_MIN = CTAS_PER_SM == 2 ? 0 : 118 * 1024;
     static constexpr uint32_t SMEM = (SMEM_USED + 1024 > SMEM_MIN) ? SMEM_USED + 1024 : SMEM_MIN;
     static_assert(HD % 64 == 0 && BN % 16 == 0 && BN <= 128, "tile shape");
+    static_assert(KS == 2 && VS >= 2 && VS <= 4, "ring stages");
     static_assert(TMEM_COLS <= 512, "TMEM budget");
-    static_assert(CTAS_PER_SM == 1 || 2 * SMEM <= 227 * 1024, "two CTAs per SM");
+    // two CTAs, each with the 1 KB the runtime reserves per CTA, in the SM's 228 KB
+    static_assert(CTAS_PER_SM == 1 || 2 * (SMEM + 1024) <= 228 * 1024, "two CTAs per SM");
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
 // Number of key tiles a query tile needs (its work), bottom-right causal.
@@ -180,8 +192,9 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(
 
 // One work item: a 128-row query tile of one request for one query head.
 struct PrefillItem {
-    int r, h, qo_start, qo_len, kv_start, kv_len, q0, n_kv;
-    bool work;  // the tile holds query rows (it is written, possibly with zeros)
+    int r, h, qo_start, qo_len, kv_start, kv_len, q0;
+    int n_kv;   // key tiles; -1 marks the end of the work list
+    int work;   // the tile holds query rows (it is written, possibly with zeros)
 };
 
 template <bool PAGED, int BN>
@@ -205,6 +218,12 @@ __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, long
     return w;
 }
 
+__device__ __forceinline__ PrefillItem end_item() {
+    PrefillItem w{};
+    w.n_kv = -1;
+    return w;
+}
+
 // Persistent: each CTA claims items of the heaviest-first list (item i = query
 // tile i / nq, head i % nq) one at a time from a global counter, so the load
 // balances itself; TMEM and barriers are set up once and the next item's
@@ -217,30 +236,32 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    // A tcgen05.commit costs the single MMA thread far more than an MMA, so each key
+    // tile g (counted over all items of the CTA) has exactly two: s_full[g % 2] when
+    // S_g = Q K_g^T is done and v_empty[g % VS] when O += P_g V_g is done.  Everything
+    // else is read off those two: K_g's stage and (after an item's last tile) Q are
+    // free once S_g is done; O is final, or may be rescaled, once the last issued
+    // P.V is done.  Each of these parity waits is unambiguous because the barrier
+    // can be neither two phases behind the awaited one (the waiter's own previous
+    // wait on it, or the in-order completion of S_g after P_{g-2} V, saw the phase
+    // before) nor one ahead (the next phase needs work the waiter has not released).
     uint64_t *q_full = bars + 0;
-    uint64_t *q_empty = bars + 1;   // committed after an item's last S = Q K^T
-    uint64_t *k_full = bars + 2;    // [2]
-    uint64_t *k_empty = bars + 4;   // [2]
-    uint64_t *v_full = bars + 6;    // [2]
-    uint64_t *v_empty = bars + 8;   // [2]
-    uint64_t *s_full = bars + 10;   // [2]
-    uint64_t *p_full = bars + 12;   // [2]
-    // o_done completes one phase per P.V (counted over all items).  While softmax
-    // works on key tile j only P_{j-1} V can be pending (S_j completing implies
-    // P_{j-2} V completed, and the previous item finished before), so a parity wait
-    // on it is unambiguous; an item's epilogue waits on o_final instead (committed
-    // after the item's last P.V), and hands O back with o_free.
-    uint64_t *o_done = bars + 14;
-    uint64_t *o_final = bars + 15;
-    uint64_t *o_free = bars + 16;
-    uint64_t *drain = bars + 17;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 19);
+    uint64_t *k_full = bars + 2;    // [KS]
+    uint64_t *v_full = bars + 10;   // [VS]
+    uint64_t *v_empty = bars + 14;  // [VS]
+    uint64_t *s_full = bars + 18;   // [2]
+    uint64_t *p_full = bars + 20;   // [2]
+    uint64_t *o_free = bars + 24;   // the epilogue has read O (arrive by 128 threads)
+    uint64_t *drain = bars + 25;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 26);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 27);
     // Work items are claimed dynamically (atomicAdd on a global counter) by the
-    // producer and handed to the MMA and softmax warps through a 4-deep queue.
-    uint64_t *item_full = bars + 20;   // [4]
-    uint64_t *item_empty = bars + 24;  // [4]: released by the MMA thread + 4 softmax warps
-    volatile int *item_q = reinterpret_cast<volatile int *>(bars + 28);  // [4]
+    // producer, decoded once (the tile list and indptr reads are two dependent
+    // global round trips) and handed to the MMA and softmax warps, decoded, through
+    // a 4-deep queue in shared memory.
+    uint64_t *item_full = bars + 28;   // [4]
+    uint64_t *item_empty = bars + 32;  // [4]: released by the MMA thread + 4 softmax warps
+    PrefillItem *item_q = reinterpret_cast<PrefillItem *>(bars + 40);  // [4]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -249,17 +270,17 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::KS; ++s) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < C::VS; ++s) {
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], 128);
         }
-        mbar_init(o_done, 1);
-        mbar_init(o_final, 1);
         mbar_init(o_free, 128);
         mbar_init(drain, 1);
         for (int k = 0; k < 4; ++k) {
@@ -285,45 +306,50 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             prefetch_tensormap(&p.tm_k);
             prefetch_tensormap(&p.tm_v);
         }
-        uint32_t kv_it = 0, q_it = 0;
+        uint32_t kv_it = 0;
         int stop = 0;
-        // Claims the k-th item of this CTA and publishes it to the MMA and softmax
-        // warps; returns the item index, or -1 when the list is exhausted.
-        auto claim = [&](uint32_t k) -> int {
-            int i = -1;
+        // Claims the k-th item of this CTA, decodes it and publishes it to the MMA
+        // and softmax warps; an item with n_kv == -1 ends the list.
+        auto claim = [&](uint32_t k) -> PrefillItem {
+            const int slot = k & 3;
             if (lane == 0) {
-                const int slot = k & 3;
                 if (!mbar_wait(&item_empty[slot], ((k >> 2) & 1) ^ 1u, p.status, abort_flag)) {
                     stop = 1;
                 } else {
                     const long long claimed = atomicAdd(p.item_counter, 1);
-                    i = claimed < n_items ? static_cast<int>(claimed) : -1;
-                    item_q[slot] = i;
+                    item_q[slot] =
+                        claimed < n_items ? prefill_item<PAGED, BN>(p, claimed) : end_item();
                     mbar_arrive(&item_full[slot]);
                 }
             }
+            __syncwarp();
             stop = __shfl_sync(kFullMask, stop, 0);
-            return stop ? -1 : __shfl_sync(kFullMask, i, 0);
+            return stop ? end_item() : item_q[slot];
         };
-        // Page id of page `pidx` of request r for lanes that ask (pages past the
-        // sequence or bad ids -> num_blocks, an out-of-range box that reads zeros).
-        auto page_of = [&](int r, int pidx, int pages_seq, bool ask) -> int {
-            int page = -1;
-            const bool in_seq = ask && pidx < pages_seq;
-            if (in_seq) page = p.block_tables[static_cast<int64_t>(r) * p.max_blocks + pidx];
-            const bool bad = in_seq && (page < 0 || page >= p.num_blocks);
+        // Block-table entry of page `lane` of key tile j (lanes < BN / 16); -2 for
+        // lanes and pages past the sequence.  Issued a tile early, checked at use.
+        auto page_raw = [&](int r, int j, int pages_seq) -> int {
+            const int pidx = j * (BN / kBlockSize) + lane;
+            if (lane >= BN / kBlockSize || pidx >= pages_seq) return -2;
+            return p.block_tables[static_cast<int64_t>(r) * p.max_blocks + pidx];
+        };
+        // Bad ids are flagged; they and pages past the sequence become num_blocks, an
+        // out-of-range box that reads zeros.
+        auto page_fix = [&](int raw) -> int {
+            const bool bad = raw != -2 && (raw < 0 || raw >= p.num_blocks);
             if (__any_sync(kFullMask, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
-            return (!in_seq || bad) ? static_cast<int>(p.num_blocks) : page;
+            return (raw == -2 || bad) ? static_cast<int>(p.num_blocks) : raw;
         };
         for (uint32_t k = 0; !stop; ++k) {
-            const int cur = claim(k);
-            if (stop || cur < 0) break;
-            const PrefillItem w = prefill_item<PAGED, BN>(p, cur);
+            const PrefillItem w = claim(k);
+            if (stop || w.n_kv < 0) break;
             if (w.n_kv == 0) continue;
             const int kh = w.h / group;
 
             if (lane == 0) {
-                if (!mbar_wait(q_empty, (q_it & 1) ^ 1u, p.status, abort_flag)) {
+                // Q is reused once the previous item's last S (tile kv_it - 1) is done
+                if (kv_it > 0 && !mbar_wait(&s_full[(kv_it - 1) & 1], ((kv_it - 1) >> 1) & 1,
+                                            p.status, abort_flag)) {
                     stop = 1;
                 } else {
                     mbar_arrive_expect_tx(q_full, C::Q_BYTES);
@@ -334,47 +360,67 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             }
             stop = __shfl_sync(kFullMask, stop, 0);
             if (stop) break;
-            ++q_it;
             const int pages_seq = (w.kv_len + kBlockSize - 1) / kBlockSize;
-            for (int j = 0; j < w.n_kv && !stop; ++j, ++kv_it) {
-                const int s = kv_it & 1;
-                const uint32_t ph = ((kv_it >> 1) & 1) ^ 1u;
-                int page = 0;
-                if constexpr (PAGED)
-                    page = page_of(w.r, j * (BN / kBlockSize) + lane, pages_seq,
-                                   lane < BN / kBlockSize);
-                for (int kv = 0; kv < 2; ++kv) {
-                    uint64_t *full = kv ? &v_full[s] : &k_full[s];
-                    uint64_t *empty = kv ? &v_empty[s] : &k_empty[s];
-                    const CUtensorMap *tm = kv ? &p.tm_v : &p.tm_k;
-                    uint8_t *dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::KV_BYTES;
-                    if (lane == 0) {
-                        if (!mbar_wait(empty, ph, p.status, abort_flag)) {
-                            stop = 1;
-                        } else {
-                            mbar_arrive_expect_tx(full, C::KV_BYTES);
-                            if constexpr (!PAGED) {
-                                for (int c = 0; c < C::QCH; ++c)
-                                    tma_load_3d(dst + c * C::KV_CHUNK, tm, c * 64, kh,
-                                                w.kv_start + j * BN, full);
-                            }
-                        }
-                    }
-                    stop = __shfl_sync(kFullMask, stop, 0);
-                    if (stop) break;
-                    if constexpr (PAGED) {
-#pragma unroll
-                        for (int e = 0; e < BN / kBlockSize; ++e) {
-                            const int pg = __shfl_sync(kFullMask, page, e);
-                            if (lane == 0) {
-                                for (int c = 0; c < C::QCH; ++c)
-                                    tma_load_4d(dst + c * C::KV_CHUNK + e * kBlockSize * 128, tm,
-                                                c * 64, 0, kh, pg, full);
-                            }
+            // Loads key tile j (kv = 0) or value tile j (kv = 1) of this item into its
+            // ring stage; g is the tile's index over all items of this CTA.
+            auto load_tile = [&](int kv, int j, uint32_t g, int page) {
+                const int ns = kv ? C::VS : C::KS;
+                const int s = g % ns;
+                const uint32_t ph = ((g / ns) & 1) ^ 1u;
+                uint64_t *full = kv ? &v_full[s] : &k_full[s];
+                uint64_t *empty = kv ? &v_empty[s] : &s_full[s];   // K stage s == S buffer s
+                const CUtensorMap *tm = kv ? &p.tm_v : &p.tm_k;
+                uint8_t *dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::KV_BYTES;
+                if (lane == 0) {
+                    if (!mbar_wait(empty, ph, p.status, abort_flag)) {
+                        stop = 1;
+                    } else {
+                        mbar_arrive_expect_tx(full, C::KV_BYTES);
+                        if constexpr (!PAGED) {
+                            for (int c = 0; c < C::QCH; ++c)
+                                tma_load_3d(dst + c * C::KV_CHUNK, tm, c * 64, kh,
+                                            w.kv_start + j * BN, full);
                         }
                     }
                 }
+                stop = __shfl_sync(kFullMask, stop, 0);
+                if (stop) return;
+                if constexpr (PAGED) {
+#pragma unroll
+                    for (int e = 0; e < BN / kBlockSize; ++e) {
+                        const int pg = __shfl_sync(kFullMask, page, e);
+                        if (lane == 0) {
+                            for (int c = 0; c < C::QCH; ++c)
+                                tma_load_4d(dst + c * C::KV_CHUNK + e * kBlockSize * 128, tm,
+                                            c * 64, 0, kh, pg, full);
+                        }
+                    }
+                }
+            };
+            // The MMA warp consumes K_{j+1} (for S_{j+1}) before V_j (for P_j V_j), so K
+            // runs one tile ahead: a K load then never waits behind a V stage, whose
+            // release depends on the softmax of an earlier tile.
+            // Pages are looked up once per tile (K_j and V_j share them), one tile
+            // ahead of their use.
+            int pg_cur = 0, raw_next = -2;
+            if constexpr (PAGED) {
+                pg_cur = page_fix(page_raw(w.r, 0, pages_seq));
+                if (w.n_kv > 1) raw_next = page_raw(w.r, 1, pages_seq);
             }
+            load_tile(0, 0, kv_it, pg_cur);
+            for (int j = 0; j < w.n_kv && !stop; ++j) {
+                int pg_next = 0;
+                if (j + 1 < w.n_kv) {
+                    if constexpr (PAGED) {
+                        pg_next = page_fix(raw_next);
+                        if (j + 2 < w.n_kv) raw_next = page_raw(w.r, j + 2, pages_seq);
+                    }
+                    load_tile(0, j + 1, kv_it + j + 1, pg_next);
+                }
+                if (!stop) load_tile(1, j, kv_it + j, pg_cur);
+                pg_cur = pg_next;
+            }
+            kv_it += w.n_kv;
         }
     } else if (warp == 1) {
         // -------------------------------- MMA issuer --------------------------------
@@ -387,12 +433,12 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             // O += P_g V_g for global key tile g (tile jj of an item with kv_len keys)
             auto issue_pv = [&](uint32_t g, int jj, int kv_len) {
                 if (!ok) return;
-                const int s = g & 1;
-                const uint32_t ph = (g >> 1) & 1;
+                const int b = g & 1;          // S / P buffer
+                const int s = g % C::VS;      // V stage
                 if (jj == 0 && o_items > 0)  // the previous item's epilogue has read O
                     ok = mbar_wait(o_free, (o_items - 1) & 1, p.status, abort_flag);
-                ok = ok && mbar_wait(&p_full[s], ph, p.status, abort_flag) &&
-                     mbar_wait(&v_full[s], ph, p.status, abort_flag);
+                ok = ok && mbar_wait(&p_full[b], (g >> 1) & 1, p.status, abort_flag) &&
+                     mbar_wait(&v_full[s], (g / C::VS) & 1, p.status, abort_flag);
                 if (!ok) return;
                 tc_fence_after_sync();
                 if constexpr (PAGED) {
@@ -416,20 +462,18 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint64_t bdesc =
                         smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
-                    mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + s * BN + kk * 8, bdesc, idesc_o,
+                    mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + b * BN + kk * 8, bdesc, idesc_o,
                                 (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&v_empty[s]);
-                tc_commit(o_done);
             };
             for (uint32_t k = 0; ok; ++k) {
                 const int slot = k & 3;
                 ok = mbar_wait(&item_full[slot], (k >> 2) & 1, p.status, abort_flag);
                 if (!ok) break;
-                const int i = item_q[slot];
+                const PrefillItem w = item_q[slot];
                 mbar_arrive(&item_empty[slot]);
-                if (i < 0) break;
-                const PrefillItem w = prefill_item<PAGED, BN>(p, i);
+                if (w.n_kv < 0) break;
                 if (w.n_kv == 0) continue;
                 ok = mbar_wait(q_full, q_it & 1, p.status, abort_flag);
                 if (!ok) break;
@@ -437,8 +481,9 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 const uint32_t base = kv_it;
                 for (int j = 0; j < w.n_kv && ok; ++j) {
                     const uint32_t g = base + j;
-                    const int s = g & 1;
-                    ok = mbar_wait(&k_full[s], (g >> 1) & 1, p.status, abort_flag);
+                    const int s = g % C::KS;      // K stage
+                    const int b = g & 1;          // S / P buffer
+                    ok = mbar_wait(&k_full[s], (g / C::KS) & 1, p.status, abort_flag);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t k_base = smem_addr(smem + C::OFF_K + s * C::KV_BYTES);
@@ -449,16 +494,13 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                             smem_desc_sw128(q_base + c * kBM * 128 + inner, 16, 1024);
                         const uint64_t bdesc =
                             smem_desc_sw128(k_base + c * C::KV_CHUNK + inner, 16, 1024);
-                        mma_bf16_ss(tmem + C::TM_S + s * BN, adesc, bdesc, idesc_s,
+                        mma_bf16_ss(tmem + C::TM_S + b * BN, adesc, bdesc, idesc_s,
                                     kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(&k_empty[s]);
-                    tc_commit(&s_full[s]);
-                    if (j == w.n_kv - 1) tc_commit(q_empty);  // Q is no longer read
+                    tc_commit(&s_full[b]);
                     if (j >= 1) issue_pv(g - 1, j - 1, w.kv_len);
                 }
                 issue_pv(base + w.n_kv - 1, w.n_kv - 1, w.kv_len);
-                if (ok) tc_commit(o_final);
                 kv_it += w.n_kv;
                 ++q_it;
                 ++o_items;
@@ -480,17 +522,16 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
         const int row = quad * 32 + lane;           // query row within the tile
         const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
         const float scale = p.scale_log2;
-        uint32_t kv_it = 0, o_items = 0;
+        uint32_t kv_it = 0;
         bool ok = true;
         for (uint32_t k = 0; ok; ++k) {
             const int slot = k & 3;
             ok = mbar_wait(&item_full[slot], (k >> 2) & 1, p.status, abort_flag);
             if (__any_sync(kFullMask, !ok)) break;
-            const int i = item_q[slot];
+            const PrefillItem w = item_q[slot];
             __syncwarp();
             if (lane == 0) mbar_arrive(&item_empty[slot]);
-            if (i < 0) break;
-            const PrefillItem w = prefill_item<PAGED, BN>(p, i);
+            if (w.n_kv < 0) break;
             if (!w.work) continue;
             const int off = w.kv_len - w.qo_len;
             const int q_pos = w.q0 + row + off;     // last key this row may see (causal)
@@ -517,12 +558,12 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 const bool need_mask =
                     (j + 1) * BN > w.kv_len || (p.causal && (j + 1) * BN - 1 > w.q0 + off);
                 if (need_mask) {
+                    // the visible keys of this row form a prefix of the tile: columns < lim
+                    int lim = w.kv_len - j * BN;
+                    if (p.causal) lim = min(lim, q_pos + 1 - j * BN);
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) {
-                        const int kj = j * BN + c;
-                        if (kj >= w.kv_len || (p.causal && kj > q_pos))
-                            sr[c] = __float_as_uint(-INFINITY);
-                    }
+                    for (int c = 0; c < BN; ++c)
+                        if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
                 }
                 // row max of the raw scores (sm_scale > 0, so it scales to the max of
                 // s * scale); eight partial maxima keep the dependency chain short
@@ -539,7 +580,8 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 const float corr = (m == -INFINITY) ? 0.f : fast_exp2(m - m_use);
                 if (j > 0 && __any_sync(kFullMask, grow)) {
                     // O holds P_0..P_{j-1} V: wait for the last P.V, then rescale in TMEM
-                    ok = mbar_wait(o_done, (g - 1) & 1, p.status, abort_flag);
+                    ok = mbar_wait(&v_empty[(g - 1) % C::VS], ((g - 1) / C::VS) & 1, p.status,
+                                   abort_flag);
                     if (__any_sync(kFullMask, !ok)) {
                         ok = false;
                         break;
@@ -601,35 +643,48 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             }
             if (!ok) break;
             kv_it += w.n_kv;
-            if (w.n_kv > 0) {
-                ok = mbar_wait(o_final, o_items & 1, p.status, abort_flag);
+            if (w.n_kv > 0) {   // O is final once the item's last P.V (tile kv_it - 1) is done
+                ok = mbar_wait(&v_empty[(kv_it - 1) % C::VS], ((kv_it - 1) / C::VS) & 1, p.status,
+                               abort_flag);
                 if (__any_sync(kFullMask, !ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
             }
-            const bool row_ok = w.q0 + row < w.qo_len;
-            const bool o_32B = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;  // rows are 32B multiples
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
-                                  (static_cast<int64_t>(w.qo_start + w.q0 + row) * p.nq + w.h) * HD;
-#pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
+            // O / l -> bf16, 32 columns at a time (o_free is released as soon as the
+            // last columns have left TMEM)
+            auto o_chunk = [&](int c, uint32_t (&wv)[16]) {
                 uint32_t o[32];
                 if (w.n_kv > 0) {
                     tmem_load_32(tmem + t_lane + C::TM_O + c * 32, o);
+                    if (c == HD / 32 - 1) {
+                        tc_fence_before_sync();
+                        mbar_arrive(o_free);   // O may be overwritten by the next item
+                    }
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0u;
                 }
-                uint32_t wv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     wv[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv,
                                         __uint_as_float(o[2 * e + 1]) * inv);
-                // each thread owns one output row, so a warp's store touches 32 rows:
-                // 32-byte stores fill whole sectors (half the sector writes of 16-byte ones)
+            };
+            // Each thread owns one output row, so a warp's store touches 32 rows; 32-byte
+            // stores (when o is 32-byte aligned: rows are multiples of 32 bytes) fill
+            // whole sectors.  Staging through shared memory for wider coalescing, or a
+            // TMA store of full tiles, measured slower here (the epilogue sits on the
+            // softmax warps' critical path and both add latency).
+            const bool row_ok = w.q0 + row < w.qo_len;
+            const bool o_32B = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
+                                  (static_cast<int64_t>(w.qo_start + w.q0 + row) * p.nq + w.h) * HD;
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t wv[16];
+                o_chunk(c, wv);
                 if (row_ok && o_32B) {
                     st_global_32B(orow + c * 32, wv[0], wv[1], wv[2], wv[3], wv[4], wv[5], wv[6],
                                   wv[7]);
@@ -642,11 +697,6 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                     dst[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
                     dst[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
                 }
-            }
-            if (w.n_kv > 0) {
-                tc_fence_before_sync();
-                mbar_arrive(o_free);   // O may be overwritten by the next item
-                ++o_items;
             }
         }
     }
