@@ -43,11 +43,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # for the source file hash they were measured on (otherwise reported as null).
 TRAFFIC = {
     # ncu capture of one decode_kernel<128,4,persistent> launch on the Llama-8B decode
-    # workload: dram__bytes_read.sum 568.39 MB + dram__bytes_write.sum 5.43 MB
+    # workload: dram__bytes_read.sum 568.38 MB + dram__bytes_write.sum 5.44 MB
     "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
-        "src": "b593ae57d3f2f152", "bytes_per_launch": 573817344},
+        "src": "2f606a466f1fd67e", "bytes_per_launch": 573826560},
+    # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
+    # causal prefill: dram__bytes_read.sum 298.72 MB + dram__bytes_write.sum 109.05 MB
+    "ragged_prefill:ragged_prefill_r16_h32kv8_d128": {
+        "src": "924f90cd0af3f0e0", "bytes_per_launch": 407768320},
 }
-
 
 # ---------------------------------------------------------------------------------------
 # host-side helpers (also exercised by the CPU tests)
