@@ -60,29 +60,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// 2^x for a pair, on the FMA / ALU pipes instead of the MUFU unit (so the two
-// can share the softmax's exponentials).  Range reduction 2^x = 2^n * 2^f with
-// n = round(x) taken from the low mantissa bits of x + 1.5 * 2^23, f in
-// [-0.5, 0.5]; 2^f by a cubic minimax fit on that interval (max relative error
-// 7.5e-5, far below the bf16 rounding that P gets next); 2^n added straight to
-// the exponent bits.  x is clamped at -125 so the exponent never underflows:
-// masked scores (-inf) come out as ~2e-38 instead of 0, which no bf16 sum of P
-// or P.V can see.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 t = __fadd2_rn(x, make_float2(kMagic, kMagic));
-    const float2 n = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
-    const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
-    float2 pv = __ffma2_rn(f, make_float2(0.055171505f, 0.055171505f),
-                           make_float2(0.24261115f, 0.24261115f));
-    pv = __ffma2_rn(f, pv, make_float2(0.693261f, 0.693261f));
-    pv = __ffma2_rn(f, pv, make_float2(0.99992806f, 0.99992806f));
-    return make_float2(__int_as_float(__float_as_int(pv.x) + (__float_as_int(t.x) << 23)),
-                       __int_as_float(__float_as_int(pv.y) + (__float_as_int(t.y) << 23)));
-}
-
 // 32-byte store (one full L2 sector per thread); the address must be 32-byte aligned.
 __device__ __forceinline__ void st_global_32B(void *ptr, uint32_t a0, uint32_t a1, uint32_t a2,
                                               uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
@@ -95,6 +72,79 @@ __device__ __forceinline__ void st_global_32B(void *ptr, uint32_t a0, uint32_t a
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// max(a, b, c) in one instruction (three-input max.f32 of the sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Online-softmax state of one query row; m is a running max of s * scale (log2 units).
+struct RowSoftmax {
+    float m, l;
+};
+
+// Masks columns >= lim of a key tile (when need_mask: the visible keys of a row are a
+// prefix of the tile), takes the row max and makes the lazy-rescale decision: m moves
+// only when the max grows by more than 2^8.  Returns whether it moves; m_use is the
+// max the tile's P is then taken against and corr the factor O and l are scaled by.
+template <int BN>
+__device__ __forceinline__ bool tile_max(uint32_t (&sr)[BN], bool need_mask, int lim, float scale,
+                                         const RowSoftmax &rs, float &m_use, float &corr) {
+    if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+            if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+    }
+    // row max of the raw scores (sm_scale > 0, so it scales to the max of s * scale);
+    // eight partial maxima, each taking two new columns per three-input max, keep the
+    // dependency chains short
+    static_assert(BN % 16 == 0, "row max works in groups of 16 columns");
+    float pmax[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) pmax[e] = fmaxf(__uint_as_float(sr[e]), __uint_as_float(sr[8 + e]));
+#pragma unroll
+    for (int c = 16; c < BN; c += 16)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            pmax[e] = fmax3(pmax[e], __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 8 + e]));
+    const float tmax = fmax3(fmax3(pmax[0], pmax[1], pmax[2]), fmax3(pmax[3], pmax[4], pmax[5]),
+                             fmaxf(pmax[6], pmax[7]));
+    const float m_new = fmaxf(rs.m, tmax * scale);   // -inf stays -inf
+    const bool grow = m_new > rs.m + 8.0f;
+    m_use = grow ? m_new : rs.m;
+    corr = (rs.m == -INFINITY) ? 0.f : fast_exp2(rs.m - m_use);
+    return grow;
+}
+
+// P = 2^(s * scale - m) for a key tile, packed to bf16 pairs, and its row sum added
+// to l.  All exponentials go to the MUFU unit: the softmax is bound by its issue
+// slots and latency, not by MUFU throughput, so moving some of them to an FMA-pipe
+// polynomial (more instructions per exponential) measured slower.
+template <int BN>
+__device__ __forceinline__ void tile_exp(const uint32_t (&sr)[BN], float scale, RowSoftmax &rs,
+                                         uint32_t (&pk)[BN / 2]) {
+    float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
+    if (rs.m != -INFINITY) {
+        const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-rs.m, -rs.m);
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) {
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nm2);
+            const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            lsum[c & 3] = __fadd2_rn(lsum[c & 3], e);
+            pk[c] = pack_bf16x2(e.x, e.y);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;
+    }
+    const float2 ls01 = __fadd2_rn(lsum[0], lsum[1]), ls23 = __fadd2_rn(lsum[2], lsum[3]);
+    const float2 lsum_t = __fadd2_rn(ls01, ls23);
+    rs.l += lsum_t.x + lsum_t.y;
 }
 
 template <int HD, int BN>
@@ -250,8 +300,11 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
     uint64_t *v_full = bars + 10;   // [VS]
     uint64_t *v_empty = bars + 14;  // [VS]
     uint64_t *s_full = bars + 18;   // [2]
-    uint64_t *p_full = bars + 20;   // [2]
-    uint64_t *o_free = bars + 24;   // the epilogue has read O (arrive by 128 threads)
+    // p_full and o_free take one arrival per softmax warp (lane 0, after the warp's
+    // tcgen05 fences and a __syncwarp): 128 per-thread arrivals on one mbarrier are
+    // serialised and sat on the softmax -> MMA critical path.
+    uint64_t *p_full = bars + 20;   // [2]: P_j is in TMEM
+    uint64_t *o_free = bars + 24;   // the epilogue has read O
     uint64_t *drain = bars + 25;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 26);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 27);
@@ -279,9 +332,9 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&s_full[s], 1);
-            mbar_init(&p_full[s], 128);
+            mbar_init(&p_full[s], 4);
         }
-        mbar_init(o_free, 128);
+        mbar_init(o_free, 4);
         mbar_init(drain, 1);
         for (int k = 0; k < 4; ++k) {
             mbar_init(&item_full[k], 1);
@@ -535,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             if (!w.work) continue;
             const int off = w.kv_len - w.qo_len;
             const int q_pos = w.q0 + row + off;     // last key this row may see (causal)
-            float m = -INFINITY, l = 0.f;
+            RowSoftmax rs{-INFINITY, 0.f};
             for (int j = 0; j < w.n_kv && ok; ++j) {
                 const uint32_t g = kv_it + j;
                 const int s = g & 1;
@@ -557,27 +610,9 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 }
                 const bool need_mask =
                     (j + 1) * BN > w.kv_len || (p.causal && (j + 1) * BN - 1 > w.q0 + off);
-                if (need_mask) {
-                    // the visible keys of this row form a prefix of the tile: columns < lim
-                    int lim = w.kv_len - j * BN;
-                    if (p.causal) lim = min(lim, q_pos + 1 - j * BN);
-#pragma unroll
-                    for (int c = 0; c < BN; ++c)
-                        if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
-                }
-                // row max of the raw scores (sm_scale > 0, so it scales to the max of
-                // s * scale); eight partial maxima keep the dependency chain short
-                float pmax[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) pmax[e] = __uint_as_float(sr[e]);
-#pragma unroll
-                for (int c = 8; c < BN; ++c) pmax[c & 7] = fmaxf(pmax[c & 7], __uint_as_float(sr[c]));
-                const float tmax = fmaxf(fmaxf(fmaxf(pmax[0], pmax[1]), fmaxf(pmax[2], pmax[3])),
-                                         fmaxf(fmaxf(pmax[4], pmax[5]), fmaxf(pmax[6], pmax[7])));
-                const float m_new = fmaxf(m, tmax * scale);   // -inf stays -inf
-                const bool grow = m_new > m + 8.0f;     // lazy rescale threshold: 2^8
-                const float m_use = grow ? m_new : m;
-                const float corr = (m == -INFINITY) ? 0.f : fast_exp2(m - m_use);
+                const int lim = min(w.kv_len, p.causal ? q_pos + 1 : w.kv_len) - j * BN;
+                float m_use, corr;
+                const bool grow = tile_max<BN>(sr, need_mask, lim, scale, rs, m_use, corr);
                 if (j > 0 && __any_sync(kFullMask, grow)) {
                     // O holds P_0..P_{j-1} V: wait for the last P.V, then rescale in TMEM
                     ok = mbar_wait(&v_empty[(g - 1) % C::VS], ((g - 1) / C::VS) & 1, p.status,
@@ -599,38 +634,11 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                     tmem_store_wait();
                 }
                 if (grow) {
-                    l *= corr;
-                    m = m_use;
+                    rs.l *= corr;
+                    rs.m = m_use;
                 }
-                // P = 2^(s * scale - m): three pairs in four on the MUFU unit, one on the
-                // FMA pipe (exp2_poly2), so neither unit alone bounds the softmax
                 uint32_t pk[BN / 2];
-                float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                  make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                if (m != -INFINITY) {
-                    const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(-m, -m);
-#pragma unroll
-                    for (int c = 0; c < BN / 2; ++c) {
-                        const float2 x = __ffma2_rn(
-                            make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
-                            sc2, nm2);
-                        float2 e;
-                        if ((c & 3) == 3) {
-                            e = exp2_poly2(x);
-                        } else {
-                            e.x = fast_exp2(x.x);
-                            e.y = fast_exp2(x.y);
-                        }
-                        lsum[c & 3] = __fadd2_rn(lsum[c & 3], e);
-                        pk[c] = pack_bf16x2(e.x, e.y);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < BN / 2; ++c) pk[c] = 0u;
-                }
-                const float2 ls01 = __fadd2_rn(lsum[0], lsum[1]), ls23 = __fadd2_rn(lsum[2], lsum[3]);
-                const float2 lsum_t = __fadd2_rn(ls01, ls23);
-                l += lsum_t.x + lsum_t.y;
+                tile_exp<BN>(sr, scale, rs, pk);
                 if constexpr (BN == 128) {
                     tmem_store_64(tmem + t_lane + C::TM_S + s * BN, pk);
                 } else {
@@ -639,7 +647,8 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 }
                 tmem_store_wait();
                 tc_fence_before_sync();
-                mbar_arrive(&p_full[s]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[s]);
             }
             if (!ok) break;
             kv_it += w.n_kv;
@@ -652,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 }
                 tc_fence_after_sync();
             }
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = rs.l > 0.f ? 1.f / rs.l : 0.f;
             // O / l -> bf16, 32 columns at a time (o_free is released as soon as the
             // last columns have left TMEM)
             auto o_chunk = [&](int c, uint32_t (&wv)[16]) {
@@ -661,7 +670,8 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                     tmem_load_32(tmem + t_lane + C::TM_O + c * 32, o);
                     if (c == HD / 32 - 1) {
                         tc_fence_before_sync();
-                        mbar_arrive(o_free);   // O may be overwritten by the next item
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(o_free);   // O may be overwritten next
                     }
                 } else {
 #pragma unroll
@@ -774,13 +784,15 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
                                                     p.item_counter, p.status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto kern = prefill_kernel<HD, BN, PAGED>;
+    const void *kern = reinterpret_cast<const void *>(prefill_kernel<HD, BN, PAGED>);
+    const uint32_t smem = C::SMEM;
+    const int per_sm = C::CTAS_PER_SM, threads = kThreads;
     static int configured_device = -1;
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
@@ -790,9 +802,12 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
     if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 152;
     const long long items = static_cast<long long>(p.n_tiles) * p.nq;
-    long long ctas = static_cast<long long>(sms) * C::CTAS_PER_SM;
+    long long ctas = static_cast<long long>(sms) * per_sm;
     if (items < ctas) ctas = items;
-    kern<<<static_cast<unsigned>(ctas), kThreads, C::SMEM, stream>>>(p);
+    void *args[] = {&p};
+    e = cudaLaunchKernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(threads), args, smem,
+                         stream);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
