@@ -244,9 +244,12 @@ def flush_l2(stream, device):
 
 def time_steps(step, steps, warmup, stream, device, labels, flush=False):
     """Warm up, then time exactly `steps` steps with CUDA events on `stream`.
-    With flush, L2 is flushed before every step outside the timed intervals and the
-    step time is the sum of its kernels' intervals.  Returns (ms per step,
-    {label: avg ms}, launches)."""
+    Without flush the step time comes from one pass with events only around the whole
+    loop (nothing between a step's kernels, so back-to-back launches may overlap as in
+    use); a second pass of `steps` steps with an event after every kernel gives the
+    per-kernel times.  With flush, L2 is flushed before every step outside the timed
+    intervals and the step time is the sum of its kernels' intervals.
+    Returns (ms per step, {label: avg ms}, launches per timed pass)."""
     import torch.distributed as dist
     for _ in range(warmup):
         if flush:
@@ -256,16 +259,22 @@ def time_steps(step, steps, warmup, stream, device, labels, flush=False):
     if dist.is_available() and dist.is_initialized():
         dist.barrier()
     torch.cuda.synchronize()
+    ms_whole = None
+    if not flush:
+        start = _ev(stream)
+        for _ in range(steps):
+            step(None)
+        end = _ev(stream)
+        torch.cuda.synchronize()
+        ms_whole = start.elapsed_time(end) / steps
     all_evs = []
     launches = 0
-    start = _ev(stream)
     for _ in range(steps):
         if flush:
             flush_l2(stream, device)
         evs = []
         launches += step(evs)
         all_evs.append(evs)
-    end = _ev(stream)
     torch.cuda.synchronize()
     if dist.is_available() and dist.is_initialized():
         dist.barrier()
@@ -274,7 +283,7 @@ def time_steps(step, steps, warmup, stream, device, labels, flush=False):
         for i, l in enumerate(labels):
             per[l] += evs[i].elapsed_time(evs[i + 1])
     per = {l: v / steps for l, v in per.items()}
-    ms = sum(per.values()) if flush else start.elapsed_time(end) / steps
+    ms = sum(per.values()) if flush else ms_whole
     return ms, per, launches
 
 

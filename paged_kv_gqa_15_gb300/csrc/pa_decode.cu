@@ -161,6 +161,10 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_ABORT);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Launched as a programmatic dependent of the previous kernel in the stream (the
+    // cache write): the launch and CTA start-up overlap it, nothing it may have
+    // written is read before it has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     long long total = 0;
     if constexpr (MODE == kSplitPersistent) {
@@ -570,6 +574,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Deco
     constexpr int PL = 256 / DG;   // partition lanes
     __shared__ float red[PL][HD];
     __shared__ float stat[8];
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the partials are complete
     const int h = blockIdx.x, b = blockIdx.y;
     const int nq = p.num_q_heads;
     int L = p.seq_lens[b];
@@ -624,6 +629,27 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Deco
     }
 }
 
+// Launches a kernel as a programmatic dependent of the previous work in the stream:
+// its CTAs may start while that work finishes, and wait for it (griddepcontrol.wait)
+// before reading anything.
+template <typename... Args>
+cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, const DecodeParams &p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {const_cast<DecodeParams *>(&p)};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kern), args);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 int sm_count() {
     static int count[64] = {0};
     int dev = 0;
@@ -665,8 +691,7 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     } else {
         grid = dim3(MODE == kSplitDirect ? p.max_parts : 1, p.num_kv_heads, p.num_seqs);
     }
-    kern<<<grid, C::NT, C::SMEM, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(kern, grid, dim3(C::NT), C::SMEM, stream, p);
 }
 
 template <int HD, int G>
@@ -704,12 +729,11 @@ cudaError_t launch_merge(const DecodeParams &p, int head_dim, cudaStream_t strea
     if (p.num_seqs == 0) return cudaSuccess;
     const dim3 grid(p.num_q_heads, p.num_seqs);
     switch (head_dim) {
-        case 64: merge_kernel<64><<<grid, 256, 0, stream>>>(p); break;
-        case 128: merge_kernel<128><<<grid, 256, 0, stream>>>(p); break;
-        case 256: merge_kernel<256><<<grid, 256, 0, stream>>>(p); break;
+        case 64: return launch_dependent(merge_kernel<64>, grid, dim3(256), 0, stream, p);
+        case 128: return launch_dependent(merge_kernel<128>, grid, dim3(256), 0, stream, p);
+        case 256: return launch_dependent(merge_kernel<256>, grid, dim3(256), 0, stream, p);
         default: return cudaErrorNotSupported;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace pa

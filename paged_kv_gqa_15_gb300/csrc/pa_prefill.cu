@@ -193,6 +193,8 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(
     __shared__ int hist[kSchedBuckets];
     __shared__ int total_sh;
     const int tid = threadIdx.x;
+    // the prefill kernel may launch now (it sets up, then waits for this grid)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) *item_counter = 0;  // the prefill kernel claims items from here
     for (int i = tid; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
     if (tid == 0) total_sh = 0;
@@ -359,6 +361,11 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             prefetch_tensormap(&p.tm_k);
             prefetch_tensormap(&p.tm_v);
         }
+        // This grid is launched as a programmatic dependent of the schedule kernel:
+        // the set-up above overlaps it, and the work list and item counter it writes
+        // are read only after it has completed.  The other warps see items only
+        // through this warp.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         uint32_t kv_it = 0;
         int stop = 0;
         // Claims the k-th item of this CTA, decodes it and publishes it to the MMA
@@ -805,8 +812,17 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
     long long ctas = static_cast<long long>(sms) * per_sm;
     if (items < ctas) ctas = items;
     void *args[] = {&p};
-    e = cudaLaunchKernel(kern, dim3(static_cast<unsigned>(ctas)), dim3(threads), args, smem,
-                         stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, kern, args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

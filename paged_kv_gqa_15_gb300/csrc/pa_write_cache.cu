@@ -15,6 +15,9 @@ namespace pa {
 namespace {
 
 __global__ void __launch_bounds__(256) write_cache_kernel(const __grid_constant__ WriteCacheParams p) {
+    // a decode launched next in the stream may start up now; it waits for this grid
+    // to complete before reading the cache
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int cpr = p.head_dim / 8;                  // 16-byte chunks per row
     const int64_t per_tok = static_cast<int64_t>(p.num_kv_heads) * cpr;
     const int64_t total = p.num_tokens * per_tok;
