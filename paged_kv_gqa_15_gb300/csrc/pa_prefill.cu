@@ -487,7 +487,16 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, HD, false, true);
-            const uint32_t q_base = smem_addr(smem + C::OFF_Q);
+            // Operand descriptors are built once: within a 128-byte-swizzled operand a
+            // byte offset moves only the start-address field (address / 16, 14 bits,
+            // never carried out of for shared-memory addresses), so each MMA adds a
+            // constant to a base descriptor instead of rebuilding it -- the single
+            // issuing thread otherwise spends more time on descriptor arithmetic than
+            // the tensor core spends on a 128 x 64 x 16 MMA.
+            const uint64_t q_desc = smem_desc_sw128(smem_addr(smem + C::OFF_Q), 16, 1024);
+            const uint64_t k_desc = smem_desc_sw128(smem_addr(smem + C::OFF_K), 16, 1024);
+            const uint64_t v_desc =
+                smem_desc_sw128(smem_addr(smem + C::OFF_V), C::KV_CHUNK, 1024);
             uint32_t kv_it = 0, q_it = 0, o_items = 0;
             bool ok = true;
             // O += P_g V_g for global key tile g (tile jj of an item with kv_len keys)
@@ -517,14 +526,11 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                         fence_proxy_async_smem();
                     }
                 }
-                const uint32_t v_base = smem_addr(smem + C::OFF_V + s * C::KV_BYTES);
+                const uint64_t vd = v_desc + ((s * C::KV_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bdesc =
-                        smem_desc_sw128(v_base + kk * 16 * 128, C::KV_CHUNK, 1024);
-                    mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + b * BN + kk * 8, bdesc, idesc_o,
-                                (jj > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + b * BN + kk * 8,
+                                vd + ((kk * 16 * 128) >> 4), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(&v_empty[s]);
             };
             for (uint32_t k = 0; ok; ++k) {
@@ -546,16 +552,12 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                     ok = mbar_wait(&k_full[s], (g / C::KS) & 1, p.status, abort_flag);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    const uint32_t k_base = smem_addr(smem + C::OFF_K + s * C::KV_BYTES);
+                    const uint64_t kd = k_desc + ((s * C::KV_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
                         const uint32_t c = kk / 4, inner = (kk % 4) * 32;
-                        const uint64_t adesc =
-                            smem_desc_sw128(q_base + c * kBM * 128 + inner, 16, 1024);
-                        const uint64_t bdesc =
-                            smem_desc_sw128(k_base + c * C::KV_CHUNK + inner, 16, 1024);
-                        mma_bf16_ss(tmem + C::TM_S + b * BN, adesc, bdesc, idesc_s,
-                                    kk > 0 ? 1u : 0u);
+                        mma_bf16_ss(tmem + C::TM_S + b * BN, q_desc + ((c * kBM * 128 + inner) >> 4),
+                                    kd + ((c * C::KV_CHUNK + inner) >> 4), idesc_s, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(&s_full[b]);
                     if (j >= 1) issue_pv(g - 1, j - 1, w.kv_len);
