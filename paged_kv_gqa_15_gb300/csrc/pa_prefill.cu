@@ -413,13 +413,13 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                     stop = 1;
                 } else {
                     mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-                    for (int c = 0; c < C::QCH; ++c)
-                        tma_load_3d(smem + C::OFF_Q + c * kBM * 128, &p.tm_q, c * 64, w.h,
-                                    w.qo_start + w.q0, q_full);
                 }
             }
             stop = __shfl_sync(kFullMask, stop, 0);
             if (stop) break;
+            if (lane < C::QCH)   // one 64-column chunk of Q per lane
+                tma_load_3d(smem + C::OFF_Q + lane * kBM * 128, &p.tm_q, lane * 64, w.h,
+                            w.qo_start + w.q0, q_full);
             const int pages_seq = (w.kv_len + kBlockSize - 1) / kBlockSize;
             // Loads key tile j (kv = 0) or value tile j (kv = 1) of this item into its
             // ring stage; g is the tile's index over all items of this CTA.
@@ -432,29 +432,26 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 const CUtensorMap *tm = kv ? &p.tm_v : &p.tm_k;
                 uint8_t *dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::KV_BYTES;
                 if (lane == 0) {
-                    if (!mbar_wait(empty, ph, p.status, abort_flag)) {
+                    if (!mbar_wait(empty, ph, p.status, abort_flag))
                         stop = 1;
-                    } else {
-                        mbar_arrive_expect_tx(full, C::KV_BYTES);
-                        if constexpr (!PAGED) {
-                            for (int c = 0; c < C::QCH; ++c)
-                                tma_load_3d(dst + c * C::KV_CHUNK, tm, c * 64, kh,
-                                            w.kv_start + j * BN, full);
-                        }
-                    }
+                    else
+                        mbar_arrive_expect_tx(full, C::KV_BYTES);   // before any copy lands
                 }
-                stop = __shfl_sync(kFullMask, stop, 0);
+                stop = __shfl_sync(kFullMask, stop, 0);   // also orders lane 0 before the copies
                 if (stop) return;
+                // One box per lane, so a tile's boxes leave in one warp instruction: lane
+                // l copies 64-column chunk l % QCH of page l / QCH (paged) or chunk l.
                 if constexpr (PAGED) {
-#pragma unroll
-                    for (int e = 0; e < BN / kBlockSize; ++e) {
-                        const int pg = __shfl_sync(kFullMask, page, e);
-                        if (lane == 0) {
-                            for (int c = 0; c < C::QCH; ++c)
-                                tma_load_4d(dst + c * C::KV_CHUNK + e * kBlockSize * 128, tm,
-                                            c * 64, 0, kh, pg, full);
-                        }
+                    const int pg = __shfl_sync(kFullMask, page, (lane / C::QCH) & 31);
+                    if (lane < (BN / kBlockSize) * C::QCH) {
+                        const int e = lane / C::QCH, c = lane % C::QCH;
+                        tma_load_4d(dst + c * C::KV_CHUNK + e * kBlockSize * 128, tm, c * 64, 0, kh,
+                                    pg, full);
                     }
+                } else {
+                    if (lane < C::QCH)
+                        tma_load_3d(dst + lane * C::KV_CHUNK, tm, lane * 64, kh,
+                                    w.kv_start + j * BN, full);
                 }
             };
             // The MMA warp consumes K_{j+1} (for S_{j+1}) before V_j (for P_j V_j), so K
