@@ -717,6 +717,7 @@ cudaError_t dispatch_group(const DecodeParams &p, bool split, cudaStream_t strea
 
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
+    if (split && decode_tc_supported(p, head_dim)) return launch_decode_tc(p, stream);
     switch (head_dim) {
         case 64: return dispatch_group<64>(p, split, stream);
         case 128: return dispatch_group<128>(p, split, stream);

@@ -58,7 +58,15 @@ struct PrefillLaunch {
     int head_dim;
 };
 
+// Tiled tensor map of a bf16 tensor with 128-byte swizzle, out-of-range reads as
+// zeros; false when the driver entry point or the encoding fails.
+bool encode_tensor_map_bf16(CUtensorMap *tm, const void *base, int rank, const cuuint64_t *dims,
+                            const cuuint64_t *strides_bytes, const cuuint32_t *box);
+
 cudaError_t launch_write_cache(const WriteCacheParams &p, cudaStream_t stream);
+// Tensor-core partition pass of the split decode (head_dim 128, GQA group 4 or 8).
+bool decode_tc_supported(const DecodeParams &p, int head_dim);
+cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
 // Returns cudaErrorNotSupported for an unsupported (head_dim, group) pair.
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams &p, int head_dim, cudaStream_t stream);

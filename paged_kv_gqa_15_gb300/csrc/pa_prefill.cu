@@ -726,35 +726,6 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
 
 // ---- host side ----------------------------------------------------------------------
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-bool encode(CUtensorMap *tm, const void *base, int rank, const cuuint64_t *dims,
-            const cuuint64_t *strides_bytes, const cuuint32_t *box) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
-              strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int HD, int BN, bool PAGED>
 cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream) {
     using C = PrefillCfg<HD, BN>;
@@ -764,7 +735,7 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
         const cuuint64_t str[2] = {static_cast<cuuint64_t>(HD) * 2,
                                    static_cast<cuuint64_t>(p.nq) * HD * 2};
         const cuuint32_t box[3] = {64, 1, kBM};
-        if (!encode(&p.tm_q, L.q, 3, dims, str, box)) return cudaErrorInvalidValue;
+        if (!encode_tensor_map_bf16(&p.tm_q, L.q, 3, dims, str, box)) return cudaErrorInvalidValue;
     }
     if constexpr (!PAGED) {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(p.nkv),
@@ -772,8 +743,8 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
         const cuuint64_t str[2] = {static_cast<cuuint64_t>(HD) * 2,
                                    static_cast<cuuint64_t>(p.nkv) * HD * 2};
         const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(BN)};
-        if (!encode(&p.tm_k, L.k, 3, dims, str, box)) return cudaErrorInvalidValue;
-        if (!encode(&p.tm_v, L.v, 3, dims, str, box)) return cudaErrorInvalidValue;
+        if (!encode_tensor_map_bf16(&p.tm_k, L.k, 3, dims, str, box)) return cudaErrorInvalidValue;
+        if (!encode_tensor_map_bf16(&p.tm_v, L.v, 3, dims, str, box)) return cudaErrorInvalidValue;
     } else {
         const cuuint64_t dims[4] = {static_cast<cuuint64_t>(HD), 16,
                                     static_cast<cuuint64_t>(p.nkv),
@@ -782,8 +753,8 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
                                    static_cast<cuuint64_t>(L.s_head) * 2,
                                    static_cast<cuuint64_t>(L.s_block) * 2};
         const cuuint32_t box[4] = {64, 16, 1, 1};
-        if (!encode(&p.tm_k, L.k, 4, dims, str, box)) return cudaErrorInvalidValue;
-        if (!encode(&p.tm_v, L.v, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!encode_tensor_map_bf16(&p.tm_k, L.k, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!encode_tensor_map_bf16(&p.tm_v, L.v, 4, dims, str, box)) return cudaErrorInvalidValue;
     }
     prefill_schedule_kernel<<<1, 1024, 0, stream>>>(p.qo_indptr, p.kv_indptr, p.batch, p.causal,
                                                     BN, p.n_tiles, const_cast<int2 *>(p.tiles),
@@ -827,6 +798,36 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
 }
 
 }  // namespace
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+bool encode_tensor_map_bf16(CUtensorMap *tm, const void *base, int rank,
+                            const cuuint64_t *dims, const cuuint64_t *strides_bytes,
+                            const cuuint32_t *box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
+              strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_prefill(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream) {
     if (p.n_tiles == 0) return cudaSuccess;

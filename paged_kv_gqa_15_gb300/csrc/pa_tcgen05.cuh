@@ -121,6 +121,18 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
 }
 
+// tcgen05.ld of 8 consecutive 32-bit columns for this warp's 32 lanes, then
+// wait::ld in the same asm block so the outputs are ready when it returns.
+__device__ __forceinline__ void tmem_load_8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
+
 // tcgen05.ld of 64 consecutive 32-bit columns for this warp's 32 lanes, then
 // wait::ld in the same asm block so the outputs are ready when it returns.
 __device__ __forceinline__ void tmem_load_64(uint32_t taddr, uint32_t (&r)[64]) {

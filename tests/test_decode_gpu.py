@@ -154,12 +154,16 @@ def test_split_partials_match_oracle_partitions():
     P = (L + 511) // 512
     po, pm, pl = pa.decode_split_workspace_views(ws, w.batch, w.num_q_heads, w.head_dim, L)
     m, l, o = oracle.decode_partitions(q, kc, vc, w.block_tables, w.seq_lens, 2, 16, w.scale, P)
+    vmax = float(np.abs(W.bits_to_float(vc)).max())
     for b, Lb in enumerate(w.seq_lens):
         np_ = (int(Lb) + 511) // 512
         gm, gl, go = (x[b, :, :np_].cpu().numpy().astype(np.float64) for x in (pm, pl, po))
         np.testing.assert_allclose(gm, m[b, :, :np_], atol=1e-4, rtol=0)
         np.testing.assert_allclose(gl, l[b, :, :np_], rtol=1e-4, atol=0)
-        np.testing.assert_allclose(go, o[b, :, :np_], atol=1e-4, rtol=0)
+        # The partial output is a p-weighted mean of V rows; the tensor-core P.V takes
+        # P rounded to bf16 (relative error <= 2^-9 per weight), which can move it by up
+        # to 2^-9 * max|V| (fp32 P on the CUDA-core path stays far inside this bound).
+        np.testing.assert_allclose(go, o[b, :, :np_], atol=2.0 ** -9 * vmax + 1e-5, rtol=0)
     assert_close_bf16(out, ref, what="split")
 
 
