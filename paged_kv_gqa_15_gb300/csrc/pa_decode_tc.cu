@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             prefetch_tensormap(tm);
             if (!is_v) prefetch_tensormap(&prm.tm_q);
         }
+        const uint64_t policy = l2_policy_evict_first();
         uint32_t it = 0;   // ring uses
         int stop = 0;
         int b, kh, part;
@@ -249,10 +250,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 if (stop) break;
                 // lane l: page l / 2 of the tile, 64-column chunk l % 2
                 const int pg = __shfl_sync(kFullMaskTc, page, (i * kPagesPerTile + lane / 2) & 31);
-                if (lane < 2 * kPagesPerTile)
-                    tma_load_4d(ring + s * kTileBytes + (lane & 1) * kTileChunk +
-                                    (lane >> 1) * kBlockSize * 128,
-                                tm, (lane & 1) * 64, 0, kh, pg, &full[s]);
+                if (lane < 2 * kPagesPerTile)   // K / V are read once: evict them first
+                    tma_load_4d_hint(ring + s * kTileBytes + (lane & 1) * kTileChunk +
+                                         (lane >> 1) * kBlockSize * 128,
+                                     tm, (lane & 1) * 64, 0, kh, pg, &full[s], policy);
             }
         }
         // never leave the CTA with copies still landing in its shared memory

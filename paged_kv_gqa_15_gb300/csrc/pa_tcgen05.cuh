@@ -111,6 +111,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, in
         : "memory");
 }
 
+// tma_load_4d with an L2 cache-policy hint (e.g. evict-first for data read once).
+__device__ __forceinline__ void tma_load_4d_hint(void *dst, const CUtensorMap *tm, int c0, int c1,
+                                                 int c2, int c3, uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+        "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy
 // reads (tensor-core operand fetches) of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
