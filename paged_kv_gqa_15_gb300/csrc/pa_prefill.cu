@@ -153,7 +153,10 @@ struct PrefillCfg {
     static constexpr uint32_t Q_BYTES = QCH * kBM * 128;
     static constexpr uint32_t KV_CHUNK = BN * 128;            // one chunk of a K / V tile
     static constexpr uint32_t KV_BYTES = QCH * KV_CHUNK;
-    static constexpr int KS = 2;   // K ring stages: one per S buffer (K_j is free once S_j is)
+    // K ring stages.  With two, stage j % 2 is S buffer j % 2 and K_j is free once S_j
+    // is done (s_full); head_dim 256 runs one CTA per SM, where a third stage (freed
+    // by a softmax-side arrival on k_empty) hides more of the TMA latency.
+    static constexpr int KS = HD == 256 ? 3 : 2;
     static constexpr int VS = 2;                              // V ring stages
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
@@ -172,7 +175,7 @@ struct PrefillCfg {
     static constexpr uint32_t SMEM_MIN = CTAS_PER_SM == 2 ? 0 : 118 * 1024;
     static constexpr uint32_t SMEM = (SMEM_USED + 1024 > SMEM_MIN) ? SMEM_USED + 1024 : SMEM_MIN;
     static_assert(HD % 64 == 0 && BN % 16 == 0 && BN <= 128, "tile shape");
-    static_assert(KS == 2 && VS >= 2 && VS <= 4, "ring stages");
+    static_assert(KS >= 2 && KS <= 4 && VS >= 2 && VS <= 4, "ring stages");
     static_assert(TMEM_COLS <= 512, "TMEM budget");
     // two CTAs, each with the 1 KB the runtime reserves per CTA, in the SM's 228 KB
     static_assert(CTAS_PER_SM == 1 || 2 * (SMEM + 1024) <= 228 * 1024, "two CTAs per SM");
@@ -299,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
     // before) nor one ahead (the next phase needs work the waiter has not released).
     uint64_t *q_full = bars + 0;
     uint64_t *k_full = bars + 2;    // [KS]
+    uint64_t *k_empty = bars + 6;   // [KS] (KS != 2): one softmax thread arrives once S_g is done
     uint64_t *v_full = bars + 10;   // [VS]
     uint64_t *v_empty = bars + 14;  // [VS]
     uint64_t *s_full = bars + 18;   // [2]
@@ -327,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
         mbar_init(q_full, 1);
         for (int s = 0; s < C::KS; ++s) {
             mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
         }
         for (int s = 0; s < C::VS; ++s) {
             mbar_init(&v_full[s], 1);
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 const int s = g % ns;
                 const uint32_t ph = ((g / ns) & 1) ^ 1u;
                 uint64_t *full = kv ? &v_full[s] : &k_full[s];
-                uint64_t *empty = kv ? &v_empty[s] : &s_full[s];   // K stage s == S buffer s
+                uint64_t *empty = kv ? &v_empty[s] : (C::KS == 2 ? &s_full[s] : &k_empty[s]);
                 const CUtensorMap *tm = kv ? &p.tm_v : &p.tm_k;
                 uint8_t *dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::KV_BYTES;
                 if (lane == 0) {
@@ -603,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                     ok = false;
                     break;
                 }
+                if (C::KS != 2 && warp == 2 && lane == 0) mbar_arrive(&k_empty[g % C::KS]);   // K_g read
                 tc_fence_after_sync();
                 uint32_t sr[BN];
                 if constexpr (BN == 64) {
