@@ -42,15 +42,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch from ncu captures, keyed by kernel, valid only
 # for the source file hash they were measured on (otherwise reported as null).
 TRAFFIC = {
-    # ncu capture of one decode_kernel<128,4,persistent> launch on the Llama-8B decode
-    # workload: dram__bytes_read.sum 568.38 MB + dram__bytes_write.sum 5.44 MB
+    # ncu capture of one decode_tc_kernel<4> launch on the Llama-8B decode workload:
+    # dram__bytes_read.sum 568.32 MB + dram__bytes_write.sum 5.33 MB
     "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
-        "src": "2f606a466f1fd67e", "bytes_per_launch": 573826560},
+        "src": "a4b0745b68763b53", "bytes_per_launch": 573654784},
     # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
-    # causal prefill: dram__bytes_read.sum 298.72 MB + dram__bytes_write.sum 109.05 MB
+    # causal prefill: dram__bytes_read.sum 297.11 MB + dram__bytes_write.sum 109.05 MB
     "ragged_prefill:ragged_prefill_r16_h32kv8_d128": {
-        "src": "924f90cd0af3f0e0", "bytes_per_launch": 407768320},
+        "src": "0b6e207836ee269d", "bytes_per_launch": 406167040},
 }
+
 
 # ---------------------------------------------------------------------------------------
 # host-side helpers (also exercised by the CPU tests)
@@ -311,7 +312,7 @@ def bench_decode(w, steps, warmup, dev, stream, peaks, peak_kind):
     kv = w.kv_bytes()
     value, ms_max = aggregate_throughput(kv, ms, dev)
     kern_ms = per["decode_partitions"]
-    src = ("pa_decode.cu", "pa_device.cuh")
+    src = ("pa_decode_tc.cu", "pa_tcgen05.cuh", "pa_device.cuh")
     res = {
         "value": value / 1e9, "unit": "GB/s", "ms_per_step": ms_max,
         "kv_bytes_per_step": kv, "launches": launches,
