@@ -212,6 +212,12 @@ def decode_step(w, s, stream, evs=None):
         n += 1
         if evs is not None:
             evs.append(_ev(stream))
+    if not w.split:   # the workload's decode is one pass over each sequence
+        pa.pa_decode(s["out"], t["q"], t["k_cache"], t["v_cache"], s["bt"], s["sl"], w.scale,
+                     stream=stream)
+        if evs is not None:
+            evs.append(_ev(stream))
+        return n + 1
     L = max(w.max_seq_len, 1)
     pa.pa_decode_partitions(t["q"], t["k_cache"], t["v_cache"], s["bt"], s["sl"], w.scale, L,
                             s["ws"], stream=stream)
@@ -302,8 +308,8 @@ def prefill_footprint(w):
 def bench_decode(w, steps, warmup, dev, stream, peaks, peak_kind):
     s = decode_setup(w, dev)
     flush = decode_footprint(w) < L2_FLUSH_BYTES
-    labels = (["write_cache"] if w.new_token_write else []) + ["decode_partitions",
-                                                               "decode_merge"]
+    labels = (["write_cache"] if w.new_token_write else []) + (
+        ["decode_partitions", "decode_merge"] if w.split else ["decode"])
 
     def step(evs):
         return decode_step(w, s, stream, evs)
@@ -311,8 +317,9 @@ def bench_decode(w, steps, warmup, dev, stream, peaks, peak_kind):
     ms, per, launches = time_steps(step, steps, warmup, stream, dev, labels, flush)
     kv = w.kv_bytes()
     value, ms_max = aggregate_throughput(kv, ms, dev)
-    kern_ms = per["decode_partitions"]
-    src = ("pa_decode_tc.cu", "pa_tcgen05.cuh", "pa_device.cuh")
+    kern_ms = per["decode_partitions" if w.split else "decode"]
+    src = ("pa_decode_tc.cu", "pa_tcgen05.cuh", "pa_device.cuh") if w.split else \
+        ("pa_decode.cu", "pa_device.cuh")
     res = {
         "value": value / 1e9, "unit": "GB/s", "ms_per_step": ms_max,
         "kv_bytes_per_step": kv, "launches": launches,

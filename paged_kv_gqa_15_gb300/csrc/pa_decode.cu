@@ -629,6 +629,56 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Deco
     }
 }
 
+// The same merge with one warp per (sequence, query head), for calls whose sequences
+// have at most 32 partitions: lane i holds partition i's (m, l), the max and the
+// weight sum are warp reductions, and each lane accumulates HD / 32 output dims over
+// the partitions -- no block-wide syncs, so short-sequence batches are not bound by
+// the latency of a 256-thread reduction per (sequence, head).
+template <int HD>
+__global__ void __launch_bounds__(256) merge_warp_kernel(const __grid_constant__ DecodeParams p) {
+    constexpr int DPL = HD / 32;   // output dims per lane
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the partials are complete
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int nq = p.num_q_heads;
+    if (gw >= static_cast<int64_t>(p.num_seqs) * nq) return;
+    const int b = static_cast<int>(gw / nq), h = static_cast<int>(gw % nq);
+    int L = p.seq_lens[b];
+    if (L < 0) L = 0;
+    if (L > p.max_seq_len) L = p.max_seq_len;
+    const int np = (L + kPartition - 1) / kPartition;   // <= 32 for this kernel
+    const int64_t row0 = (static_cast<int64_t>(b) * nq + h) * p.max_parts;
+    const float mi = lane < np ? p.part_m[row0 + lane] : -INFINITY;
+    float M = mi;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    const float wi = (lane < np && mi != -INFINITY) ? p.part_l[row0 + lane] * exp2f((mi - M) * kLog2e)
+                                                     : 0.f;
+    float W = wi;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) W += __shfl_xor_sync(kFull, W, off);
+    float acc[DPL];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < np; ++i) {
+        const float w = __shfl_sync(kFull, wi, i);
+        const float *o = p.part_o + (row0 + i) * HD + lane * DPL;
+#pragma unroll
+        for (int d = 0; d < DPL; d += 2) {
+            const float2 v = *reinterpret_cast<const float2 *>(o + d);
+            acc[d] = fmaf(w, v.x, acc[d]);
+            acc[d + 1] = fmaf(w, v.y, acc[d + 1]);
+        }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + (static_cast<int64_t>(b) * nq + h) * HD +
+                         lane * DPL;
+#pragma unroll
+    for (int d = 0; d < DPL; d += 2)
+        *reinterpret_cast<__nv_bfloat162 *>(out + d) = __floats2bfloat162_rn(acc[d] * inv, acc[d + 1] * inv);
+}
+
 // Launches a kernel as a programmatic dependent of the previous work in the stream:
 // its CTAs may start while that work finishes, and wait for it (griddepcontrol.wait)
 // before reading anything.
@@ -728,6 +778,16 @@ cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaS
 
 cudaError_t launch_merge(const DecodeParams &p, int head_dim, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
+    if (p.max_parts <= 32) {   // one warp per (sequence, head)
+        const int64_t warps = static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
+        const dim3 wgrid(static_cast<unsigned>((warps + 7) / 8));
+        switch (head_dim) {
+            case 64: return launch_dependent(merge_warp_kernel<64>, wgrid, dim3(256), 0, stream, p);
+            case 128: return launch_dependent(merge_warp_kernel<128>, wgrid, dim3(256), 0, stream, p);
+            case 256: return launch_dependent(merge_warp_kernel<256>, wgrid, dim3(256), 0, stream, p);
+            default: return cudaErrorNotSupported;
+        }
+    }
     const dim3 grid(p.num_q_heads, p.num_seqs);
     switch (head_dim) {
         case 64: return launch_dependent(merge_kernel<64>, grid, dim3(256), 0, stream, p);
