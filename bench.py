@@ -328,7 +328,35 @@ def bench_decode(w, steps, warmup, dev, stream, peaks, peak_kind):
                              traffic_for("decode_partitions:" + w.name, src), peak_kind),
         "roofline_nominal_frac": round(kv / (kern_ms / 1e3) / 1e9 / 8000.0, 4),
     }
+    res["graph"] = bench_decode_graph(w, s, steps, warmup, dev, stream, flush)
     return res, s
+
+
+def bench_decode_graph(w, s, steps, warmup, dev, stream, flush):
+    """The same step captured once in a CUDA graph and replayed (serving replays a
+    captured decode); one graph launch replaces the step's kernel launches."""
+    with torch.cuda.stream(stream):
+        decode_step(w, s, stream, None)   # one-time set-up happens outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        n = decode_step(w, s, stream, None)
+    torch.cuda.synchronize()
+
+    def replay(evs):
+        if evs is not None:
+            evs.append(_ev(stream))
+        with torch.cuda.stream(stream):
+            graph.replay()
+        if evs is not None:
+            evs.append(_ev(stream))
+        return n
+
+    ms, _, _ = time_steps(replay, steps, warmup, stream, dev, ["step"], flush)
+    value, ms_max = aggregate_throughput(w.kv_bytes(), ms, dev)
+    del graph
+    return {"value": round(value / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms_max, 5),
+            "kernels_per_replay": n}
 
 
 def bench_decode_e2e(w, s, steps, warmup, dev, stream):
@@ -618,6 +646,7 @@ def main(argv=None):
             "roofline": res["roofline"], "roofline_nominal_frac": res["roofline_nominal_frac"],
             "kernels_ms": res["kernels_ms"], "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": res["launches"], "clocks": clk, "device_status": status,
+            "graph": res.get("graph"),
             "workloads": extra,
         }
         print(json.dumps(line), flush=True)

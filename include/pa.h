@@ -17,6 +17,9 @@
  *                       or paged K/V ("spark_runtime/flashinfer.rs",
  *                       ragged_prefill_bf16_hd256; "paged_attn.py",
  *                       _forward_prefix_pytorch)
+ *   pa_block_table_sync upload of the changed rows of a block table, for
+ *                       CUDA-graph replays of the decode ("libmir-cuda
+ *                       attention/mod.rs", captured decode nodes)
  *
  * Conventions shared by every entry point:
  *  - All data pointers are DEVICE pointers of the current CUDA device unless
@@ -218,6 +221,29 @@ int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
                       int total_kv_rows, int num_q_heads, int num_kv_heads, int head_dim,
                       float sm_scale, int causal, void *workspace, size_t workspace_bytes,
                       void *stream);
+
+/*
+ * Block-table upload for CUDA-graph replays ("libmir-cuda attention/mod.rs",
+ * the captured decode nodes and their block-table snapshot; "paged_attn.py",
+ * block tables padded for graph capture): a captured decode reads a fixed
+ * device table, so between replays only the rows that changed need copying.
+ *   host_table   [num_rows][row_len] int32, the table the caller wants on the
+ *                device (any host memory);
+ *   snapshot     [num_rows][row_len] int32 PINNED host memory owned by the
+ *                caller, holding what was last uploaded (fill it with a value
+ *                no row has, e.g. -1, or call once with rows_uploaded == NULL
+ *                semantics in mind, before the first sync);
+ *   device_table [num_rows][row_len] int32 device memory.
+ * Rows of host_table that differ from the snapshot are copied into it, and
+ * each run of consecutive changed rows is enqueued on `stream` as one async
+ * copy from the snapshot to device_table.  *rows_uploaded (if not NULL)
+ * receives the number of rows copied.  The snapshot's rows must not change
+ * again until the stream has executed those copies (for instance, sync once
+ * per step, after the previous step's work on the stream is done).
+ * Returns PA_OK, PA_ERR_INVALID or PA_ERR_CUDA.
+ */
+int pa_block_table_sync(const int32_t *host_table, int32_t *snapshot, int32_t *device_table,
+                        int num_rows, int row_len, int *rows_uploaded, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

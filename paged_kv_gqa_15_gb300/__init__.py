@@ -58,6 +58,8 @@ def load():
     lib.pa_ragged_prefill.argtypes = [P, P, P, P, P, P, P, P, P, I, I, L, L, L, L, I, I, I, I, I,
                                       I, F, I, P, Z, P]
     lib.pa_get_device_status.argtypes = [P, P]
+    lib.pa_block_table_sync.argtypes = [P, P, P, I, I, P, P]
+    lib.pa_block_table_sync.restype = I
     lib.pa_last_error.restype = ctypes.c_char_p
     for name in ("pa_write_cache", "pa_decode", "pa_decode_split", "pa_decode_partitions",
                  "pa_decode_merge", "pa_ragged_prefill",
@@ -99,6 +101,28 @@ def _pool_geometry(cache, layout):
     else:
         bs, nkv, hd = cache.shape[1], cache.shape[2], cache.shape[3]
     return nb, nkv, bs, hd
+
+
+def _host_ptr(a):
+    """Address of a C-contiguous host array (numpy or CPU torch tensor)."""
+    if isinstance(a, torch.Tensor):
+        assert a.device.type == "cpu" and a.is_contiguous()
+        return ctypes.c_void_p(a.data_ptr())
+    assert a.flags["C_CONTIGUOUS"]
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def pa_block_table_sync(host_table, snapshot, device_table, stream=None) -> int:
+    """Uploads the rows of host_table (int32 [rows, cols], host) that differ from
+    snapshot (a pinned int32 host tensor holding what was last uploaded) into
+    device_table, refreshing the snapshot; returns the number of rows copied."""
+    rows, cols = host_table.shape
+    assert tuple(snapshot.shape) == (rows, cols) and tuple(device_table.shape) == (rows, cols)
+    n = ctypes.c_int(0)
+    _check(load().pa_block_table_sync(_host_ptr(host_table), _host_ptr(snapshot),
+                                      _ptr(device_table), rows, cols, ctypes.byref(n),
+                                      _stream(stream) if torch.cuda.is_available() else None))
+    return n.value
 
 
 def pa_write_cache(k, v, k_cache, v_cache, slot_mapping, layout="HND", stream=None):

@@ -24,6 +24,21 @@ int cuda_fail(cudaError_t e, const char *what) {
     return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+}  // namespace
+
+// Error reporting for entry points defined in other translation units.
+int pa::api_fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int pa::api_cuda_fail(cudaError_t e, const char *what) { return cuda_fail(e, what); }
+
+namespace {
+
 // Device status word (OR of 1 << PA_ERR_* bits), one per device.
 __device__ int g_status_word;
 

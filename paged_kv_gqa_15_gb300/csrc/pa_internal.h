@@ -58,6 +58,10 @@ struct PrefillLaunch {
     int head_dim;
 };
 
+// Set the thread's last-error message and return `code` (or PA_ERR_CUDA).
+int api_fail(int code, const char *fmt, ...);
+int api_cuda_fail(cudaError_t e, const char *what);
+
 // Tiled tensor map of a bf16 tensor with 128-byte swizzle, out-of-range reads as
 // zeros; false when the driver entry point or the encoding fails.
 bool encode_tensor_map_bf16(CUtensorMap *tm, const void *base, int rank, const cuuint64_t *dims,

@@ -114,3 +114,21 @@ def test_error_raises_with_message(lib):
     with pytest.raises(pa.PaError) as ei:
         pa._check(_decode(lib, hd=96))
     assert "head_dim" in str(ei.value)
+
+
+def test_block_table_sync_uploads_nothing_when_unchanged():
+    # host logic only: an unchanged table makes no CUDA call, so this runs without a GPU
+    import ctypes
+    import numpy as np
+    import paged_kv_gqa_15_gb300 as pa
+    lib = pa.load()
+    host = np.arange(12, dtype=np.int32).reshape(3, 4)
+    snap = host.copy()
+    n = ctypes.c_int(-1)
+    rc = lib.pa_block_table_sync(host.ctypes.data, snap.ctypes.data, ctypes.c_void_p(8),
+                                 3, 4, ctypes.byref(n), None)
+    assert rc == pa.PA_OK and n.value == 0
+    assert lib.pa_block_table_sync(None, snap.ctypes.data, ctypes.c_void_p(8), 3, 4, None,
+                                   None) == pa.PA_ERR_INVALID
+    assert lib.pa_block_table_sync(host.ctypes.data, snap.ctypes.data, ctypes.c_void_p(8),
+                                   -1, 4, None, None) == pa.PA_ERR_INVALID
