@@ -440,6 +440,93 @@ def bench_prefill(w, steps, warmup, dev, stream, peaks, peak_kind):
             "roofline_nominal_frac": round(achieved / 2250.0, 4)}
 
 
+# Page-copy legs: a Llama-3-8B-shaped cache (32 layers x K and V pools of 1024
+# 16-token pages, 8 kv heads x head_dim 128 bf16 = 32 KB per page, 2 GiB in all) and
+# 256 pages per pool per call (a 4096-token context): 512 MiB of pages per call.
+BLOCK_LEGS = ("copy_blocks_fork", "swap_blocks")
+BLOCK_LAYERS, BLOCK_POOL_PAGES, BLOCK_PAIRS, BLOCK_PAGE = 32, 1024, 256, (8, 16, 128)
+
+
+def blocks_config(name):
+    cfg = {"workload": name, "layers": BLOCK_LAYERS, "pools": 2 * BLOCK_LAYERS,
+           "pages_per_pool": BLOCK_POOL_PAGES, "pairs_per_call": BLOCK_PAIRS,
+           "page_bytes": int(np.prod(BLOCK_PAGE)) * 2,
+           "page": "8 kv heads x 16 tokens x head_dim 128 bf16", "l2": "inputs > L2 (no flush)"}
+    if name == "swap_blocks":
+        cfg["host_pool_pages"] = BLOCK_PAIRS
+    return cfg
+
+
+def bench_blocks(name, steps, warmup, dev, stream, peaks, peak_kind):
+    """copy_blocks_fork: one pa_copy_blocks call duplicates 256 pages in all 64 pools
+    (read + write 1 GiB of HBM).  swap_blocks: the same pages go out to pinned host pools
+    and come back to other device pages, one pa_swap_blocks call per direction; the link
+    is judged against a contiguous copy-engine copy of the same bytes timed here."""
+    import paged_kv_gqa_15_gb300 as pa
+    rng = np.random.default_rng(2024)
+    perm = rng.permutation(BLOCK_POOL_PAGES)
+    pools = [torch.empty((BLOCK_POOL_PAGES,) + BLOCK_PAGE, dtype=torch.bfloat16,
+                         device=dev).normal_() for _ in range(2 * BLOCK_LAYERS)]
+    page_bytes = int(np.prod(BLOCK_PAGE)) * 2
+    moved = BLOCK_PAIRS * len(pools) * page_bytes          # bytes of pages per call
+
+    def timed(call, label):
+        def step(evs):
+            if evs is not None:
+                evs.append(_ev(stream))
+            call()
+            if evs is not None:
+                evs.append(_ev(stream))
+            return 1
+        ms, _, n = time_steps(step, steps, warmup, stream, dev, [label])
+        return ms, n
+
+    if name == "copy_blocks_fork":
+        pairs = np.stack([perm[:BLOCK_PAIRS], perm[BLOCK_PAIRS:2 * BLOCK_PAIRS]], 1)
+        m = torch.from_numpy(pairs.astype(np.int64)).to(dev)
+        ms, n = timed(lambda: pa.pa_copy_blocks(pools[0::2], pools[1::2], m, stream=stream),
+                      "copy_blocks")
+        hbm = 2 * moved / (ms / 1e3) / 1e9                  # read + write
+        return {"value": round(hbm, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+                "bytes_per_step": 2 * moved, "launches": n,
+                "kernels_ms": {"copy_blocks": round(ms, 5)},
+                "roofline": roofline("hbm", hbm, peaks["hbm_gbs"], "GB/s", None, peak_kind),
+                "roofline_nominal_frac": round(hbm / 8000.0, 4),
+                "config": blocks_config(name)}
+
+    host = [torch.empty((BLOCK_PAIRS,) + BLOCK_PAGE, dtype=torch.bfloat16).pin_memory()
+            for _ in pools]
+    out_pairs = np.stack([perm[:BLOCK_PAIRS], np.arange(BLOCK_PAIRS)], 1).astype(np.int64)
+    in_pairs = np.stack([np.arange(BLOCK_PAIRS), perm[2 * BLOCK_PAIRS:3 * BLOCK_PAIRS]],
+                        1).astype(np.int64)
+    m_out = torch.from_numpy(out_pairs).to(dev)
+    m_in = torch.from_numpy(in_pairs).to(dev)
+    ms_out, n1 = timed(lambda: pa.pa_swap_blocks(pools, host, m_out, stream=stream), "swap_out")
+    ms_in, n2 = timed(lambda: pa.pa_swap_blocks(host, pools, m_in, stream=stream), "swap_in")
+    # the link's copy-engine rate for the same bytes, as one contiguous copy each way
+    dbuf = torch.empty(moved, dtype=torch.uint8, device=dev)
+    hbuf = torch.empty(moved, dtype=torch.uint8).pin_memory()
+
+    def ce(dst, src):
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)
+    ce_out, _ = timed(lambda: ce(hbuf, dbuf), "ce_out")
+    ce_in, _ = timed(lambda: ce(dbuf, hbuf), "ce_in")
+    del dbuf, hbuf, host
+    gbs = lambda ms: moved / (ms / 1e3) / 1e9
+    both, both_ce = 2 * moved / ((ms_out + ms_in) / 1e3) / 1e9, \
+        2 * moved / ((ce_out + ce_in) / 1e3) / 1e9
+    rl = roofline("link", both, round(both_ce, 2), "GB/s", None,
+                  "measured here: one contiguous cudaMemcpyAsync of the same bytes each way "
+                  "between pinned host memory and the device")
+    return {"value": round(both, 2), "unit": "GB/s", "ms_per_step": round(ms_out + ms_in, 5),
+            "bytes_per_step": 2 * moved, "launches": n1 + n2,
+            "kernels_ms": {"swap_out": round(ms_out, 5), "swap_in": round(ms_in, 5)},
+            "out": {"GB/s": round(gbs(ms_out), 2), "copy_engine_GB/s": round(gbs(ce_out), 2)},
+            "in": {"GB/s": round(gbs(ms_in), 2), "copy_engine_GB/s": round(gbs(ce_in), 2)},
+            "roofline": rl, "config": blocks_config(name)}
+
+
 # ---------------------------------------------------------------------------------------
 # oracle (CPU) arm
 # ---------------------------------------------------------------------------------------
@@ -555,7 +642,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode")
     ap.add_argument("--extra", default="long_context_decode,tiny_decode,ragged_prefill,"
-                                       "chunked_paged_prefill",
+                                       "chunked_paged_prefill,copy_blocks_fork,swap_blocks",
                     help="other workloads measured in the same run (N=1 only); 'none' for none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -609,6 +696,11 @@ def main(argv=None):
     extra = {}
     if world == 1 and args.extra:
         for name in [x for x in args.extra.split(",") if x and x not in ("none", args.workload)]:
+            if name in BLOCK_LEGS:
+                extra[name] = bench_blocks(name, max(3, min(args.steps, 50)), args.warmup, dev,
+                                           stream, peaks, peak_kind)
+                torch.cuda.empty_cache()
+                continue
             wx = W.WORKLOADS[name]()
             try:
                 if isinstance(wx, W.DecodeWorkload):

@@ -20,6 +20,10 @@
  *   pa_block_table_sync upload of the changed rows of a block table, for
  *                       CUDA-graph replays of the decode ("libmir-cuda
  *                       attention/mod.rs", captured decode nodes)
+ *   pa_copy_blocks      copy-on-write page copies inside every layer's K and
+ *                       V pools ("paged_attn.py", PagedAttention.copy_blocks)
+ *   pa_swap_blocks      page copies between pools on the device and in pinned
+ *                       host memory ("paged_attn.py", PagedAttention.swap_blocks)
  *
  * Conventions shared by every entry point:
  *  - All data pointers are DEVICE pointers of the current CUDA device unless
@@ -244,6 +248,55 @@ int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
  */
 int pa_block_table_sync(const int32_t *host_table, int32_t *snapshot, int32_t *device_table,
                         int num_rows, int row_len, int *rows_uploaded, void *stream);
+
+/*
+ * Whole-page copies ("paged_attn.py", PagedAttention.copy_blocks and
+ * PagedAttention.swap_blocks).  A page of a pool is the block_bytes contiguous
+ * bytes at byte offset page * block_bytes (block_bytes = stride_block * element
+ * size for a dense pool of either page layout); block_bytes must be a positive
+ * multiple of 16 and every pool 16-byte aligned.
+ * block_mapping is [num_pairs][2] int64 (source page, destination page).  For
+ * each pair and each pool, the source page's bytes become the destination
+ * page's bytes, bit for bit.  A pair with a negative entry is skipped (padding);
+ * a pair with a source >= the source pool's block count or a destination >=
+ * the destination pool's block count is skipped and sets PA_ERR_DEVICE_BOUNDS
+ * in the device status word.  A destination that appears twice, or that is
+ * also a source in the same call, gives an unspecified result.  One kernel
+ * launch moves every (pair, pool) of a call (one launch per 128 pools); the
+ * calls allocate nothing and return once the work is enqueued on `stream`.
+ */
+
+/*
+ * pa_copy_blocks -- copy_blocks: the pairs are applied inside each of the
+ * num_pools pools (pass every layer's key pool and value pool, e.g.
+ * [k_0, v_0, k_1, v_1, ...]); all pools have num_blocks pages.
+ *   pools          HOST array of num_pools device pointers
+ *   block_mapping  device memory (or pinned host memory whose device address
+ *                  equals its host address, as cudaHostAlloc gives), read by
+ *                  the kernel; the call makes no CUDA runtime query, so it can
+ *                  be captured into a CUDA graph.
+ * Returns PA_OK, PA_ERR_INVALID or PA_ERR_CUDA.
+ */
+int pa_copy_blocks(void *const *pools, int num_pools, const int64_t *block_mapping,
+                   int64_t num_pairs, int64_t num_blocks, int64_t block_bytes, void *stream);
+
+/*
+ * pa_swap_blocks -- swap_blocks: pool i of src_pools (src_num_blocks pages)
+ * into pool i of dst_pools (dst_num_blocks pages), for i < num_pools <= 4096.
+ * Each pool and block_mapping may be device memory of the current device or
+ * pinned host memory (cudaHostAlloc / cudaHostRegister), or any host memory on
+ * a device that can read pageable memory; host pages are read and written by
+ * the kernel directly over the CPU-GPU link.  The host addresses are resolved
+ * with cudaPointerGetAttributes on every call (capture this call only where that
+ * query is allowed).  Memory that the device cannot address is rejected with
+ * PA_ERR_INVALID.  Host memory must stay valid and unchanged until the stream
+ * has run the copy.
+ *   src_pools, dst_pools  HOST arrays of num_pools pointers
+ * Returns PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED or PA_ERR_CUDA.
+ */
+int pa_swap_blocks(const void *const *src_pools, void *const *dst_pools, int num_pools,
+                   const int64_t *block_mapping, int64_t num_pairs, int64_t src_num_blocks,
+                   int64_t dst_num_blocks, int64_t block_bytes, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

@@ -51,6 +51,10 @@ def load_library(path: str):
     lib.oracle_prefill.argtypes = [P, P, P, P, P, P, P, I, I, L, L, L, I, I, I, I, D, I,
                                    P, L, I]
     lib.oracle_prefill.restype = I
+    lib.oracle_swap_blocks.argtypes = [P, P, P, L, L, L, L]
+    lib.oracle_swap_blocks.restype = L
+    lib.oracle_copy_blocks.argtypes = [P, I, P, L, L, L]
+    lib.oracle_copy_blocks.restype = L
     return lib
 
 
@@ -193,3 +197,30 @@ def prefill(q, k, v, qo_indptr, kv_indptr, num_kv_heads, scale, causal=True,
                                 nthreads or default_threads())
     assert rc == 0
     return out
+
+
+def _pages(pool):
+    """(num_blocks, block_bytes) of a C-contiguous numpy pool [num_blocks, ...]."""
+    assert pool.flags.c_contiguous
+    return pool.shape[0], pool.nbytes // max(1, pool.shape[0])
+
+
+def swap_blocks(src, dst, block_mapping):
+    """In-place page copies src -> dst (numpy pools) for the int64 [n, 2] pairs;
+    returns the number of out-of-range pairs."""
+    bm = _c(block_mapping, np.int64).reshape(-1, 2)
+    snb, sbb = _pages(src)
+    dnb, dbb = _pages(dst)
+    assert sbb == dbb
+    return _load().oracle_swap_blocks(_ptr(src), _ptr(dst), _ptr(bm), bm.shape[0], snb, dnb, sbb)
+
+
+def copy_blocks(pools, block_mapping):
+    """In-place page copies inside each numpy pool of the list; returns the number of
+    out-of-range pairs summed over the pools."""
+    bm = _c(block_mapping, np.int64).reshape(-1, 2)
+    nb, bb = _pages(pools[0])
+    for p in pools:
+        assert _pages(p) == (nb, bb)
+    arr = (ctypes.c_void_p * len(pools))(*[p.ctypes.data for p in pools])
+    return _load().oracle_copy_blocks(arr, len(pools), _ptr(bm), bm.shape[0], nb, bb)

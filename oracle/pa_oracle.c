@@ -22,6 +22,8 @@
  *        oracle_merge_partitions
  *      PagedAttention._forward_prefix_pytorch (cached context, then the new
  *        chunk under the mask k_rel > q_rel)   -> oracle_prefill, paged mode
+ *      PagedAttention.swap_blocks / copy_blocks -> oracle_swap_blocks,
+ *        oracle_copy_blocks
  *  - "spark_runtime/flashinfer.rs" (Atlas): ragged_prefill_bf16_hd256 and its
  *      CPU reference test (per request, per head, kh = h / group, causal)
  *                                            -> oracle_prefill, contiguous mode
@@ -33,6 +35,7 @@
  *  R3 a query row (or a sequence) with no visible key yields an all-zero row.
  *  R4 partition p covers tokens [P*p, min(P*(p+1), L)); o_p is normalised by
  *     l_p, m_p is the max of the scaled scores (natural-log units).
+ *  R13 a page-copy pair with a negative entry is padding and is skipped.
  *
  * Parity status: every function here is pinned by the CPU test-suite
  * (brute-force dense attention written separately, closed forms and
@@ -422,4 +425,48 @@ int oracle_prefill(double *out, const uint16_t *q, const uint16_t *k, const uint
     int64_t nr = rows ? n_rows : (int64_t)qo_indptr[batch];
     run_items(prefill_item, &c, nr * nq, nthreads);
     return 0;
+}
+
+/* ---- whole-page copies ------------------------------------------------------ */
+
+/*
+ * swap_blocks ("paged_attn.py", PagedAttention.swap_blocks, which applies the
+ * op to the key pool and then to the value pool): the pairs are taken in order;
+ * pair i is (s, d) = (mapping[2i], mapping[2i + 1]) and copies page s of src --
+ * the block_bytes bytes from byte s * block_bytes on -- to page d of dst.
+ * R13: a pair with a negative entry is padding and is skipped, as a negative
+ * slot is in the cache write; a pair with s >= src_blocks or d >= dst_blocks is
+ * skipped and counted.  Returns that count.
+ */
+int64_t oracle_swap_blocks(const uint8_t *src, uint8_t *dst, const int64_t *mapping,
+                           int64_t num_pairs, int64_t src_blocks, int64_t dst_blocks,
+                           int64_t block_bytes) {
+    int64_t bad = 0;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        int64_t s = mapping[2 * i], d = mapping[2 * i + 1];
+        if (s < 0 || d < 0) continue;
+        if (s >= src_blocks || d >= dst_blocks) {
+            ++bad;
+            continue;
+        }
+        const uint8_t *from = src + s * block_bytes;
+        uint8_t *to = dst + d * block_bytes;
+        for (int64_t b = 0; b < block_bytes; ++b) to[b] = from[b];
+    }
+    return bad;
+}
+
+/*
+ * copy_blocks ("paged_attn.py", PagedAttention.copy_blocks: the same pairs
+ * applied to every layer's key pool and value pool): the page copy above with
+ * source and destination the same pool, for each of the num_pools pools.
+ * Returns the number of out-of-range pairs (counted once per pool).
+ */
+int64_t oracle_copy_blocks(uint8_t *const *pools, int num_pools, const int64_t *mapping,
+                           int64_t num_pairs, int64_t num_blocks, int64_t block_bytes) {
+    int64_t bad = 0;
+    for (int t = 0; t < num_pools; ++t)
+        bad += oracle_swap_blocks(pools[t], pools[t], mapping, num_pairs, num_blocks,
+                                  num_blocks, block_bytes);
+    return bad;
 }

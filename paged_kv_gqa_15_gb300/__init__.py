@@ -60,6 +60,10 @@ def load():
     lib.pa_get_device_status.argtypes = [P, P]
     lib.pa_block_table_sync.argtypes = [P, P, P, I, I, P, P]
     lib.pa_block_table_sync.restype = I
+    lib.pa_copy_blocks.argtypes = [P, I, P, L, L, L, P]
+    lib.pa_copy_blocks.restype = I
+    lib.pa_swap_blocks.argtypes = [P, P, I, P, L, L, L, L, P]
+    lib.pa_swap_blocks.restype = I
     lib.pa_last_error.restype = ctypes.c_char_p
     for name in ("pa_write_cache", "pa_decode", "pa_decode_split", "pa_decode_partitions",
                  "pa_decode_merge", "pa_ragged_prefill",
@@ -123,6 +127,58 @@ def pa_block_table_sync(host_table, snapshot, device_table, stream=None) -> int:
                                       _ptr(device_table), rows, cols, ctypes.byref(n),
                                       _stream(stream) if torch.cuda.is_available() else None))
     return n.value
+
+
+def _page_geometry(pools):
+    """(num_blocks, block_bytes) shared by a list of pools, each [num_blocks, ...] with
+    densely packed pages (page b = bytes [b * block_bytes, (b + 1) * block_bytes))."""
+    nb, bb = None, None
+    for t in pools:
+        page_elems = t[0].numel() if t.shape[0] > 0 else 0
+        assert t.stride(0) == page_elems and t[0].is_contiguous(), \
+            "pool pages must be densely packed"
+        b = page_elems * t.element_size()
+        assert (nb, bb) in ((None, None), (t.shape[0], b)), "pools differ in geometry"
+        nb, bb = t.shape[0], b
+    return nb, bb
+
+
+def _pointer_array(tensors):
+    arr = (ctypes.c_void_p * max(1, len(tensors)))()
+    for i, t in enumerate(tensors):
+        arr[i] = t.data_ptr()
+    return arr
+
+
+def pa_copy_blocks(key_caches, value_caches, block_mapping, stream=None):
+    """copy_blocks: for every (src, dst) row of block_mapping (int64 [n, 2], on the
+    device), page src of every layer's key and value pool is copied to page dst."""
+    pools = [t for kv in zip(key_caches, value_caches) for t in kv]
+    if not pools or block_mapping.numel() == 0:
+        return
+    assert block_mapping.dtype == torch.int64 and block_mapping.is_contiguous()
+    nb, bb = _page_geometry(pools)
+    _check(load().pa_copy_blocks(_pointer_array(pools), len(pools), _ptr(block_mapping),
+                                 block_mapping.shape[0], nb, bb, _stream(stream)))
+
+
+def pa_swap_blocks(src, dst, block_mapping, stream=None):
+    """swap_blocks: page src of each source pool to page dst of the matching
+    destination pool, for every row of block_mapping (int64 [n, 2]).  src / dst are a
+    pool or a list of pools, each on the device or in pinned host memory; the mapping
+    may be on either side too."""
+    src = list(src) if isinstance(src, (list, tuple)) else [src]
+    dst = list(dst) if isinstance(dst, (list, tuple)) else [dst]
+    assert len(src) == len(dst)
+    if not src or block_mapping.numel() == 0:
+        return
+    assert block_mapping.dtype == torch.int64 and block_mapping.is_contiguous()
+    snb, sbb = _page_geometry(src)
+    dnb, dbb = _page_geometry(dst)
+    assert sbb == dbb, "source and destination pages differ in size"
+    _check(load().pa_swap_blocks(_pointer_array(src), _pointer_array(dst), len(src),
+                                 _ptr(block_mapping), block_mapping.shape[0], snb, dnb, sbb,
+                                 _stream(stream)))
 
 
 def pa_write_cache(k, v, k_cache, v_cache, slot_mapping, layout="HND", stream=None):

@@ -136,6 +136,8 @@ int decode_common(pa::DecodeParams &p, void *out, const void *q, const void *k_c
 
 int pa::set_error(int code, const char *msg) { return fail(code, "%s", msg); }
 
+int pa::api_status_ptr(int **out) { return status_ptr(out); }
+
 extern "C" {
 
 const char *pa_last_error(void) { return g_last_error; }

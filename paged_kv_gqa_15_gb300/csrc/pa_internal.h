@@ -78,5 +78,7 @@ cudaError_t launch_prefill(PrefillParams &p, const PrefillLaunch &L, cudaStream_
 
 // Records `msg` as this thread's pa_last_error() text and returns `code`.
 int set_error(int code, const char *msg);
+// Device address of the current device's status word (PA_OK or an error status).
+int api_status_ptr(int **out);
 
 }  // namespace pa

@@ -132,3 +132,31 @@ def test_block_table_sync_uploads_nothing_when_unchanged():
                                    None) == pa.PA_ERR_INVALID
     assert lib.pa_block_table_sync(host.ctypes.data, snap.ctypes.data, ctypes.c_void_p(8),
                                    -1, 4, None, None) == pa.PA_ERR_INVALID
+
+
+def test_page_copies_reject_bad_arguments(lib):
+    # validation happens before any CUDA call, so this runs without a GPU
+    pools = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+    odd = (ctypes.c_void_p * 2)(0x10000, 0x20008)
+
+    def copy(pl=pools, n=2, m=FAKE, pairs=3, nb=10, bb=32768):
+        return lib.pa_copy_blocks(pl, n, m, pairs, nb, bb, None)
+    assert copy(bb=100) == pa.PA_ERR_INVALID          # not a multiple of 16
+    assert copy(bb=0) == pa.PA_ERR_INVALID
+    assert copy(pairs=-1) == pa.PA_ERR_INVALID
+    assert copy(n=-1) == pa.PA_ERR_INVALID
+    assert copy(m=None) == pa.PA_ERR_INVALID
+    assert copy(nb=0) == pa.PA_ERR_INVALID
+    assert copy(pl=odd) == pa.PA_ERR_INVALID
+    assert copy(pl=None) == pa.PA_ERR_INVALID
+    assert copy(pairs=0) == pa.PA_OK                  # nothing to do, nothing enqueued
+    assert copy(n=0) == pa.PA_OK
+
+    def swap(src=pools, dst=pools, n=2, m=FAKE, pairs=3, snb=10, dnb=4, bb=32768):
+        return lib.pa_swap_blocks(src, dst, n, m, pairs, snb, dnb, bb, None)
+    assert swap(bb=24) == pa.PA_ERR_INVALID
+    assert swap(dnb=0) == pa.PA_ERR_INVALID
+    assert swap(m=None) == pa.PA_ERR_INVALID
+    assert swap(src=None) == pa.PA_ERR_INVALID
+    assert swap(n=5000) == pa.PA_ERR_UNSUPPORTED
+    assert swap(pairs=0) == pa.PA_OK

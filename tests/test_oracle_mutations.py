@@ -35,6 +35,16 @@ MUTATIONS = {
     "partition_unnormalised": ("for (int e = 0; e < d->hd; ++e) op[e] /= lsum;", ""),
     "max_not_subtracted": ("double p = exp(scores[j] - mx);", "double p = exp(scores[j]);"),
     "wrong_exp_sign": ("double w = exp(sc[j - j0] - mx);", "double w = exp(mx - sc[j - j0]);"),
+    "pair_columns_swapped": ("int64_t s = mapping[2 * i], d = mapping[2 * i + 1];",
+                             "int64_t d = mapping[2 * i], s = mapping[2 * i + 1];"),
+    "copy_from_destination_index": ("const uint8_t *from = src + s * block_bytes;",
+                                    "const uint8_t *from = src + d * block_bytes;"),
+    "half_page_copied": ("for (int64_t b = 0; b < block_bytes; ++b) to[b] = from[b];",
+                         "for (int64_t b = 0; b < block_bytes / 2; ++b) to[b] = from[b];"),
+    "page_bound_off_by_one": ("if (s >= src_blocks || d >= dst_blocks) {",
+                              "if (s > src_blocks || d > dst_blocks) {"),
+    "first_pool_only": ("for (int t = 0; t < num_pools; ++t)\n        bad +=",
+                        "for (int t = 0; t < 1; ++t)\n        bad +="),
 }
 
 
@@ -93,7 +103,26 @@ def _check_large_logits():
     np.testing.assert_allclose(got, ref, atol=1e-12, rtol=0)
 
 
-CHECKS = [_check_decode, _check_prefill, _check_split, _check_write, _check_large_logits]
+def _check_blocks():
+    rng = np.random.default_rng(8)
+    pools = [rng.integers(0, 256, size=(6, 48), dtype=np.uint8) for _ in range(3)]
+    ref = [p.copy() for p in pools]
+    # pairs past the end of the pool must be skipped: (5, 6) would write one page past it,
+    # so the pools get a guard page that has to stay untouched
+    guarded = [np.concatenate([p, np.full((1, 48), 0xAB, np.uint8)]) for p in pools]
+    views = [g[:6] for g in guarded]
+    bad = oracle.copy_blocks(views, [(1, 4), (2, 0), (5, 6), (6, 3)])
+    assert bad == 2 * len(pools)
+    for g, r in zip(guarded, ref):
+        exp = r.copy()
+        exp[4] = r[1]
+        exp[0] = r[2]
+        np.testing.assert_array_equal(g[:6], exp)
+        np.testing.assert_array_equal(g[6], 0xAB)
+
+
+CHECKS = [_check_decode, _check_prefill, _check_split, _check_write, _check_large_logits,
+          _check_blocks]
 
 
 def _run_checks_in_child(lib_path):
