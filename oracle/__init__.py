@@ -41,15 +41,15 @@ def load_library(path: str):
     I, L, D = ctypes.c_int, ctypes.c_int64, ctypes.c_double
     lib.oracle_write_cache.argtypes = [P, P, P, P, P, L, I, I, I, L, L, L, L]
     lib.oracle_write_cache.restype = L
-    lib.oracle_decode.argtypes = [P, P, P, P, L, L, L, P, P, I, I, I, I, I, I, D, P, L, I]
+    lib.oracle_decode.argtypes = [P, P, P, P, L, L, L, P, P, I, I, I, I, I, I, D, P, L, I, I]
     lib.oracle_decode.restype = I
     lib.oracle_decode_partitions.argtypes = [P, P, P, P, P, P, L, L, L, P, P, I, I, I, I,
-                                             I, I, D, I, I, I]
+                                             I, I, D, I, I, I, I]
     lib.oracle_decode_partitions.restype = I
-    lib.oracle_merge_partitions.argtypes = [P, P, P, P, P, I, I, I, I, I]
+    lib.oracle_merge_partitions.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
     lib.oracle_merge_partitions.restype = I
     lib.oracle_prefill.argtypes = [P, P, P, P, P, P, P, I, I, L, L, L, I, I, I, I, D, I,
-                                   P, L, I]
+                                   P, L, I, I]
     lib.oracle_prefill.restype = I
     lib.oracle_swap_blocks.argtypes = [P, P, P, L, L, L, L]
     lib.oracle_swap_blocks.restype = L
@@ -117,8 +117,9 @@ def write_cache(k, v, k_cache, v_cache, slot_mapping, block_size, strides=None):
 
 
 def decode(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, block_size, scale,
-           strides=None, items=None, nthreads=None, out=None):
-    """softmax(scale q K^T) V per (sequence, query head), fp64 [B][nq][hd]."""
+           strides=None, items=None, nthreads=None, out=None, window=0):
+    """softmax(scale q K^T) V per (sequence, query head), fp64 [B][nq][hd]; window > 0
+    keeps the last `window` keys of each sequence."""
     q = _c(q, np.uint16)
     B, nq, hd = q.shape
     bt = _c(block_tables, np.int32)
@@ -132,13 +133,13 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, block_size
                                _ptr(_c(v_cache, np.uint16)), *strides, _ptr(bt), _ptr(sl),
                                B, nq, num_kv_heads, hd, block_size, bt.shape[1], scale,
                                _ptr(it), 0 if it is None else it.size,
-                               nthreads or default_threads())
+                               nthreads or default_threads(), int(window))
     assert rc == 0
     return out
 
 
 def decode_partitions(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, block_size,
-                      scale, max_parts, strides=None, part=PARTITION, nthreads=None):
+                      scale, max_parts, strides=None, part=PARTITION, nthreads=None, window=0):
     """Per-partition (m, l, o) of the split-KV pass; untouched entries are NaN."""
     q = _c(q, np.uint16)
     B, nq, hd = q.shape
@@ -154,12 +155,12 @@ def decode_partitions(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads,
                                           _ptr(_c(v_cache, np.uint16)), *strides, _ptr(bt),
                                           _ptr(sl), B, nq, num_kv_heads, hd, block_size,
                                           bt.shape[1], scale, part, max_parts,
-                                          nthreads or default_threads())
+                                          nthreads or default_threads(), int(window))
     assert rc == 0
     return m, l, o
 
 
-def merge_partitions(m, l, o, seq_lens, part=PARTITION):
+def merge_partitions(m, l, o, seq_lens, part=PARTITION, window=0):
     """Log-sum-exp merge of partition results, fp64 [B][nq][hd]."""
     m = _c(m, np.float64)
     l = _c(l, np.float64)
@@ -167,14 +168,15 @@ def merge_partitions(m, l, o, seq_lens, part=PARTITION):
     B, nq, P, hd = o.shape
     out = np.zeros((B, nq, hd), np.float64)
     rc = _load().oracle_merge_partitions(_ptr(out), _ptr(m), _ptr(l), _ptr(o),
-                                         _ptr(_c(seq_lens, np.int32)), B, nq, hd, part, P)
+                                         _ptr(_c(seq_lens, np.int32)), B, nq, hd, part, P,
+                                         int(window))
     assert rc == 0
     return out
 
 
 def prefill(q, k, v, qo_indptr, kv_indptr, num_kv_heads, scale, causal=True,
             block_tables=None, block_size=16, strides=None, rows=None, nthreads=None,
-            out=None):
+            out=None, window=0):
     """Ragged prefill, fp64 [total_qo][nq][hd]; contiguous (block_tables None) or paged."""
     q = _c(q, np.uint16)
     total_qo, nq, hd = q.shape
@@ -194,7 +196,7 @@ def prefill(q, k, v, qo_indptr, kv_indptr, num_kv_heads, scale, causal=True,
                                 0 if bt is None else bt.shape[1], block_size, *strides,
                                 batch, nq, num_kv_heads, hd, scale, 1 if causal else 0,
                                 _ptr(rw), 0 if rw is None else rw.size,
-                                nthreads or default_threads())
+                                nthreads or default_threads(), int(window))
     assert rc == 0
     return out
 

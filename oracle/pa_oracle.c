@@ -36,6 +36,13 @@
  *  R4 partition p covers tokens [P*p, min(P*(p+1), L)); o_p is normalised by
  *     l_p, m_p is the max of the scaled scores (natural-log units).
  *  R13 a page-copy pair with a negative entry is padding and is skipped.
+ *  R14 a sliding window of W > 0 keys ("paged_attn.py", forward_prefix's
+ *     sliding_window; "libmir-cuda attention/mod.rs", active_partitions(token
+ *     count, window)): a query at position pos sees only keys j > pos - W, the
+ *     W most recent keys including its own position (and, if causal, j <= pos).
+ *     W <= 0 means no window.  In decode pos = L - 1.  Split partitions keep
+ *     their absolute 512-token ranges; partitions wholly before the window are
+ *     neither computed nor merged.
  *
  * Parity status: every function here is pinned by the CPU test-suite
  * (brute-force dense attention written separately, closed forms and
@@ -142,6 +149,12 @@ static void attend_row(double *out, const uint16_t *q, const uint16_t *kbase,
     for (int d = 0; d < hd; ++d) out[d] /= den;
 }
 
+/* First key a query at position pos sees under a sliding window of w keys (R14). */
+static int64_t window_first(int64_t pos, int64_t w) {
+    if (w <= 0 || pos - w + 1 <= 0) return 0;
+    return pos - w + 1;
+}
+
 /* ---- cache write ------------------------------------------------------------ */
 
 /*
@@ -191,6 +204,7 @@ typedef struct {
     int nq, nkv, hd, bs, max_blocks;
     double scale;
     const int32_t *items;      /* optional list of b*nq+h items */
+    int window;                /* sliding window in keys (R14); <= 0: none */
 } decode_ctx;
 
 /* Element offset of token j of sequence b, kv head kh, in the paged pool. */
@@ -207,10 +221,13 @@ static void decode_item(void *vctx, int64_t it) {
     int kh = h / g; /* contiguous GQA groups */
     int64_t L = c->seq_lens[b];
     if (L < 0) L = 0;
-    int64_t *off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(L > 0 ? L : 1));
-    double *sc = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
-    for (int64_t j = 0; j < L; ++j) off[j] = paged_offset(c, b, kh, j);
-    attend_row(c->out + bh * c->hd, c->q + bh * c->hd, c->kc, c->vc, off, off, L,
+    /* keys j0 .. L-1: all of them, or the window's (R14) */
+    int64_t j0 = L > 0 ? window_first(L - 1, c->window) : 0;
+    int64_t n = L - j0;
+    int64_t *off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    double *sc = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    for (int64_t j = j0; j < L; ++j) off[j - j0] = paged_offset(c, b, kh, j);
+    attend_row(c->out + bh * c->hd, c->q + bh * c->hd, c->kc, c->vc, off, off, n,
                c->hd, c->scale, sc);
     free(off);
     free(sc);
@@ -221,7 +238,8 @@ static void decode_item(void *vctx, int64_t it) {
  * the exact softmax it computes tile by tile): for sequence b and query head h,
  * kh = h / (nq / nkv); the L = seq_lens[b] keys are token j at page
  * bt[b][j / bs], row j % bs.  out[b][h] = softmax(scale * q K^T) V; L == 0
- * gives zeros (the "seq_len == 0" branch of the same function).
+ * gives zeros (the "seq_len == 0" branch of the same function).  With a
+ * window > 0 only the last `window` keys are attended (R14).
  * items (optional, n_items entries of b * nq + h) restricts the work to those
  * output rows; the others are left untouched.
  */
@@ -230,10 +248,11 @@ int oracle_decode(double *out, const uint16_t *q, const uint16_t *k_cache,
                   int64_t s_token, const int32_t *block_tables,
                   const int32_t *seq_lens, int num_seqs, int nq, int nkv, int hd,
                   int bs, int max_blocks, double scale, const int32_t *items,
-                  int64_t n_items, int nthreads) {
+                  int64_t n_items, int nthreads, int window) {
     if (nkv <= 0 || nq % nkv != 0) return -1;
     decode_ctx c = {out, q, k_cache, v_cache, s_block, s_head, s_token,
-                    block_tables, seq_lens, nq, nkv, hd, bs, max_blocks, scale, items};
+                    block_tables, seq_lens, nq, nkv, hd, bs, max_blocks, scale, items,
+                    window};
     int64_t n = items ? n_items : (int64_t)num_seqs * nq;
     run_items(decode_item, &c, n, nthreads);
     return 0;
@@ -256,11 +275,14 @@ static void part_item(void *vctx, int64_t it) {
     int64_t L = d->seq_lens[b];
     if (L < 0) L = 0;
     int64_t np = (L + c->part - 1) / c->part;
+    /* the window's first key and the partition holding it (R14) */
+    int64_t jw = L > 0 ? window_first(L - 1, d->window) : 0;
     double *sc = (double *)malloc(sizeof(double) * (size_t)c->part);
     const uint16_t *qr = d->q + bh * d->hd;
-    for (int64_t p = 0; p < np && p < c->max_parts; ++p) {
+    for (int64_t p = jw / c->part; p < np && p < c->max_parts; ++p) {
         int64_t j0 = p * c->part, j1 = j0 + c->part;
         if (j1 > L) j1 = L;
+        if (j0 < jw) j0 = jw;
         /* m_p: max of the scaled scores in the partition (R4) */
         double mx = -INFINITY;
         for (int64_t j = j0; j < j1; ++j) {
@@ -292,7 +314,9 @@ static void part_item(void *vctx, int64_t it) {
  * Split-KV partition pass ("paged_attn.py", PagedAttention.forward_decode, V2
  * branch: _PARTITION_SIZE-token partitions, per-partition max_logits, exp_sums
  * and tmp_output).  For p < ceil(L / part): m_p, l_p, o_p as in R4.  Entries
- * for p >= ceil(L / part) are left untouched.
+ * for p >= ceil(L / part) are left untouched.  With a window > 0 (R14) the
+ * partitions run from the one holding key L - window on, that first one over
+ * its keys inside the window only; the earlier entries are left untouched.
  */
 int oracle_decode_partitions(double *m, double *l, double *o, const uint16_t *q,
                              const uint16_t *k_cache, const uint16_t *v_cache,
@@ -300,11 +324,12 @@ int oracle_decode_partitions(double *m, double *l, double *o, const uint16_t *q,
                              const int32_t *block_tables, const int32_t *seq_lens,
                              int num_seqs, int nq, int nkv, int hd, int bs,
                              int max_blocks, double scale, int part, int max_parts,
-                             int nthreads) {
+                             int nthreads, int window) {
     if (nkv <= 0 || nq % nkv != 0 || part <= 0) return -1;
     part_ctx c;
     decode_ctx d = {NULL, q, k_cache, v_cache, s_block, s_head, s_token,
-                    block_tables, seq_lens, nq, nkv, hd, bs, max_blocks, scale, NULL};
+                    block_tables, seq_lens, nq, nkv, hd, bs, max_blocks, scale, NULL,
+                    window};
     c.d = d;
     c.m = m;
     c.l = l;
@@ -320,26 +345,28 @@ int oracle_decode_partitions(double *m, double *l, double *o, const uint16_t *q,
  * w_p = l_p * exp(m_p - M), out = sum_p w_p o_p / sum_p w_p over
  * p < ceil(L / part); L == 0 gives zeros.  This is the rescale-and-add rule
  * that "paged_attn.py" (_forward_decode_pytorch) applies between tiles,
- * applied once over all partitions.
+ * applied once over all partitions -- with a window > 0, over the partitions
+ * from the one holding key L - window on (R14).
  */
 int oracle_merge_partitions(double *out, const double *m, const double *l,
                             const double *o, const int32_t *seq_lens, int num_seqs,
-                            int nq, int hd, int part, int max_parts) {
+                            int nq, int hd, int part, int max_parts, int window) {
     if (part <= 0) return -1;
     for (int b = 0; b < num_seqs; ++b) {
         int64_t L = seq_lens[b] > 0 ? seq_lens[b] : 0;
         int64_t np = (L + part - 1) / part;
         if (np > max_parts) np = max_parts;
+        int64_t p0 = (L > 0 ? window_first(L - 1, window) : 0) / part;
         for (int h = 0; h < nq; ++h) {
             int64_t bh = (int64_t)b * nq + h;
             double *dst = out + bh * hd;
             for (int e = 0; e < hd; ++e) dst[e] = 0.0;
             if (np == 0) continue;
             double M = -INFINITY;
-            for (int64_t p = 0; p < np; ++p)
+            for (int64_t p = p0; p < np; ++p)
                 if (m[bh * max_parts + p] > M) M = m[bh * max_parts + p];
             double W = 0.0;
-            for (int64_t p = 0; p < np; ++p) {
+            for (int64_t p = p0; p < np; ++p) {
                 double w = l[bh * max_parts + p] * exp(m[bh * max_parts + p] - M);
                 W += w;
                 const double *op = o + (bh * max_parts + p) * hd;
@@ -364,6 +391,7 @@ typedef struct {
     int batch, nq, nkv, hd, causal;
     double scale;
     const int64_t *rows;          /* optional list of query rows */
+    int window;                   /* sliding window in keys (R14); <= 0: none */
 } prefill_ctx;
 
 static void prefill_item(void *vctx, int64_t it) {
@@ -384,18 +412,21 @@ static void prefill_item(void *vctx, int64_t it) {
         if (lim < n) n = lim;
     }
     if (n < 0) n = 0;
-    int64_t *off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
-    double *sc = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
-    for (int64_t j = 0; j < n; ++j) {
+    /* and j > pos - window for the row's position pos = i + (kv - qo) (R14) */
+    int64_t lo = window_first(i + (kv - qo), c->window);
+    int64_t cnt = n > lo ? n - lo : 0;
+    int64_t *off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(cnt > 0 ? cnt : 1));
+    double *sc = (double *)malloc(sizeof(double) * (size_t)(cnt > 0 ? cnt : 1));
+    for (int64_t j = lo; j < n; ++j) {
         if (c->bt) {
             int64_t page = c->bt[(int64_t)r * c->max_blocks + j / c->bs];
-            off[j] = page * c->s_block + (int64_t)kh * c->s_head + (j % c->bs) * c->s_token;
+            off[j - lo] = page * c->s_block + (int64_t)kh * c->s_head + (j % c->bs) * c->s_token;
         } else {
-            off[j] = ((c->kv_indptr[r] + j) * c->nkv + kh) * (int64_t)c->hd;
+            off[j - lo] = ((c->kv_indptr[r] + j) * c->nkv + kh) * (int64_t)c->hd;
         }
     }
     int64_t oidx = (row * c->nq + h) * (int64_t)c->hd;
-    attend_row(c->out + oidx, c->q + oidx, c->k, c->v, off, off, n, c->hd, c->scale, sc);
+    attend_row(c->out + oidx, c->q + oidx, c->k, c->v, off, off, cnt, c->hd, c->scale, sc);
     free(off);
     free(sc);
 }
@@ -410,6 +441,7 @@ static void prefill_item(void *vctx, int64_t it) {
  * cache): key j is token j of the request's block table row, addressed as in
  * decode.  Query head h reads kv head h / (nq / nkv); causal masking per R2;
  * rows with no visible key are zero (R3).
+ * A window > 0 further limits row i to keys j > i + (kv - qo) - window (R14).
  * rows (optional, n_rows entries) restricts the work to those query rows (all
  * heads of each); other output rows are left untouched.
  */
@@ -418,10 +450,11 @@ int oracle_prefill(double *out, const uint16_t *q, const uint16_t *k, const uint
                    const int32_t *block_tables, int max_blocks, int bs, int64_t s_block,
                    int64_t s_head, int64_t s_token, int batch, int nq, int nkv, int hd,
                    double scale, int causal, const int64_t *rows, int64_t n_rows,
-                   int nthreads) {
+                   int nthreads, int window) {
     if (nkv <= 0 || nq % nkv != 0 || batch <= 0) return -1;
     prefill_ctx c = {out, q, k, v, qo_indptr, kv_indptr, block_tables, max_blocks, bs,
-                     s_block, s_head, s_token, batch, nq, nkv, hd, causal, scale, rows};
+                     s_block, s_head, s_token, batch, nq, nkv, hd, causal, scale, rows,
+                     window};
     int64_t nr = rows ? n_rows : (int64_t)qo_indptr[batch];
     run_items(prefill_item, &c, nr * nq, nthreads);
     return 0;

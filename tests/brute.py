@@ -50,7 +50,8 @@ def dense_softmax_attention(q, K, V, scale, visible=None):
     return out
 
 
-def brute_decode(q_bits, kc_bits, vc_bits, bt, seq_lens, nkv, bs, scale, strides):
+def brute_decode(q_bits, kc_bits, vc_bits, bt, seq_lens, nkv, bs, scale, strides, window=0):
+    """window > 0: the query (position L - 1) sees only keys j > L - 1 - window."""
     B, nq, hd = q_bits.shape
     g = nq // nkv
     q = widen(q_bits)
@@ -63,19 +64,28 @@ def brute_decode(q_bits, kc_bits, vc_bits, bt, seq_lens, nkv, bs, scale, strides
             if L == 0:
                 continue
             heads = list(range(kh * g, (kh + 1) * g))
-            out[b, heads] = dense_softmax_attention(q[b, heads], K, V, scale)
+            vis = None
+            if window > 0:
+                vis = np.repeat((np.arange(L) > L - 1 - window)[None, :], g, axis=0)
+            out[b, heads] = dense_softmax_attention(q[b, heads], K, V, scale, vis)
     return out
 
 
-def causal_visible(qo, kv, causal):
+def causal_visible(qo, kv, causal, window=0):
+    """Query row i sits at position i + kv - qo; causal keeps keys j <= that position and a
+    window W > 0 keeps keys j > position - W."""
     i = np.arange(qo)[:, None]
     j = np.arange(kv)[None, :]
-    if not causal:
-        return np.ones((qo, kv), bool)
-    return j <= i + (kv - qo)
+    vis = np.ones((qo, kv), bool)
+    if causal:
+        vis &= j <= i + (kv - qo)
+    if window > 0:
+        vis &= j > i + (kv - qo) - window
+    return vis
 
 
-def brute_prefill_contiguous(q_bits, k_bits, v_bits, qo_indptr, kv_indptr, nkv, scale, causal):
+def brute_prefill_contiguous(q_bits, k_bits, v_bits, qo_indptr, kv_indptr, nkv, scale, causal,
+                             window=0):
     T, nq, hd = q_bits.shape
     g = nq // nkv
     q, k, v = widen(q_bits), widen(k_bits), widen(v_bits)
@@ -83,7 +93,7 @@ def brute_prefill_contiguous(q_bits, k_bits, v_bits, qo_indptr, kv_indptr, nkv, 
     for r in range(len(qo_indptr) - 1):
         q0, q1 = qo_indptr[r], qo_indptr[r + 1]
         k0, k1 = kv_indptr[r], kv_indptr[r + 1]
-        vis = causal_visible(q1 - q0, k1 - k0, causal)
+        vis = causal_visible(q1 - q0, k1 - k0, causal, window)
         for h in range(nq):
             out[q0:q1, h] = dense_softmax_attention(q[q0:q1, h], k[k0:k1, h // g],
                                                     v[k0:k1, h // g], scale, vis)

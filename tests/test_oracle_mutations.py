@@ -45,6 +45,14 @@ MUTATIONS = {
                               "if (s > src_blocks || d > dst_blocks) {"),
     "first_pool_only": ("for (int t = 0; t < num_pools; ++t)\n        bad +=",
                         "for (int t = 0; t < 1; ++t)\n        bad +="),
+    "window_one_key_wider": ("    return pos - w + 1;\n}", "    return pos - w;\n}"),
+    "decode_window_from_length": ("int64_t j0 = L > 0 ? window_first(L - 1, c->window) : 0;",
+                                  "int64_t j0 = L > 0 ? window_first(L, c->window) : 0;"),
+    "partition_not_clipped_to_window": ("        if (j0 < jw) j0 = jw;\n", ""),
+    "merge_from_partition_zero": (
+        "int64_t p0 = (L > 0 ? window_first(L - 1, window) : 0) / part;", "int64_t p0 = 0;"),
+    "prefill_window_ignored": ("int64_t lo = window_first(i + (kv - qo), c->window);",
+                               "int64_t lo = 0;"),
 }
 
 
@@ -121,8 +129,36 @@ def _check_blocks():
         np.testing.assert_array_equal(g[6], 0xAB)
 
 
+def _check_window():
+    lens = [1, 17, 300, 513, 1100]
+    w = W.make_decode("mut", lens, 4, 2, 64, seed=40)
+    t = w.tensors("cpu")
+    q, kc, vc = (W.to_bits(t[n]) for n in ("q", "k_cache", "v_cache"))
+    strides = oracle.hnd_strides(2, 16, 64)
+    for window in (1, 100, 600):
+        ref = brute.brute_decode(q, kc, vc, w.block_tables, w.seq_lens, 2, 16, w.scale,
+                                 strides, window=window)
+        got = oracle.decode(q, kc, vc, w.block_tables, w.seq_lens, 2, 16, w.scale,
+                            window=window)
+        np.testing.assert_allclose(got, ref, atol=1e-12, rtol=0)
+        m, l, o = oracle.decode_partitions(q, kc, vc, w.block_tables, w.seq_lens, 2, 16,
+                                           w.scale, 3, window=window)
+        merged = oracle.merge_partitions(m, l, o, w.seq_lens, window=window)
+        np.testing.assert_allclose(merged, ref, atol=1e-12, rtol=0)
+    qo, kv = np.array([6, 40, 3]), np.array([6, 50, 9])
+    wp = W.make_prefill("mut", qo, kv, 4, 2, 64, seed=41)
+    tp = wp.tensors("cpu")
+    qq, k, v = (W.to_bits(tp[n]) for n in ("q", "k", "v"))
+    for causal in (True, False):
+        got = oracle.prefill(qq, k, v, wp.qo_indptr, wp.kv_indptr, 2, wp.scale, causal=causal,
+                             window=5)
+        ref = brute.brute_prefill_contiguous(qq, k, v, wp.qo_indptr, wp.kv_indptr, 2, wp.scale,
+                                             causal, window=5)
+        np.testing.assert_allclose(got, ref, atol=1e-12, rtol=0)
+
+
 CHECKS = [_check_decode, _check_prefill, _check_split, _check_write, _check_large_logits,
-          _check_blocks]
+          _check_blocks, _check_window]
 
 
 def _run_checks_in_child(lib_path):
