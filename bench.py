@@ -214,16 +214,16 @@ def decode_step(w, s, stream, evs=None):
             evs.append(_ev(stream))
     if not w.split:   # the workload's decode is one pass over each sequence
         pa.pa_decode(s["out"], t["q"], t["k_cache"], t["v_cache"], s["bt"], s["sl"], w.scale,
-                     stream=stream)
+                     stream=stream, sliding_window=w.window)
         if evs is not None:
             evs.append(_ev(stream))
         return n + 1
     L = max(w.max_seq_len, 1)
     pa.pa_decode_partitions(t["q"], t["k_cache"], t["v_cache"], s["bt"], s["sl"], w.scale, L,
-                            s["ws"], stream=stream)
+                            s["ws"], stream=stream, sliding_window=w.window)
     if evs is not None:
         evs.append(_ev(stream))
-    pa.pa_decode_merge(s["out"], s["sl"], L, s["ws"], stream=stream)
+    pa.pa_decode_merge(s["out"], s["sl"], L, s["ws"], stream=stream, sliding_window=w.window)
     if evs is not None:
         evs.append(_ev(stream))
     return n + 2
@@ -420,7 +420,8 @@ def bench_prefill(w, steps, warmup, dev, stream, peaks, peak_kind):
         k = t["k_cache"] if w.paged else t["k"]
         v = t["v_cache"] if w.paged else t["v"]
         pa.pa_ragged_prefill(o, t["q"], k, v, w.qo_indptr, w.kv_indptr, qo_d, kv_d, w.scale,
-                             causal=w.causal, block_tables=bt, workspace=ws, stream=stream)
+                             causal=w.causal, block_tables=bt, workspace=ws, stream=stream,
+                             sliding_window=w.window)
         if evs is not None:
             evs.append(_ev(stream))
         return n + 1
@@ -538,9 +539,12 @@ def oracle_decode_time(w, t_host, seqs, nthreads):
     seqs = np.asarray(seqs)
     t0 = time.perf_counter()
     oracle.decode(q[seqs], kc, vc, w.block_tables[seqs], w.seq_lens[seqs], w.num_kv_heads,
-                  w.block_size, w.scale, nthreads=nthreads)
+                  w.block_size, w.scale, nthreads=nthreads, window=w.window)
     dt = time.perf_counter() - t0
-    kv = int(w.seq_lens[seqs].astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 4
+    lens = w.seq_lens[seqs].astype(np.int64)
+    if w.window > 0:
+        lens = np.minimum(lens, w.window)
+    kv = int(lens.sum()) * w.num_kv_heads * w.head_dim * 4
     return dt, kv
 
 
@@ -625,11 +629,12 @@ def workload_config(w):
                 "block_size": w.block_size,
                 "seq_lens": f"U[{int(w.seq_lens.min())},{int(w.seq_lens.max())}] seed {w.seed}",
                 "num_blocks": w.num_blocks, "kv_bytes_per_step": w.kv_bytes(),
-                "l2": l2_note(decode_footprint(w))}
+                "sliding_window": w.window or None, "l2": l2_note(decode_footprint(w))}
     return {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "causal": w.causal,
             "paged": w.paged, "total_qo": w.total_qo, "total_kv": w.total_kv,
-            "flops_per_step": w.flops(), "l2": l2_note(prefill_footprint(w))}
+            "sliding_window": w.window or None, "flops_per_step": w.flops(),
+            "l2": l2_note(prefill_footprint(w))}
 
 
 # ---------------------------------------------------------------------------------------
@@ -642,7 +647,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode")
     ap.add_argument("--extra", default="long_context_decode,tiny_decode,ragged_prefill,"
-                                       "chunked_paged_prefill,copy_blocks_fork,swap_blocks",
+                                       "chunked_paged_prefill,window_decode,window_prefill,"
+                                       "copy_blocks_fork,swap_blocks",
                     help="other workloads measured in the same run (N=1 only); 'none' for none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -41,6 +41,13 @@
  *  - Supported shapes: head_dim in {64, 128, 256}; block_size == 16;
  *    num_q_heads % num_kv_heads == 0 with group size in {1, 2, 4, 8}.
  *    Pointers must be 16-byte aligned and strides multiples of 8 elements.
+ *  - sliding_window (decode and prefill): a query at position pos attends only
+ *    to keys j > pos - sliding_window, the sliding_window most recent keys
+ *    including its own position ("paged_attn.py", forward_prefix's
+ *    sliding_window; "libmir-cuda attention/mod.rs", active_partitions(token
+ *    count, window)).  sliding_window <= 0 means no window.  A decode query sits
+ *    at position seq_len - 1.  Block-table entries of pages that lie wholly
+ *    before a query's window are never read, so a caller may recycle them.
  *  - Return value: PA_OK or an error status; on error nothing was enqueued and
  *    pa_last_error() (thread-local) describes the problem.
  *  - Device-side guards: a block-table entry outside [0, num_blocks), a
@@ -108,7 +115,8 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
               int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
-              int64_t stride_head, int64_t stride_token, float sm_scale, void *stream);
+              int64_t stride_head, int64_t stride_token, float sm_scale, int sliding_window,
+              void *stream);
 
 /*
  * Bytes of workspace pa_decode_split needs (256-byte aligned sub-buffers):
@@ -130,7 +138,9 @@ void pa_decode_split_workspace_offsets(int num_seqs, int num_q_heads, int head_d
  * of query heads m_p = max of the scaled scores over tokens
  * [512 p, min(512 (p+1), L)), l_p = sum exp(s - m_p) and
  * o_p = sum exp(s - m_p) V / l_p, into the workspace (fp32).  Partitions at or
- * past ceil(L / 512) are neither written nor read.
+ * past ceil(L / 512) are neither written nor read; under a sliding window, neither
+ * are those before the partition holding key L - sliding_window, whose tokens
+ * before the window are left out of its m_p, l_p and o_p.
  * Pass 2 (merge): M = max_p m_p, w_p = l_p exp(m_p - M),
  * out = sum_p w_p o_p / sum_p w_p, rounded to bf16; L == 0 gives zeros.
  * max_seq_len must be >= every seq_lens[b]; a larger seq_len is clamped to it
@@ -142,13 +152,14 @@ int pa_decode_split(void *out, const void *q, const void *k_cache, const void *v
                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                     int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
                     int64_t stride_head, int64_t stride_token, float sm_scale,
-                    int max_seq_len, void *workspace, size_t workspace_bytes,
-                    void *stream);
+                    int sliding_window, int max_seq_len, void *workspace,
+                    size_t workspace_bytes, void *stream);
 
 /*
  * The two passes of pa_decode_split as separate calls (same arguments and
  * workspace): pa_decode_partitions writes the per-partition (m_p, l_p, o_p)
- * into the workspace; pa_decode_merge reads them and writes out.
+ * into the workspace; pa_decode_merge reads them and writes out.  Both passes
+ * must be given the same sliding_window.
  * pa_decode_split == pa_decode_partitions followed by pa_decode_merge.
  */
 int pa_decode_partitions(const void *q, const void *k_cache, const void *v_cache,
@@ -156,10 +167,10 @@ int pa_decode_partitions(const void *q, const void *k_cache, const void *v_cache
                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                          int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
                          int64_t stride_head, int64_t stride_token, float sm_scale,
-                         int max_seq_len, void *workspace, size_t workspace_bytes,
-                         void *stream);
+                         int sliding_window, int max_seq_len, void *workspace,
+                         size_t workspace_bytes, void *stream);
 int pa_decode_merge(void *out, const int32_t *seq_lens, int num_seqs, int num_q_heads,
-                    int head_dim, int max_seq_len, const void *workspace,
+                    int head_dim, int max_seq_len, int sliding_window, const void *workspace,
                     size_t workspace_bytes, void *stream);
 
 /*
@@ -188,7 +199,7 @@ int pa_decode_split_static(void *out, const void *q, const void *k_cache, const 
                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                            int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
                            int64_t stride_head, int64_t stride_token, float sm_scale,
-                           int max_seq_len, void *stream);
+                           int sliding_window, int max_seq_len, void *stream);
 
 /*
  * Bytes of workspace pa_ragged_prefill needs (a device-built tile schedule).
@@ -202,8 +213,9 @@ size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_
  * kv_len_r = kv_indptr[r+1] - kv_indptr[r] keys.  Query row i of request r,
  * head h, attends to keys j < kv_len_r of kv head h / (num_q_heads/num_kv_heads)
  * and, if causal != 0, only to j <= i + (kv_len_r - qo_len_r) (bottom-right
- * alignment: the query rows are the LAST qo_len_r positions).  A row with no
- * visible key is written as zeros.
+ * alignment: the query rows are the LAST qo_len_r positions).  Under a sliding
+ * window, row i sees only keys j > i + (kv_len_r - qo_len_r) - sliding_window.
+ * A row with no visible key is written as zeros.
  *   o, q  [total_qo_rows][num_q_heads][head_dim] bf16
  *   Contiguous mode (block_tables == NULL): k, v are
  *         [total_kv_rows][num_kv_heads][head_dim] bf16 and key j of request r
@@ -223,8 +235,8 @@ int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
                       int64_t num_blocks, int64_t stride_block, int64_t stride_head,
                       int64_t stride_token, int batch, int total_qo_rows,
                       int total_kv_rows, int num_q_heads, int num_kv_heads, int head_dim,
-                      float sm_scale, int causal, void *workspace, size_t workspace_bytes,
-                      void *stream);
+                      float sm_scale, int causal, int sliding_window, void *workspace,
+                      size_t workspace_bytes, void *stream);
 
 /*
  * Block-table upload for CUDA-graph replays ("libmir-cuda attention/mod.rs",

@@ -42,21 +42,23 @@ def load():
     P, I, L, F, Z = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                      ctypes.c_size_t)
     lib.pa_write_cache.argtypes = [P, P, P, P, P, L, I, I, I, L, L, L, L, P]
-    lib.pa_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, P]
+    lib.pa_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, P]
     lib.pa_decode_split_workspace_size.argtypes = [I, I, I, I]
     lib.pa_decode_split_workspace_size.restype = Z
     lib.pa_decode_split_workspace_offsets.argtypes = [I, I, I, I, P, P, P]
     lib.pa_decode_split_workspace_offsets.restype = None
-    lib.pa_decode_split.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, P, Z, P]
-    lib.pa_decode_partitions.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, P, Z, P]
-    lib.pa_decode_merge.argtypes = [P, P, I, I, I, I, P, Z, P]
+    lib.pa_decode_split.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, I, P,
+                                    Z, P]
+    lib.pa_decode_partitions.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, I, P,
+                                         Z, P]
+    lib.pa_decode_merge.argtypes = [P, P, I, I, I, I, I, P, Z, P]
     lib.pa_decode_split_static.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I,
-                                           P]
+                                           I, P]
     lib.pa_decode_split_static.restype = I
     lib.pa_ragged_prefill_workspace_size.argtypes = [I, I, I, I]
     lib.pa_ragged_prefill_workspace_size.restype = Z
     lib.pa_ragged_prefill.argtypes = [P, P, P, P, P, P, P, P, P, I, I, L, L, L, L, I, I, I, I, I,
-                                      I, F, I, P, Z, P]
+                                      I, F, I, I, P, Z, P]
     lib.pa_get_device_status.argtypes = [P, P]
     lib.pa_block_table_sync.argtypes = [P, P, P, I, I, P, P]
     lib.pa_block_table_sync.restype = I
@@ -191,14 +193,15 @@ def pa_write_cache(k, v, k_cache, v_cache, slot_mapping, layout="HND", stream=No
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale, layout="HND",
-              stream=None):
-    """Single-pass paged GQA decode into out [B, nq, hd]."""
+              stream=None, sliding_window=0):
+    """Single-pass paged GQA decode into out [B, nq, hd]; sliding_window > 0 keeps the
+    last sliding_window keys of each sequence."""
     nb, nkv, bs, hd = _pool_geometry(k_cache, layout)
     sb, sh, st = pool_strides(k_cache, layout)
     B, nq, _ = q.shape
     _check(load().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                             _ptr(seq_lens), B, nq, nkv, hd, bs, block_tables.shape[1], nb, sb,
-                            sh, st, float(sm_scale), _stream(stream)))
+                            sh, st, float(sm_scale), int(sliding_window), _stream(stream)))
 
 
 def decode_split_workspace_size(num_seqs, num_q_heads, head_dim, max_seq_len) -> int:
@@ -230,7 +233,7 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 
 def pa_decode_split(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale, max_seq_len,
-                    workspace, layout="HND", stream=None):
+                    workspace, layout="HND", stream=None, sliding_window=0):
     """Split-KV paged GQA decode (512-token partitions + LSE merge) into out [B, nq, hd]."""
     nb, nkv, bs, hd = _pool_geometry(k_cache, layout)
     sb, sh, st = pool_strides(k_cache, layout)
@@ -238,15 +241,15 @@ def pa_decode_split(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale, 
     _check(load().pa_decode_split(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(block_tables), _ptr(seq_lens), B, nq, nkv, hd, bs,
                                   block_tables.shape[1], nb, sb, sh, st, float(sm_scale),
-                                  int(max_seq_len), _ptr(workspace), workspace.numel(),
-                                  _stream(stream)))
+                                  int(sliding_window), int(max_seq_len), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)))
 
 
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # PA_STATIC_SCRATCH_BYTES in include/pa.h
 
 
 def pa_decode_split_static(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale,
-                           max_seq_len, layout="HND", stream=None):
+                           max_seq_len, layout="HND", stream=None, sliding_window=0):
     """pa_decode_split with the library's fixed device scratch instead of a workspace,
     for callers that cannot allocate device memory.  Batches needing more than
     STATIC_SCRATCH_BYTES of partials are rejected; concurrent calls on one device race."""
@@ -256,26 +259,30 @@ def pa_decode_split_static(out, q, k_cache, v_cache, block_tables, seq_lens, sm_
     _check(load().pa_decode_split_static(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                          _ptr(block_tables), _ptr(seq_lens), B, nq, nkv, hd, bs,
                                          block_tables.shape[1], nb, sb, sh, st, float(sm_scale),
-                                         int(max_seq_len), _stream(stream)))
+                                         int(sliding_window), int(max_seq_len),
+                                         _stream(stream)))
 
 
 def pa_decode_partitions(q, k_cache, v_cache, block_tables, seq_lens, sm_scale, max_seq_len,
-                         workspace, layout="HND", stream=None):
+                         workspace, layout="HND", stream=None, sliding_window=0):
     """Split-KV pass 1: per-partition (m, l, o) into the workspace."""
     nb, nkv, bs, hd = _pool_geometry(k_cache, layout)
     sb, sh, st = pool_strides(k_cache, layout)
     B, nq, _ = q.shape
     _check(load().pa_decode_partitions(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                        _ptr(seq_lens), B, nq, nkv, hd, bs, block_tables.shape[1],
-                                       nb, sb, sh, st, float(sm_scale), int(max_seq_len),
-                                       _ptr(workspace), workspace.numel(), _stream(stream)))
+                                       nb, sb, sh, st, float(sm_scale), int(sliding_window),
+                                       int(max_seq_len), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)))
 
 
-def pa_decode_merge(out, seq_lens, max_seq_len, workspace, stream=None):
-    """Split-KV pass 2: log-sum-exp merge of the workspace partitions into out."""
+def pa_decode_merge(out, seq_lens, max_seq_len, workspace, stream=None, sliding_window=0):
+    """Split-KV pass 2: log-sum-exp merge of the workspace partitions into out (the
+    same sliding_window as pass 1)."""
     B, nq, hd = out.shape
     _check(load().pa_decode_merge(_ptr(out), _ptr(seq_lens), B, nq, hd, int(max_seq_len),
-                                  _ptr(workspace), workspace.numel(), _stream(stream)))
+                                  int(sliding_window), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)))
 
 
 def ragged_prefill_workspace_size(batch, total_qo_rows, num_q_heads, head_dim) -> int:
@@ -285,7 +292,7 @@ def ragged_prefill_workspace_size(batch, total_qo_rows, num_q_heads, head_dim) -
 
 def pa_ragged_prefill(o, q, k, v, qo_indptr_h, kv_indptr_h, qo_indptr_d, kv_indptr_d, sm_scale,
                       causal=True, block_tables=None, num_kv_heads=None, layout="HND",
-                      workspace=None, stream=None):
+                      workspace=None, stream=None, sliding_window=0):
     """Ragged prefill.  Contiguous mode: k, v [total_kv, nkv, hd].  Paged mode
     (block_tables given): k, v are pools and kv_indptr only carries lengths.
     qo_indptr_h / kv_indptr_h are int32 host tensors (or numpy arrays)."""
@@ -310,8 +317,8 @@ def pa_ragged_prefill(o, q, k, v, qo_indptr_h, kv_indptr_h, qo_indptr_d, kv_indp
         _ptr(o), _ptr(q), _ptr(k), _ptr(v), qh.ctypes.data_as(ctypes.c_void_p),
         kh.ctypes.data_as(ctypes.c_void_p), _ptr(qo_indptr_d), _ptr(kv_indptr_d),
         _ptr(block_tables), mb, bs, nb, sb, sh, st, batch, total_qo, total_kv, nq, nkv, hd,
-        float(sm_scale), 1 if causal else 0, _ptr(workspace), workspace.numel(),
-        _stream(stream)))
+        float(sm_scale), 1 if causal else 0, int(sliding_window), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
 
 
 def device_status(stream=None) -> int:

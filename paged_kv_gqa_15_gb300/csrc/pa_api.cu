@@ -98,7 +98,7 @@ int decode_common(pa::DecodeParams &p, void *out, const void *q, const void *k_c
                   const void *v_cache, const int32_t *block_tables, const int32_t *seq_lens,
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                   int max_blocks_per_seq, int64_t num_blocks, int64_t sb, int64_t sh, int64_t st,
-                  float sm_scale) {
+                  float sm_scale, int sliding_window) {
     if (num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs %d", num_seqs);
     int rc = check_heads(head_dim, num_q_heads, num_kv_heads);
     if (rc) return rc;
@@ -129,6 +129,7 @@ int decode_common(pa::DecodeParams &p, void *out, const void *q, const void *k_c
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.rows_contiguous = (st == head_dim) ? 1 : 0;
     p.max_seq_len = max_blocks_per_seq * 16;
+    p.window = sliding_window > 0 ? sliding_window : 0;
     return PA_OK;
 }
 
@@ -197,11 +198,13 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
               int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
-              int64_t stride_head, int64_t stride_token, float sm_scale, void *stream) {
+              int64_t stride_head, int64_t stride_token, float sm_scale, int sliding_window,
+              void *stream) {
     pa::DecodeParams p;
     int rc = decode_common(p, out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
                            num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                           num_blocks, stride_block, stride_head, stride_token, sm_scale);
+                           num_blocks, stride_block, stride_head, stride_token, sm_scale,
+                           sliding_window);
     if (rc) return rc;
     rc = status_ptr(&p.status);
     if (rc) return rc;
@@ -264,14 +267,14 @@ int pa_decode_partitions(const void *q, const void *k_cache, const void *v_cache
                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                          int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
                          int64_t stride_head, int64_t stride_token, float sm_scale,
-                         int max_seq_len, void *workspace, size_t workspace_bytes,
-                         void *stream) {
+                         int sliding_window, int max_seq_len, void *workspace,
+                         size_t workspace_bytes, void *stream) {
     pa::DecodeParams p;
     // `out` is not written by this pass; q stands in for the alignment check.
     int rc = decode_common(p, const_cast<void *>(q), q, k_cache, v_cache, block_tables,
                            seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                            max_blocks_per_seq, num_blocks, stride_block, stride_head,
-                           stride_token, sm_scale);
+                           stride_token, sm_scale, sliding_window);
     if (rc) return rc;
     p.out = nullptr;
     rc = split_setup(p, num_seqs, num_q_heads, head_dim, max_blocks_per_seq, max_seq_len,
@@ -286,7 +289,7 @@ int pa_decode_partitions(const void *q, const void *k_cache, const void *v_cache
 }
 
 int pa_decode_merge(void *out, const int32_t *seq_lens, int num_seqs, int num_q_heads,
-                    int head_dim, int max_seq_len, const void *workspace,
+                    int head_dim, int max_seq_len, int sliding_window, const void *workspace,
                     size_t workspace_bytes, void *stream) {
     if (num_seqs < 0 || num_q_heads <= 0)
         return fail(PA_ERR_INVALID, "num_seqs %d, num_q_heads %d", num_seqs, num_q_heads);
@@ -300,6 +303,7 @@ int pa_decode_merge(void *out, const int32_t *seq_lens, int num_seqs, int num_q_
     p.seq_lens = seq_lens;
     p.num_seqs = num_seqs;
     p.num_q_heads = num_q_heads;
+    p.window = sliding_window > 0 ? sliding_window : 0;
     int rc = split_setup(p, num_seqs, num_q_heads, head_dim, 0, max_seq_len, workspace,
                          workspace_bytes);
     if (rc) return rc;
@@ -316,11 +320,13 @@ int pa_decode_split(void *out, const void *q, const void *k_cache, const void *v
                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                     int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
                     int64_t stride_head, int64_t stride_token, float sm_scale,
-                    int max_seq_len, void *workspace, size_t workspace_bytes, void *stream) {
+                    int sliding_window, int max_seq_len, void *workspace,
+                    size_t workspace_bytes, void *stream) {
     pa::DecodeParams p;
     int rc = decode_common(p, out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
                            num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                           num_blocks, stride_block, stride_head, stride_token, sm_scale);
+                           num_blocks, stride_block, stride_head, stride_token, sm_scale,
+                           sliding_window);
     if (rc) return rc;
     rc = split_setup(p, num_seqs, num_q_heads, head_dim, max_blocks_per_seq, max_seq_len,
                      workspace, workspace_bytes);
@@ -354,7 +360,8 @@ int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
                       int64_t num_blocks, int64_t stride_block, int64_t stride_head,
                       int64_t stride_token, int batch, int total_qo_rows, int total_kv_rows,
                       int num_q_heads, int num_kv_heads, int head_dim, float sm_scale,
-                      int causal, void *workspace, size_t workspace_bytes, void *stream) {
+                      int causal, int sliding_window, void *workspace, size_t workspace_bytes,
+                      void *stream) {
     if (batch < 0 || total_qo_rows < 0 || total_kv_rows < 0)
         return fail(PA_ERR_INVALID, "negative size (batch %d, qo %d, kv %d)", batch,
                     total_qo_rows, total_kv_rows);
@@ -421,6 +428,7 @@ int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
     p.max_blocks = paged ? max_blocks_per_seq : 0;
     p.n_tiles = static_cast<int>(n_tiles);
     p.causal = causal ? 1 : 0;
+    p.window = sliding_window > 0 ? sliding_window : 0;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     rc = status_ptr(&p.status);
     if (rc) return rc;

@@ -24,6 +24,9 @@
 //    16-byte shared load per thread per page.  Between 512-token chunks of the
 //    single-pass kernel the running (m, l, acc) are rescaled (online softmax).
 //  * All waits are bounded; bad block ids are never dereferenced.
+//  * Sliding window (keys j >= L - window): chunks wholly before the window are
+//    skipped, and in the chunk holding L - window the pages wholly before it are
+//    neither looked up nor loaded; the earlier rows of its first page are masked.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -126,6 +129,20 @@ __device__ __forceinline__ bool decode_item(const DecodeParams &p, const int *pr
     }
 }
 
+// The chunk range [ch_begin, ch_end) of an item of a sequence of L tokens whose window
+// starts at token ws: a persistent split item's index counts from the window's first
+// partition, a single-pass item starts there, and no range runs past the last chunk.
+template <int MODE>
+__device__ __forceinline__ void item_chunks(int L, int ws, int &ch_begin, int &ch_end) {
+    if constexpr (MODE == kSplitPersistent) {
+        ch_begin += ws / kPartition;
+        ch_end = ch_begin + 1;
+    } else if constexpr (MODE == kSingle) {
+        ch_begin = ws / kPartition;
+    }
+    ch_end = min(ch_end, (L + kPartition - 1) / kPartition);
+}
+
 // Effective length of sequence b (negative -> 0, clamped to the table / max_seq_len).
 template <int MODE>
 __device__ __forceinline__ int seq_len_clamped(const DecodeParams &p, int b, bool flag) {
@@ -171,7 +188,7 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
         // prefix over sequences of their partition counts (compact item list)
         for (int b = threadIdx.x; b < p.num_seqs; b += C::NT) {
             const int L = seq_len_clamped<MODE>(p, b, blockIdx.x == 0);
-            pref[b + 1] = (L + kPartition - 1) / kPartition;
+            pref[b + 1] = (L + kPartition - 1) / kPartition - window_start(L, p.window) / kPartition;
         }
         if (threadIdx.x == 0) pref[0] = 0;
         __syncthreads();
@@ -195,6 +212,7 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
     } else if constexpr (MODE == kSplitDirect) {
         const int L = seq_len_clamped<MODE>(p, blockIdx.z, blockIdx.x == 0 && threadIdx.x == 0);
         if (static_cast<int>(blockIdx.x) * kPartition >= L) return;  // partition past the end
+        if (static_cast<int>(blockIdx.x) < window_start(L, p.window) / kPartition) return;
     } else {
         seq_len_clamped<MODE>(p, blockIdx.z, threadIdx.x == 0);  // flags an over-long seq_len
     }
@@ -229,7 +247,8 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
         for (int k = 0; !stop && decode_item<MODE>(p, pref, total, k, b, kh, ch_begin, ch_end);
              ++k) {
             const int L = seq_len_clamped<MODE>(p, b, false);
-            ch_end = min(ch_end, (L + kPartition - 1) / kPartition);
+            const int ws = window_start(L, p.window);
+            item_chunks<MODE>(L, ws, ch_begin, ch_end);
             // stage 1 of an item: its query group (G heads x HD, contiguous)
             {
                 const int s = claim();
@@ -248,14 +267,16 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
             for (int ch = ch_begin; ch < ch_end && !stop; ++ch) {
                 const int t0 = ch * kPartition;
                 const int np = (min(kPartition, L - t0) + kBlockSize - 1) / kBlockSize;
-                const int my_page = lane < np ? bt_row[t0 / kBlockSize + lane] : -1;
-                const bool my_ok = lane < np && my_page >= 0 && my_page < p.num_blocks;
-                if (__any_sync(kFull, lane < np && !my_ok) && lane == 0)
+                const int pg_lo = max(0, ws - t0) / kBlockSize;   // first page in the window
+                const bool mine = lane >= pg_lo && lane < np;
+                const int my_page = mine ? bt_row[t0 / kBlockSize + lane] : -1;
+                const bool my_ok = mine && my_page >= 0 && my_page < p.num_blocks;
+                if (__any_sync(kFull, mine && !my_ok) && lane == 0)
                     atomicOr(p.status, kStatusBounds);
                 for (int kv = 0; kv < 2 && !stop; ++kv) {
                     const __nv_bfloat16 *base =
                         static_cast<const __nv_bfloat16 *>(kv ? p.v_cache : p.k_cache);
-                    for (int pg0 = 0; pg0 < np; pg0 += C::SP) {
+                    for (int pg0 = pg_lo; pg0 < np; pg0 += C::SP) {
                         const int s = claim();
                         if (s < 0) break;
                         const int npg = min(C::SP, np - pg0);
@@ -312,7 +333,8 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
     int b, kh, ch_begin, ch_end;
     for (int k = 0; !aborted && decode_item<MODE>(p, pref, total, k, b, kh, ch_begin, ch_end); ++k) {
         const int L = seq_len_clamped<MODE>(p, b, false);
-        ch_end = min(ch_end, (L + kPartition - 1) / kPartition);
+        const int ws = window_start(L, p.window);
+        item_chunks<MODE>(L, ws, ch_begin, ch_end);
 
         // ---- the item's query group: Q x scale (heads in this lane's order) in registers ----
         float2 q2[G][4];
@@ -351,9 +373,12 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
             const int t0 = ch * kPartition;
             const int n_tok = min(kPartition, L - t0);
             const int np = (n_tok + kBlockSize - 1) / kBlockSize;
+            const int t_lo = max(0, ws - t0);              // first token in the window
+            const int pg_lo = t_lo / kBlockSize;           // pages before it are not loaded
+            const int t_first = pg_lo * kBlockSize;
 
             // ---- K pages, one 4-page stage at a time: scaled scores (log2 units) into sc ----
-            for (int pg0 = 0; pg0 < np; pg0 += C::SP) {
+            for (int pg0 = pg_lo; pg0 < np; pg0 += C::SP) {
                 const int npg = min(C::SP, np - pg0);
                 const int s = it % C::S;
                 if (!mbar_wait(&full[s], (it / C::S) & 1u, p.status, abort_flag)) aborted = true;
@@ -390,7 +415,7 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
                     const int u = idx >> C::LOG_G, g = idx & (G - 1);
                     if (u < npg) {
                         const int tok = (pg0 + u) * kBlockSize + r;
-                        const bool valid = tok < n_tok && ((okbits >> u) & 1u);
+                        const bool valid = tok < n_tok && tok >= t_lo && ((okbits >> u) & 1u);
                         sc[tok * G + g] = valid ? part[j] : -INFINITY;
                     }
                 }
@@ -401,7 +426,7 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
             float cm[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) cm[g] = -INFINITY;
-            for (int t = tid; t < n_tok; t += C::NC) {
+            for (int t = t_first + tid; t < n_tok; t += C::NC) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) cm[g] = fmaxf(cm[g], sc[t * G + g]);
             }
@@ -428,7 +453,7 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
             float ls[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) ls[g] = 0.f;
-            for (int t = tid; t < n_tok; t += C::NC) {
+            for (int t = t_first + tid; t < n_tok; t += C::NC) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const float sv = sc[t * G + g];
@@ -466,7 +491,7 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
             }
 
             // ---- V pages, one 4-page stage at a time: acc += p * V ----
-            for (int pg0 = 0; pg0 < np; pg0 += C::SP) {
+            for (int pg0 = pg_lo; pg0 < np; pg0 += C::SP) {
                 const int s = it % C::S;
                 if (!mbar_wait(&full[s], (it / C::S) & 1u, p.status, abort_flag)) aborted = true;
                 const uint32_t okbits = aborted ? 0u : static_cast<uint32_t>(stage_ok[s]);
@@ -476,7 +501,7 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G>::NT, (HD == 256 || G == 8) ? 
 #pragma unroll
                 for (int u = 0; u < C::SP; ++u) {
                     const int tok = (pg0 + u) * kBlockSize + r;
-                    const bool use = ((okbits >> u) & 1u) && tok < n_tok;
+                    const bool use = ((okbits >> u) & 1u) && tok < n_tok && tok >= t_lo;
                     raw[u] = use ? *reinterpret_cast<const uint4 *>(st + u * C::PAGE_BYTES)
                                  : make_uint4(0u, 0u, 0u, 0u);
                     if constexpr (G == 4) {
@@ -580,8 +605,10 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Deco
     int L = p.seq_lens[b];
     if (L < 0) L = 0;
     if (L > p.max_seq_len) L = p.max_seq_len;
-    const int np = (L + kPartition - 1) / kPartition;
-    const int64_t row0 = (static_cast<int64_t>(b) * nq + h) * p.max_parts;
+    // the partitions from the window's first one (all of them without a window)
+    const int p0 = window_start(L, p.window) / kPartition;
+    const int np = (L + kPartition - 1) / kPartition - p0;
+    const int64_t row0 = (static_cast<int64_t>(b) * nq + h) * p.max_parts + p0;
     const float *pm = p.part_m + row0;
     const float *pl = p.part_l + row0;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -646,8 +673,9 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(const __grid_constant__
     int L = p.seq_lens[b];
     if (L < 0) L = 0;
     if (L > p.max_seq_len) L = p.max_seq_len;
-    const int np = (L + kPartition - 1) / kPartition;   // <= 32 for this kernel
-    const int64_t row0 = (static_cast<int64_t>(b) * nq + h) * p.max_parts;
+    const int p0 = window_start(L, p.window) / kPartition;
+    const int np = (L + kPartition - 1) / kPartition - p0;   // <= 32 for this kernel
+    const int64_t row0 = (static_cast<int64_t>(b) * nq + h) * p.max_parts + p0;
     const float mi = lane < np ? p.part_m[row0 + lane] : -INFINITY;
     float M = mi;
 #pragma unroll
@@ -734,7 +762,8 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t stream) {
     }
     dim3 grid;
     if (MODE == kSplitPersistent) {
-        const long long slots = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.max_parts;
+        const long long slots = static_cast<long long>(p.num_seqs) * p.num_kv_heads *
+                                active_partitions_cap(p.max_parts, p.window);
         long long n = static_cast<long long>(sm_count()) * (blocks_per_sm > 0 ? blocks_per_sm : 1);
         if (slots < n) n = slots;
         grid = dim3(static_cast<unsigned>(n > 0 ? n : 1), 1, 1);
@@ -778,7 +807,7 @@ cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaS
 
 cudaError_t launch_merge(const DecodeParams &p, int head_dim, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
-    if (p.max_parts <= 32) {   // one warp per (sequence, head)
+    if (active_partitions_cap(p.max_parts, p.window) <= 32) {   // one warp per (sequence, head)
         const int64_t warps = static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
         const dim3 wgrid(static_cast<unsigned>((warps + 7) / 8));
         switch (head_dim) {

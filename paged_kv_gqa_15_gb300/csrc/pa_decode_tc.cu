@@ -27,6 +27,10 @@
 //    separate rings, each filled by its own producer warp: an item's V tiles wait
 //    in their ring for its softmax while the next item's K tiles (and score MMAs)
 //    go ahead, so HBM keeps streaming through the softmax.  Every wait is bounded.
+//  * Sliding window (keys j >= L - window): the item list holds only partitions
+//    that reach into the window; in the one holding L - window, tiles wholly before
+//    it are skipped, pages before it inside its first tile are read as zero boxes
+//    (their table entries are never looked up), and its earlier rows are masked.
 #include <cuda.h>
 
 #include "pa_device.cuh"
@@ -73,6 +77,8 @@ struct DecodeTcParams {
     DecodeParams d;
 };
 
+__device__ __forceinline__ int tc_seq_len(const DecodeParams &p, int b, bool flag);
+
 // The k-th item of this CTA: (b, kh, partition); false when there is none.
 __device__ __forceinline__ bool tc_item(const DecodeParams &p, const int *pref, long long total,
                                         int k, int &b, int &kh, int &part) {
@@ -87,7 +93,26 @@ __device__ __forceinline__ bool tc_item(const DecodeParams &p, const int *pref, 
     }
     b = lo;
     part = j - pref[b];
+    if (p.window > 0)   // items count from the partition holding the window's first key
+        part += window_start(tc_seq_len(p, b, false), p.window) / kPartition;
     return true;
+}
+
+// The part of item (b, part) inside the sequence and its window: tokens
+// [t0 + t_lo, t0 + n_tok) of the partition starting at t0, in tiles i_lo .. n_tiles-1.
+struct TcSpan {
+    int t0, n_tok, t_lo, i_lo, n_tiles;
+};
+
+__device__ __forceinline__ TcSpan tc_span(const DecodeParams &p, int b, int part) {
+    const int L = tc_seq_len(p, b, false);
+    TcSpan s;
+    s.t0 = part * kPartition;
+    s.n_tok = min(kPartition, L - s.t0);
+    s.t_lo = max(0, window_start(L, p.window) - s.t0);
+    s.i_lo = s.t_lo / kTok;
+    s.n_tiles = (s.n_tok + kTok - 1) / kTok;
+    return s;
 }
 
 __device__ __forceinline__ int tc_seq_len(const DecodeParams &p, int b, bool flag) {
@@ -140,8 +165,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // prefix over sequences of their partition counts (the compact item list)
-    for (int b = threadIdx.x; b < p.num_seqs; b += kThreadsTc)
-        pref[b + 1] = (tc_seq_len(p, b, blockIdx.x == 0) + kPartition - 1) / kPartition;
+    for (int b = threadIdx.x; b < p.num_seqs; b += kThreadsTc) {
+        const int L = tc_seq_len(p, b, blockIdx.x == 0);
+        pref[b + 1] = (L + kPartition - 1) / kPartition - window_start(L, p.window) / kPartition;
+    }
     if (threadIdx.x == 0) pref[0] = 0;
     // rows g .. 15 of the Q^T and P buffers stay zero (padding of the MMA's N)
     for (uint32_t i = threadIdx.x; i < (2 * kQBytes + kPBytes) / 16; i += kThreadsTc)
@@ -211,10 +238,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         int stop = 0;
         int b, kh, part;
         for (int e = 0; !stop && tc_item(p, pref, total, e, b, kh, part); ++e) {
-            const int L = tc_seq_len(p, b, false);
-            const int t0 = part * kPartition;
-            const int n_tok = min(kPartition, L - t0);
-            const int n_tiles = (n_tok + kTok - 1) / kTok;
+            const TcSpan sp = tc_span(p, b, part);
+            const int t0 = sp.t0;
+            const int n_tiles = sp.n_tiles;
             if (!is_v) {
                 const int qb = e & 1;
                 if (lane == 0) {
@@ -229,16 +255,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     tma_load_3d(smem + kOffQ + qb * kQBytes + lane * kSmallChunk, &prm.tm_q,
                                 lane * 64, kh * G, b, &q_full[qb]);
             }
-            // page ids of the partition, one per lane (past the sequence or bad: an
-            // out-of-range box that reads zeros); the V producer flags nothing twice
-            const int np = (n_tok + kBlockSize - 1) / kBlockSize;
-            int page = lane < np ? p.block_tables[static_cast<int64_t>(b) * p.max_blocks +
-                                                  t0 / kBlockSize + lane]
-                                 : -2;
+            // page ids of the partition, one per lane (past the sequence, before the
+            // window or bad: an out-of-range box that reads zeros); the V producer flags
+            // nothing twice
+            const int np = (sp.n_tok + kBlockSize - 1) / kBlockSize;
+            const int pg_lo = sp.t_lo / kBlockSize;
+            int page = (lane >= pg_lo && lane < np)
+                           ? p.block_tables[static_cast<int64_t>(b) * p.max_blocks +
+                                            t0 / kBlockSize + lane]
+                           : -2;
             const bool bad = page != -2 && (page < 0 || page >= p.num_blocks);
             if (!is_v && __any_sync(kFullMaskTc, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
             if (page == -2 || bad) page = static_cast<int>(p.num_blocks);
-            for (int i = 0; i < n_tiles; ++i, ++it) {
+            for (int i = sp.i_lo; i < n_tiles; ++i, ++it) {
                 const int s = it % NS;
                 if (lane == 0) {
                     if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1u, p.status, abort_flag))
@@ -275,15 +304,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const uint64_t p_desc = smem_desc_sw128(smem_addr(smem + kOffP), 16, 1024);
             uint32_t kit = 0, vit = 0;   // K / V ring uses
             bool ok = true;
-            // The partition's token count and tile count of item e.
-            auto item_tiles = [&](int e, int &n_tok) -> int {
+            // The token span of item e; n_tiles = -1 when there is none.
+            auto item_span = [&](int e) -> TcSpan {
                 int b, kh, part;
-                if (!tc_item(p, pref, total, e, b, kh, part)) return -1;
-                n_tok = min(kPartition, tc_seq_len(p, b, false) - part * kPartition);
-                return (n_tok + kTok - 1) / kTok;
+                if (!tc_item(p, pref, total, e, b, kh, part)) {
+                    TcSpan none = {};
+                    none.n_tiles = -1;
+                    return none;
+                }
+                return tc_span(p, b, part);
             };
             // S^T = K Q^T for every tile of item e, into S buffer e % 2
-            auto issue_s = [&](int e, int n_tiles) {
+            auto issue_s = [&](int e, const TcSpan &sp) {
+                const int n_tiles = sp.n_tiles;
                 const int x = e & 1;
                 const uint32_t use = e >> 1;
                 ok = ok && mbar_wait(&q_full[x], use & 1, p.status, abort_flag);
@@ -292,7 +325,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 if (!ok) return;
                 tc_fence_after_sync();
                 const uint64_t qd = q_desc + ((x * kQBytes) >> 4);
-                for (int i = 0; i < n_tiles && ok; ++i, ++kit) {
+                for (int i = sp.i_lo; i < n_tiles && ok; ++i, ++kit) {
                     const int s = kit % kKStages;
                     ok = mbar_wait(&k_full[s], (kit / kKStages) & 1, p.status, abort_flag);
                     if (!ok) return;
@@ -314,31 +347,41 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             };
             // O^T = V^T P over the tiles of item e, once P is in shared memory and the
             // epilogue of item e - 2 has read O buffer e % 2
-            auto issue_pv = [&](int e, int n_tiles, int n_tok) {
+            auto issue_pv = [&](int e, const TcSpan &sp) {
+                const int n_tiles = sp.n_tiles, n_tok = sp.n_tok;
                 const int x = e & 1;
                 const uint32_t use = e >> 1;
                 ok = ok && mbar_wait(&p_full[x], use & 1, p.status, abort_flag);
                 if (ok && e >= 2) ok = mbar_wait(&o_free[x], (use - 1) & 1, p.status, abort_flag);
                 if (!ok) return;
                 tc_fence_after_sync();
-                for (int i = 0; i < n_tiles && ok; ++i, ++vit) {
+                for (int i = sp.i_lo; i < n_tiles && ok; ++i, ++vit) {
                     const int s = vit % kVStages;
                     ok = mbar_wait(&v_full[s], (vit / kVStages) & 1, p.status, abort_flag);
                     if (!ok) return;
                     tc_fence_after_sync();
+                    // rows outside [t_lo, n_tok) in a page that was loaded hold whatever
+                    // the pool held (whole pages outside read as zeros); P is 0 there,
+                    // but 0 x NaN would poison O, so zero those V rows: past the sequence
+                    // in its last page, and before the window in its first page
                     const int stale = n_tok - i * kTok;   // first row past the tokens
-                    if (stale < kTok) {
-                        // rows past the sequence in its last page hold whatever the pool
-                        // held (whole pages past it read as zeros); P is 0 there, but
-                        // 0 x NaN would poison O, so zero those V rows
+                    const int head = sp.t_lo - i * kTok;  // first row in the window
+                    if (stale < kTok || (head > 0 && head < kTok)) {
                         uint8_t *vt = smem + kOffV + s * kTileBytes;
-                        const int row_end = min(kTok, (stale + kBlockSize - 1) / kBlockSize * kBlockSize);
-                        for (int c = 0; c < 2; ++c)
-                            for (int row = stale; row < row_end; ++row) {
+                        const int tail_end = min(kTok, (stale + kBlockSize - 1) / kBlockSize * kBlockSize);
+                        const int head_begin = max(0, head / kBlockSize * kBlockSize);
+                        for (int c = 0; c < 2; ++c) {
+                            for (int row = stale; row < tail_end; ++row) {
                                 uint4 *dst = reinterpret_cast<uint4 *>(vt + c * kTileChunk + row * 128);
 #pragma unroll
                                 for (int q = 0; q < 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
                             }
+                            for (int row = head_begin; row < head && row < kTok; ++row) {
+                                uint4 *dst = reinterpret_cast<uint4 *>(vt + c * kTileChunk + row * 128);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+                            }
+                        }
                         fence_proxy_async_smem();
                     }
                     const uint64_t vd = ring_v + ((s * kTileBytes) >> 4);
@@ -347,7 +390,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     for (int kk = 0; kk < kTok / 16; ++kk)
                         mma_bf16_ss(tmem + kTmO + x * kN, vd + ((kk * 16 * 128) >> 4),
                                     pd + (((kk / 4) * kSmallChunk + (kk % 4) * 32) >> 4), idesc_o,
-                                    (i > 0 || kk > 0) ? 1u : 0u);
+                                    (i > sp.i_lo || kk > 0) ? 1u : 0u);
                     tc_commit(&v_empty[s]);
                 }
                 if (!ok) return;
@@ -356,16 +399,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             // Software pipeline: the scores of item e + 1 are issued before the P.V of
             // item e, so they run while item e's softmax does and the K ring keeps
             // draining (the S buffers alternate; s_free guards their reuse).
-            int n_tok = 0;
-            int n_tiles = item_tiles(0, n_tok);
-            if (n_tiles > 0) issue_s(0, n_tiles);
-            for (int e = 0; ok && n_tiles > 0; ++e) {
-                int n_tok_next = 0;
-                const int n_tiles_next = item_tiles(e + 1, n_tok_next);
-                if (n_tiles_next > 0) issue_s(e + 1, n_tiles_next);
-                issue_pv(e, n_tiles, n_tok);
-                n_tiles = n_tiles_next;
-                n_tok = n_tok_next;
+            TcSpan cur = item_span(0);
+            if (cur.n_tiles > 0) issue_s(0, cur);
+            for (int e = 0; ok && cur.n_tiles > 0; ++e) {
+                const TcSpan next = item_span(e + 1);
+                if (next.n_tiles > 0) issue_s(e + 1, next);
+                issue_pv(e, cur);
+                cur = next;
             }
             tc_commit(drain);   // never release TMEM / smem with MMAs in flight
             const uint64_t t0 = global_timer_ns();
@@ -390,9 +430,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         bool ok = true;
         int b, kh, part;
         for (int e = 0; tc_item(p, pref, total, e, b, kh, part); ++e) {
-            const int L = tc_seq_len(p, b, false);
-            const int t0 = part * kPartition;
-            const int n_tok = min(kPartition, L - t0);
+            const TcSpan sp = tc_span(p, b, part);
+            const int n_tok = sp.n_tok;
             const int x = e & 1;
             const uint32_t use = e >> 1;
             // scores of this thread's token in each tile, in log2 units
@@ -402,7 +441,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (got) tc_fence_after_sync();
 #pragma unroll
             for (int i = 0; i < kTiles; ++i) {
-                const bool tile = got && i * kTok < n_tok;
+                const bool tile = got && i >= sp.i_lo && i * kTok < n_tok;
                 uint32_t v[8];
                 if (tile) {
                     tmem_load_8(tmem + t_lane + kTmS + x * 64 + i * kN, v);
@@ -410,7 +449,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
                     for (int g = 0; g < 8; ++g) v[g] = 0u;
                 }
-                const bool valid = tile && i * kTok + row < n_tok;
+                const bool valid = tile && i * kTok + row < n_tok && i * kTok + row >= sp.t_lo;
 #pragma unroll
                 for (int g = 0; g < G; ++g)
                     sc[i][g] = valid ? __uint_as_float(v[g]) * scale : -INFINITY;
@@ -545,7 +584,8 @@ cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
     static int sms = 0;
     if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 152;
-    const long long slots = static_cast<long long>(p.num_seqs) * p.num_kv_heads * p.max_parts;
+    const long long slots = static_cast<long long>(p.num_seqs) * p.num_kv_heads *
+                            active_partitions_cap(p.max_parts, p.window);
     long long n = sms;
     if (slots < n) n = slots;
     cudaLaunchConfig_t cfg = {};

@@ -17,6 +17,21 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Sliding window of `window` keys ("paged_attn.py", forward_prefix's sliding_window):
+// a query at position pos sees keys j > pos - window.  First visible key of the query
+// at position L - 1 (decode); 0 when there is no window (window <= 0).
+__device__ __forceinline__ int window_start(int L, int window) {
+    return (window > 0 && L > window) ? L - window : 0;
+}
+
+// Partitions a split-KV call with this window can have per sequence (the partitions
+// from the one holding key L - window to the last), capped at max_parts.
+__host__ __device__ __forceinline__ int active_partitions_cap(int max_parts, int window) {
+    if (window <= 0) return max_parts;
+    const int cap = (window - 1) / kPartition + 2;
+    return cap < max_parts ? cap : max_parts;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

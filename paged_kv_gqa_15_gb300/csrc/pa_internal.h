@@ -33,6 +33,7 @@ struct DecodeParams {
     int max_seq_len;              // split: clamp for seq_lens
     float scale_log2;             // sm_scale * log2(e)
     int rows_contiguous;          // s_token == head_dim: one bulk copy per page
+    int window;                   // sliding window in keys (> 0), or 0 for none
     int *status;
 };
 
@@ -47,6 +48,7 @@ struct PrefillParams {
     int *item_counter;                     // next unclaimed work item (zeroed per call)
     int64_t num_blocks;
     int batch, nq, nkv, max_blocks, n_tiles, causal;
+    int window;                            // sliding window in keys (> 0), or 0 for none
     float scale_log2;
     int *status;
 };

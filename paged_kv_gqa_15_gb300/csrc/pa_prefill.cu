@@ -86,17 +86,19 @@ struct RowSoftmax {
     float m, l;
 };
 
-// Masks columns >= lim of a key tile (when need_mask: the visible keys of a row are a
-// prefix of the tile), takes the row max and makes the lazy-rescale decision: m moves
-// only when the max grows by more than 2^8.  Returns whether it moves; m_use is the
-// max the tile's P is then taken against and corr the factor O and l are scaled by.
+// Masks the columns outside [lo, lim) of a key tile (when need_mask: the visible keys
+// of a row are a run of the tile's columns -- lo > 0 only under a sliding window),
+// takes the row max and makes the lazy-rescale decision: m moves only when the max
+// grows by more than 2^8.  Returns whether it moves; m_use is the max the tile's P is
+// then taken against and corr the factor O and l are scaled by.
 template <int BN>
-__device__ __forceinline__ bool tile_max(uint32_t (&sr)[BN], bool need_mask, int lim, float scale,
-                                         const RowSoftmax &rs, float &m_use, float &corr) {
+__device__ __forceinline__ bool tile_max(uint32_t (&sr)[BN], bool need_mask, int lo, int lim,
+                                         float scale, const RowSoftmax &rs, float &m_use,
+                                         float &corr) {
     if (need_mask) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
-            if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+            if (c >= lim || c < lo) sr[c] = __float_as_uint(-INFINITY);
     }
     // row max of the raw scores (sm_scale > 0, so it scales to the max of s * scale);
     // eight partial maxima, each taking two new columns per three-input max, keep the
@@ -182,17 +184,28 @@ struct PrefillCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
-// Number of key tiles a query tile needs (its work), bottom-right causal.
-__device__ __forceinline__ int key_tiles(int q0, int qo_len, int kv_len, int causal, int bn) {
+// First key any row of the query tile at q0 sees under a sliding window of `window`
+// keys (row i at position i + kv_len - qo_len sees keys j > position - window); 0
+// without a window.
+__device__ __forceinline__ int window_first_key(int q0, int qo_len, int kv_len, int window) {
+    if (window <= 0) return 0;
+    return max(0, q0 + (kv_len - qo_len) - window + 1);
+}
+
+// Number of key tiles a query tile needs (its work): bottom-right causal, from the
+// tile holding the window's first key.
+__device__ __forceinline__ int key_tiles(int q0, int qo_len, int kv_len, int causal, int window,
+                                         int bn) {
     int kv_end = kv_len;
     if (causal) kv_end = min(kv_len, max(0, q0 + kBM + (kv_len - qo_len)));
-    return (kv_end + bn - 1) / bn;
+    const int n = (kv_end + bn - 1) / bn - window_first_key(q0, qo_len, kv_len, window) / bn;
+    return n > 0 ? n : 0;
 }
 
 // Heaviest-first order of the (request, query tile) work items.
 __global__ void __launch_bounds__(1024) prefill_schedule_kernel(
-    const int32_t *qo_indptr, const int32_t *kv_indptr, int batch, int causal, int bn,
-    int n_tiles, int2 *tiles, int *item_counter, int *status) {
+    const int32_t *qo_indptr, const int32_t *kv_indptr, int batch, int causal, int window,
+    int bn, int n_tiles, int2 *tiles, int *item_counter, int *status) {
     __shared__ int hist[kSchedBuckets];
     __shared__ int total_sh;
     const int tid = threadIdx.x;
@@ -207,7 +220,8 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(
         const int kv_len = kv_indptr[r + 1] - kv_indptr[r];
         const int nt = (max(qo_len, 0) + kBM - 1) / kBM;
         for (int t = 0; t < nt; ++t) {
-            const int key = min(key_tiles(t * kBM, qo_len, kv_len, causal, bn), kSchedBuckets - 1);
+            const int key =
+                min(key_tiles(t * kBM, qo_len, kv_len, causal, window, bn), kSchedBuckets - 1);
             atomicAdd(&hist[kSchedBuckets - 1 - key], 1);
         }
         atomicAdd(&total_sh, nt);
@@ -237,7 +251,8 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(
         const int kv_len = kv_indptr[r + 1] - kv_indptr[r];
         const int nt = (max(qo_len, 0) + kBM - 1) / kBM;
         for (int t = 0; t < nt; ++t) {
-            const int key = min(key_tiles(t * kBM, qo_len, kv_len, causal, bn), kSchedBuckets - 1);
+            const int key =
+                min(key_tiles(t * kBM, qo_len, kv_len, causal, window, bn), kSchedBuckets - 1);
             const int pos = atomicAdd(&hist[kSchedBuckets - 1 - key], 1);
             if (pos < n_tiles) tiles[pos] = make_int2(r, t);
         }
@@ -250,6 +265,8 @@ struct PrefillItem {
     int r, h, qo_start, qo_len, kv_start, kv_len, q0;
     int n_kv;   // key tiles; -1 marks the end of the work list
     int work;   // the tile holds query rows (it is written, possibly with zeros)
+    int kv_lo;  // first key any row of the tile sees (> 0 only under a sliding window)
+    int j0;     // first key tile, kv_lo / BN: the item's key tiles are j0 .. j0 + n_kv - 1
 };
 
 template <bool PAGED, int BN>
@@ -269,9 +286,14 @@ __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, long
     }
     w.q0 = ok ? tile.y * kBM : 0;
     w.work = ok && w.q0 < w.qo_len;
-    w.n_kv = w.work ? key_tiles(w.q0, w.qo_len, w.kv_len, p.causal, BN) : 0;
+    w.n_kv = w.work ? key_tiles(w.q0, w.qo_len, w.kv_len, p.causal, p.window, BN) : 0;
+    w.kv_lo = w.work ? window_first_key(w.q0, w.qo_len, w.kv_len, p.window) : 0;
+    w.j0 = w.kv_lo / BN;
     return w;
 }
+
+// The item queue (4 entries) follows the 40 barrier words in the 512 bytes at OFF_BAR.
+static_assert(40 * 8 + 4 * sizeof(PrefillItem) <= 512, "item queue fits its shared memory");
 
 __device__ __forceinline__ PrefillItem end_item() {
     PrefillItem w{};
@@ -392,10 +414,11 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             return stop ? end_item() : item_q[slot];
         };
         // Block-table entry of page `lane` of key tile j (lanes < BN / 16); -2 for
-        // lanes and pages past the sequence.  Issued a tile early, checked at use.
-        auto page_raw = [&](int r, int j, int pages_seq) -> int {
+        // lanes and pages past the sequence or wholly before the window (those entries
+        // are never looked up).  Issued a tile early, checked at use.
+        auto page_raw = [&](int r, int j, int pages_seq, int page_lo) -> int {
             const int pidx = j * (BN / kBlockSize) + lane;
-            if (lane >= BN / kBlockSize || pidx >= pages_seq) return -2;
+            if (lane >= BN / kBlockSize || pidx >= pages_seq || pidx < page_lo) return -2;
             return p.block_tables[static_cast<int64_t>(r) * p.max_blocks + pidx];
         };
         // Bad ids are flagged; they and pages past the sequence become num_blocks, an
@@ -426,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 tma_load_3d(smem + C::OFF_Q + lane * kBM * 128, &p.tm_q, lane * 64, w.h,
                             w.qo_start + w.q0, q_full);
             const int pages_seq = (w.kv_len + kBlockSize - 1) / kBlockSize;
+            const int page_lo = w.kv_lo / kBlockSize;
             // Loads key tile j (kv = 0) or value tile j (kv = 1) of this item into its
             // ring stage; g is the tile's index over all items of this CTA.
             auto load_tile = [&](int kv, int j, uint32_t g, int page) {
@@ -456,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 } else {
                     if (lane < C::QCH)
                         tma_load_3d(dst + lane * C::KV_CHUNK, tm, lane * 64, kh,
-                                    w.kv_start + j * BN, full);
+                                    w.kv_start + (w.j0 + j) * BN, full);
                 }
             };
             // The MMA warp consumes K_{j+1} (for S_{j+1}) before V_j (for P_j V_j), so K
@@ -466,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             // ahead of their use.
             int pg_cur = 0, raw_next = -2;
             if constexpr (PAGED) {
-                pg_cur = page_fix(page_raw(w.r, 0, pages_seq));
-                if (w.n_kv > 1) raw_next = page_raw(w.r, 1, pages_seq);
+                pg_cur = page_fix(page_raw(w.r, w.j0, pages_seq, page_lo));
+                if (w.n_kv > 1) raw_next = page_raw(w.r, w.j0 + 1, pages_seq, page_lo);
             }
             load_tile(0, 0, kv_it, pg_cur);
             for (int j = 0; j < w.n_kv && !stop; ++j) {
@@ -475,7 +499,8 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 if (j + 1 < w.n_kv) {
                     if constexpr (PAGED) {
                         pg_next = page_fix(raw_next);
-                        if (j + 2 < w.n_kv) raw_next = page_raw(w.r, j + 2, pages_seq);
+                        if (j + 2 < w.n_kv)
+                            raw_next = page_raw(w.r, w.j0 + j + 2, pages_seq, page_lo);
                     }
                     load_tile(0, j + 1, kv_it + j + 1, pg_next);
                 }
@@ -501,8 +526,10 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 smem_desc_sw128(smem_addr(smem + C::OFF_V), C::KV_CHUNK, 1024);
             uint32_t kv_it = 0, q_it = 0, o_items = 0;
             bool ok = true;
-            // O += P_g V_g for global key tile g (tile jj of an item with kv_len keys)
-            auto issue_pv = [&](uint32_t g, int jj, int kv_len) {
+            // O += P_g V_g for global key tile g: the item's tile jj, whose first row is
+            // key j0 * BN + jj * BN; kv_rel = kv_len - j0 * BN is the key count from the
+            // item's first tile and head the first row of that tile in the window
+            auto issue_pv = [&](uint32_t g, int jj, int kv_rel, int head) {
                 if (!ok) return;
                 const int b = g & 1;          // S / P buffer
                 const int s = g % C::VS;      // V stage
@@ -513,18 +540,29 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 if (!ok) return;
                 tc_fence_after_sync();
                 if constexpr (PAGED) {
-                    // Rows past kv_len in the sequence's last page hold whatever the pool
-                    // held; P is 0 there, but 0 x NaN would still poison O, so zero them.
-                    const int first_stale = kv_len - jj * BN;
-                    if (first_stale < BN) {
+                    // Rows past kv_len in the sequence's last page, and rows before the
+                    // window in its first page, hold whatever the pool held; P is 0
+                    // there, but 0 x NaN would still poison O, so zero them.  (Whole
+                    // pages outside were read as zero boxes.)
+                    const int first_stale = kv_rel - jj * BN;
+                    const int head_end = jj == 0 ? head : 0;
+                    if (first_stale < BN || head_end > 0) {
                         uint8_t *vt = smem + C::OFF_V + s * C::KV_BYTES;
-                        for (int c = 0; c < C::QCH; ++c)
+                        const int head_begin = head_end / kBlockSize * kBlockSize;
+                        for (int c = 0; c < C::QCH; ++c) {
                             for (int row = max(first_stale, 0); row < BN; ++row) {
                                 uint4 *dst =
                                     reinterpret_cast<uint4 *>(vt + c * C::KV_CHUNK + row * 128);
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
                             }
+                            for (int row = head_begin; row < head_end; ++row) {
+                                uint4 *dst =
+                                    reinterpret_cast<uint4 *>(vt + c * C::KV_CHUNK + row * 128);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+                            }
+                        }
                         fence_proxy_async_smem();
                     }
                 }
@@ -562,9 +600,10 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                                     kd + ((c * C::KV_CHUNK + inner) >> 4), idesc_s, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(&s_full[b]);
-                    if (j >= 1) issue_pv(g - 1, j - 1, w.kv_len);
+                    if (j >= 1) issue_pv(g - 1, j - 1, w.kv_len - w.j0 * BN, w.kv_lo - w.j0 * BN);
                 }
-                issue_pv(base + w.n_kv - 1, w.n_kv - 1, w.kv_len);
+                issue_pv(base + w.n_kv - 1, w.n_kv - 1, w.kv_len - w.j0 * BN,
+                         w.kv_lo - w.j0 * BN);
                 kv_it += w.n_kv;
                 ++q_it;
                 ++o_items;
@@ -620,11 +659,16 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                         tmem_load_64(tmem + t_lane + C::TM_S + s * BN + c * 64, chunk);
                     }
                 }
-                const bool need_mask =
-                    (j + 1) * BN > w.kv_len || (p.causal && (j + 1) * BN - 1 > w.q0 + off);
-                const int lim = min(w.kv_len, p.causal ? q_pos + 1 : w.kv_len) - j * BN;
+                const int jj = w.j0 + j;               // key tile of the request
+                // under a window, row q_pos sees keys j > q_pos - window only; the tile
+                // needs the lower mask when it starts before the last row's window
+                const bool need_lo = p.window > 0 && jj * BN < w.q0 + kBM + off - p.window;
+                const bool need_mask = (jj + 1) * BN > w.kv_len ||
+                                       (p.causal && (jj + 1) * BN - 1 > w.q0 + off) || need_lo;
+                const int lim = min(w.kv_len, p.causal ? q_pos + 1 : w.kv_len) - jj * BN;
+                const int lo = p.window > 0 ? q_pos - p.window + 1 - jj * BN : 0;
                 float m_use, corr;
-                const bool grow = tile_max<BN>(sr, need_mask, lim, scale, rs, m_use, corr);
+                const bool grow = tile_max<BN>(sr, need_mask, lo, lim, scale, rs, m_use, corr);
                 if (j > 0 && __any_sync(kFullMask, grow)) {
                     // O holds P_0..P_{j-1} V: wait for the last P.V, then rescale in TMEM
                     ok = mbar_wait(&v_empty[(g - 1) % C::VS], ((g - 1) / C::VS) & 1, p.status,
@@ -763,8 +807,9 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
         if (!encode_tensor_map_bf16(&p.tm_v, L.v, 4, dims, str, box)) return cudaErrorInvalidValue;
     }
     prefill_schedule_kernel<<<1, 1024, 0, stream>>>(p.qo_indptr, p.kv_indptr, p.batch, p.causal,
-                                                    BN, p.n_tiles, const_cast<int2 *>(p.tiles),
-                                                    p.item_counter, p.status);
+                                                    p.window, BN, p.n_tiles,
+                                                    const_cast<int2 *>(p.tiles), p.item_counter,
+                                                    p.status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const void *kern = reinterpret_cast<const void *>(prefill_kernel<HD, BN, PAGED>);

@@ -110,6 +110,7 @@ class DecodeWorkload:
     new_token_write: bool = False  # write K/V of position L-1 via pa_write_cache first
     split: bool = False
     slot_mapping: Optional[np.ndarray] = None  # int64 [B] when new_token_write
+    window: int = 0               # sliding window in keys (0: none)
 
     @property
     def batch(self):
@@ -127,9 +128,16 @@ class DecodeWorkload:
     def pool_shape(self):  # HND pages
         return (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
 
+    def visible_tokens(self):
+        """Keys the queries attend to: all of each sequence, or its last `window`."""
+        lens = self.seq_lens.astype(np.int64)
+        if self.window > 0:
+            lens = np.minimum(lens, self.window)
+        return int(lens.sum())
+
     def kv_bytes(self):
         """Algorithmic decode bytes: K and V of every visible token."""
-        return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 2 * 2
+        return self.visible_tokens() * self.num_kv_heads * self.head_dim * 2 * 2
 
     def tensors(self, device="cpu"):
         """q, k_cache, v_cache (and k_new, v_new if new_token_write) as bf16 tensors."""
@@ -147,13 +155,13 @@ class DecodeWorkload:
 
 def make_decode(name, seq_lens, num_q_heads, num_kv_heads, head_dim, seed,
                 block_size=BLOCK_SIZE, num_blocks=None, new_token_write=False, split=False,
-                max_blocks=None):
+                max_blocks=None, window=0):
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, np.int32)
     bt, nb = assign_pages(seq_lens, block_size, rng, num_blocks=num_blocks,
                           max_blocks=max_blocks)
     w = DecodeWorkload(name, seq_lens, bt, nb, num_q_heads, num_kv_heads, head_dim,
-                       block_size, seed, new_token_write, split)
+                       block_size, seed, new_token_write, split, window=window)
     if new_token_write:
         w.slot_mapping = slots_for_positions(bt, np.maximum(seq_lens.astype(np.int64) - 1, 0),
                                              block_size)
@@ -178,6 +186,7 @@ class PrefillWorkload:
     chunk_write: bool = False           # paged: the new chunk's K/V go in via pa_write_cache
     chunk_slot_mapping: Optional[np.ndarray] = None  # int64 [sum qo]
     extra: dict = field(default_factory=dict)
+    window: int = 0                     # sliding window in keys (0: none)
 
     @property
     def batch(self):
@@ -204,15 +213,15 @@ class PrefillWorkload:
         return int(self.kv_lens.sum())
 
     def visible_pairs(self):
-        """Number of (query row, key) pairs left by the mask, per query head."""
+        """Number of (query row, key) pairs left by the mask, per query head: row i sits
+        at position i + kv - qo and sees keys j < kv, j <= position if causal, and
+        j > position - window under a window."""
         tot = 0
         for qo, kv in zip(self.qo_lens.astype(np.int64), self.kv_lens.astype(np.int64)):
-            if not self.causal:
-                tot += qo * kv
-                continue
-            off = kv - qo
-            i = np.arange(qo, dtype=np.int64)
-            tot += int(np.clip(i + off + 1, 0, kv).sum())
+            pos = np.arange(qo, dtype=np.int64) + (kv - qo)
+            hi = np.clip(pos + 1, 0, kv) if self.causal else np.full(qo, kv)
+            lo = np.maximum(pos - self.window + 1, 0) if self.window > 0 else np.zeros(qo, np.int64)
+            tot += int(np.clip(hi - lo, 0, None).sum())
         return int(tot)
 
     def flops(self):
@@ -240,11 +249,11 @@ class PrefillWorkload:
 
 def make_prefill(name, qo_lens, kv_lens, num_q_heads, num_kv_heads, head_dim, seed,
                  causal=True, paged=False, chunk_write=False, block_size=BLOCK_SIZE,
-                 num_blocks=None):
+                 num_blocks=None, window=0):
     qo = np.asarray(qo_lens, np.int32)
     kv = np.asarray(kv_lens, np.int32)
     w = PrefillWorkload(name, qo, kv, num_q_heads, num_kv_heads, head_dim, causal, seed,
-                        paged, block_size)
+                        paged, block_size, window=window)
     if paged:
         rng = np.random.default_rng(seed)
         w.block_tables, w.num_blocks = assign_pages(kv, block_size, rng, num_blocks=num_blocks)
@@ -301,10 +310,30 @@ def chunked_paged_prefill():
                         seed=1004, paged=True, chunk_write=True)
 
 
+def window_decode():
+    """Sliding-window decode shaped like Mistral-7B (32 q / 8 kv heads, hd 128, a
+    4096-key window): batch 32, seq_lens U[8192, 32768], split-KV."""
+    rng = np.random.default_rng(1005)
+    lens = rng.integers(8192, 32768, size=32, endpoint=True)
+    return make_decode("window_decode_b32_h32kv8_d128_w4096", lens, 32, 8, 128, seed=1005,
+                       split=True, window=4096)
+
+
+def window_prefill():
+    """Sliding-window ragged causal prefill: 8 requests, qo = kv ~ U[2048, 8192],
+    32 q / 8 kv heads, hd 128, a 1024-key window."""
+    rng = np.random.default_rng(1006)
+    lens = rng.integers(2048, 8192, size=8, endpoint=True)
+    return make_prefill("window_prefill_r8_h32kv8_d128_w1024", lens, lens, 32, 8, 128,
+                        seed=1006, window=1024)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama8b_decode": llama8b_decode,
     "long_context_decode": long_context_decode,
     "ragged_prefill": ragged_prefill,
     "chunked_paged_prefill": chunked_paged_prefill,
+    "window_decode": window_decode,
+    "window_prefill": window_prefill,
 }

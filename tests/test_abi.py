@@ -46,7 +46,7 @@ def _decode(lib, **kw):
     a.update(kw)
     return lib.pa_decode(a["out"], a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["B"], a["nq"],
                          a["nkv"], a["hd"], a["bs"], a["mb"], a["nb"], a["sb"], a["sh"], a["st"],
-                         a["scale"], None)
+                         a["scale"], 0, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -71,15 +71,15 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
 def test_split_rejects_small_workspace(lib):
     need = pa.decode_split_workspace_size(2, 8, 128, 1000)
     rc = lib.pa_decode_split(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 63, 100,
-                             2 * 16 * 128, 16 * 128, 128, 0.1, 1000, ctypes.c_void_p(0x100000),
+                             2 * 16 * 128, 16 * 128, 128, 0.1, 0, 1000, ctypes.c_void_p(0x100000),
                              need - 1, None)
     assert rc == pa.PA_ERR_WORKSPACE
     rc = lib.pa_decode_split(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 63, 100,
-                             2 * 16 * 128, 16 * 128, 128, 0.1, 1000, ctypes.c_void_p(0x100010),
+                             2 * 16 * 128, 16 * 128, 128, 0.1, 0, 1000, ctypes.c_void_p(0x100010),
                              need, None)
     assert rc == pa.PA_ERR_WORKSPACE                      # not 256-byte aligned
     rc = lib.pa_decode_split(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 10, 100,
-                             2 * 16 * 128, 16 * 128, 128, 0.1, 1000, ctypes.c_void_p(0x100000),
+                             2 * 16 * 128, 16 * 128, 128, 0.1, 0, 1000, ctypes.c_void_p(0x100000),
                              need, None)
     assert rc == pa.PA_ERR_INVALID                        # max_seq_len > table capacity
 
