@@ -39,12 +39,14 @@ def load_library(path: str):
     lib = ctypes.CDLL(path)
     P = ctypes.c_void_p
     I, L, D = ctypes.c_int, ctypes.c_int64, ctypes.c_double
-    lib.oracle_write_cache.argtypes = [P, P, P, P, P, L, I, I, I, L, L, L, L]
+    F = ctypes.c_float
+    lib.oracle_write_cache.argtypes = [P, P, P, P, P, L, I, I, I, L, L, L, L, I, F, F]
     lib.oracle_write_cache.restype = L
-    lib.oracle_decode.argtypes = [P, P, P, P, L, L, L, P, P, I, I, I, I, I, I, D, P, L, I, I]
+    lib.oracle_decode.argtypes = [P, P, P, P, L, L, L, P, P, I, I, I, I, I, I, D, P, L, I, I, I,
+                                  D, D]
     lib.oracle_decode.restype = I
     lib.oracle_decode_partitions.argtypes = [P, P, P, P, P, P, L, L, L, P, P, I, I, I, I,
-                                             I, I, D, I, I, I, I]
+                                             I, I, D, I, I, I, I, I, D, D]
     lib.oracle_decode_partitions.restype = I
     lib.oracle_merge_partitions.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
     lib.oracle_merge_partitions.restype = I
@@ -55,6 +57,10 @@ def load_library(path: str):
     lib.oracle_swap_blocks.restype = L
     lib.oracle_copy_blocks.argtypes = [P, I, P, L, L, L]
     lib.oracle_copy_blocks.restype = L
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_value.restype = D
+    lib.oracle_e4m3_encode_array.argtypes = [P, P, L]
+    lib.oracle_e4m3_encode_array.restype = None
     return lib
 
 
@@ -101,25 +107,48 @@ def hnd_strides(num_kv_heads: int, block_size: int, head_dim: int):
     return (num_kv_heads * block_size * head_dim, block_size * head_dim, head_dim)
 
 
-def write_cache(k, v, k_cache, v_cache, slot_mapping, block_size, strides=None):
-    """In-place scatter of k/v [T][nkv][hd] (uint16) into the caches; returns #bad slots."""
+def e4m3_value(code: int) -> float:
+    """Value of one FP8 E4M3 code."""
+    return _load().oracle_e4m3_value(int(code) & 0xFF)
+
+
+def e4m3_encode(x):
+    """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _load().oracle_e4m3_encode_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def write_cache(k, v, k_cache, v_cache, slot_mapping, block_size, strides=None, kv_fp8=False,
+                k_scale=1.0, v_scale=1.0):
+    """In-place scatter of k/v [T][nkv][hd] (uint16 bf16 bits) into the caches (uint16, or
+    uint8 E4M3 codes of x / scale with kv_fp8); returns #bad slots."""
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
     sm = _c(slot_mapping, np.int64)
-    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous
-    assert v_cache.dtype == np.uint16 and v_cache.flags.c_contiguous
+    cache_t = np.uint8 if kv_fp8 else np.uint16
+    assert k_cache.dtype == cache_t and k_cache.flags.c_contiguous
+    assert v_cache.dtype == cache_t and v_cache.flags.c_contiguous
     T, nkv, hd = k.shape
     if strides is None:
         strides = hnd_strides(nkv, block_size, hd)
     nblocks = k_cache.size // strides[0]
     return _load().oracle_write_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(sm),
-                                      T, nkv, hd, block_size, nblocks, *strides)
+                                      T, nkv, hd, block_size, nblocks, *strides,
+                                      1 if kv_fp8 else 0, float(k_scale), float(v_scale))
+
+
+def _pool(a, kv_fp8):
+    return _c(a, np.uint8 if kv_fp8 else np.uint16)
 
 
 def decode(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, block_size, scale,
-           strides=None, items=None, nthreads=None, out=None, window=0):
+           strides=None, items=None, nthreads=None, out=None, window=0, kv_fp8=False,
+           k_scale=1.0, v_scale=1.0):
     """softmax(scale q K^T) V per (sequence, query head), fp64 [B][nq][hd]; window > 0
-    keeps the last `window` keys of each sequence."""
+    keeps the last `window` keys of each sequence; kv_fp8 reads E4M3 pools (uint8)
+    as code value * k_scale / v_scale."""
     q = _c(q, np.uint16)
     B, nq, hd = q.shape
     bt = _c(block_tables, np.int32)
@@ -129,17 +158,19 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, block_size
     if out is None:
         out = np.zeros((B, nq, hd), np.float64)
     it = None if items is None else _c(items, np.int32)
-    rc = _load().oracle_decode(_ptr(out), _ptr(q), _ptr(_c(k_cache, np.uint16)),
-                               _ptr(_c(v_cache, np.uint16)), *strides, _ptr(bt), _ptr(sl),
+    rc = _load().oracle_decode(_ptr(out), _ptr(q), _ptr(_pool(k_cache, kv_fp8)),
+                               _ptr(_pool(v_cache, kv_fp8)), *strides, _ptr(bt), _ptr(sl),
                                B, nq, num_kv_heads, hd, block_size, bt.shape[1], scale,
                                _ptr(it), 0 if it is None else it.size,
-                               nthreads or default_threads(), int(window))
+                               nthreads or default_threads(), int(window), 1 if kv_fp8 else 0,
+                               float(k_scale), float(v_scale))
     assert rc == 0
     return out
 
 
 def decode_partitions(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads, block_size,
-                      scale, max_parts, strides=None, part=PARTITION, nthreads=None, window=0):
+                      scale, max_parts, strides=None, part=PARTITION, nthreads=None, window=0,
+                      kv_fp8=False, k_scale=1.0, v_scale=1.0):
     """Per-partition (m, l, o) of the split-KV pass; untouched entries are NaN."""
     q = _c(q, np.uint16)
     B, nq, hd = q.shape
@@ -151,11 +182,12 @@ def decode_partitions(q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads,
     l = np.full((B, nq, max_parts), np.nan)
     o = np.full((B, nq, max_parts, hd), np.nan)
     rc = _load().oracle_decode_partitions(_ptr(m), _ptr(l), _ptr(o), _ptr(q),
-                                          _ptr(_c(k_cache, np.uint16)),
-                                          _ptr(_c(v_cache, np.uint16)), *strides, _ptr(bt),
+                                          _ptr(_pool(k_cache, kv_fp8)),
+                                          _ptr(_pool(v_cache, kv_fp8)), *strides, _ptr(bt),
                                           _ptr(sl), B, nq, num_kv_heads, hd, block_size,
                                           bt.shape[1], scale, part, max_parts,
-                                          nthreads or default_threads(), int(window))
+                                          nthreads or default_threads(), int(window),
+                                          1 if kv_fp8 else 0, float(k_scale), float(v_scale))
     assert rc == 0
     return m, l, o
 

@@ -36,6 +36,11 @@
  *  R4 partition p covers tokens [P*p, min(P*(p+1), L)); o_p is normalised by
  *     l_p, m_p is the max of the scaled scores (natural-log units).
  *  R13 a page-copy pair with a negative entry is padding and is skipped.
+ *  R15 an "fp8" KV cache ("paged_attn.py": kv_cache_dtype, k_scale, v_scale on
+ *     write_to_paged_cache and forward_decode) holds OCP FP8 E4M3 codes.  The
+ *     write stores the code nearest to the fp32 quotient x / scale (x the bf16
+ *     input widened to fp32; round to nearest, ties to the even code;
+ *     saturating at +-448); a read gives code value * scale.
  *  R14 a sliding window of W > 0 keys ("paged_attn.py", forward_prefix's
  *     sliding_window; "libmir-cuda attention/mod.rs", active_partitions(token
  *     count, window)): a query at position pos sees only keys j > pos - W, the
@@ -61,6 +66,60 @@ static double widen_bf16(uint16_t bits) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* ---- FP8 E4M3 (R15) --------------------------------------------------------- */
+
+/*
+ * Value of an E4M3 code, from the format's definition (OCP 8-bit floating point,
+ * E4M3): bit 7 sign, bits 6..3 exponent e with bias 7, bits 2..0 mantissa m.
+ * e = 0 is subnormal, 2^-6 * m / 8; otherwise 2^(e - 7) * (1 + m / 8).  There are
+ * no infinities; e = 15 with m = 7 is NaN, so the largest finite value is 448.
+ */
+double oracle_e4m3_value(uint8_t code) {
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/*
+ * The E4M3 code of the finite value nearest to x: the non-negative codes are
+ * searched for the one nearest to |x|, a tie going to the even code (the even
+ * mantissa), and x's sign is kept.  Beyond 448 the nearest finite value is 448
+ * (saturation; infinities too); NaN gives 0x7F.
+ */
+uint8_t oracle_e4m3_encode(float x) {
+    if (x != x) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (isinf(a)) return sign | 0x7E;
+    int best = 0;
+    double best_err = a;  /* code 0 is the value 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        double err = fabs(oracle_e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+void oracle_e4m3_encode_array(const float *x, uint8_t *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+
+/* A K or V pool: bf16 elements, or E4M3 codes read as code value * scale (R15). */
+typedef struct {
+    const void *base;
+    int fp8;
+    double scale;
+} kv_pool;
+
+static double pool_elem(const kv_pool *p, int64_t idx) {
+    if (p->fp8) return oracle_e4m3_value(((const uint8_t *)p->base)[idx]) * p->scale;
+    return widen_bf16(((const uint16_t *)p->base)[idx]);
 }
 
 /* ---- a tiny work-item thread pool ----------------------------------------- */
@@ -120,17 +179,16 @@ static void run_items(item_fn fn, void *ctx, int64_t n_items, int nthreads) {
  * element offsets koff[j] / voff[j].  n == 0 gives an all-zero row (R3).
  * scores is caller scratch of length >= n.
  */
-static void attend_row(double *out, const uint16_t *q, const uint16_t *kbase,
-                       const uint16_t *vbase, const int64_t *koff,
+static void attend_row(double *out, const uint16_t *q, const kv_pool *kp,
+                       const kv_pool *vp, const int64_t *koff,
                        const int64_t *voff, int64_t n, int hd, double scale,
                        double *scores) {
     for (int d = 0; d < hd; ++d) out[d] = 0.0;
     if (n <= 0) return;
     double mx = -INFINITY;
     for (int64_t j = 0; j < n; ++j) {
-        const uint16_t *kr = kbase + koff[j];
         double s = 0.0;
-        for (int d = 0; d < hd; ++d) s += widen_bf16(q[d]) * widen_bf16(kr[d]);
+        for (int d = 0; d < hd; ++d) s += widen_bf16(q[d]) * pool_elem(kp, koff[j] + d);
         s *= scale;
         scores[j] = s;
         if (s > mx) mx = s;
@@ -142,9 +200,8 @@ static void attend_row(double *out, const uint16_t *q, const uint16_t *kbase,
         den += p;
     }
     for (int64_t j = 0; j < n; ++j) {
-        const uint16_t *vr = vbase + voff[j];
         double w = scores[j];
-        for (int d = 0; d < hd; ++d) out[d] += w * widen_bf16(vr[d]);
+        for (int d = 0; d < hd; ++d) out[d] += w * pool_elem(vp, voff[j] + d);
     }
     for (int d = 0; d < hd; ++d) out[d] /= den;
 }
@@ -163,14 +220,17 @@ static int64_t window_first(int64_t pos, int64_t w) {
  * k[t][h][:] to k_cache at (page = slot / bs, head h, row = slot % bs), and
  * the same for v.  Caches are addressed by element strides (s_block, s_head,
  * s_token); head_dim is contiguous.  k, v are [num_tokens][nkv][hd].
+ * With kv_fp8 (kv_cache_dtype "fp8", R15) the caches hold bytes and each
+ * element is stored as the E4M3 code of (float)x / k_scale (v_scale for v),
+ * the quotient formed in fp32.
  * Returns the number of tokens whose slot was >= num_blocks * bs (those are
  * not written).
  */
-int64_t oracle_write_cache(const uint16_t *k, const uint16_t *v, uint16_t *k_cache,
-                           uint16_t *v_cache, const int64_t *slot_mapping,
+int64_t oracle_write_cache(const uint16_t *k, const uint16_t *v, void *k_cache,
+                           void *v_cache, const int64_t *slot_mapping,
                            int64_t num_tokens, int nkv, int hd, int bs,
                            int64_t num_blocks, int64_t s_block, int64_t s_head,
-                           int64_t s_token) {
+                           int64_t s_token, int kv_fp8, float k_scale, float v_scale) {
     int64_t bad = 0;
     for (int64_t t = 0; t < num_tokens; ++t) {
         int64_t slot = slot_mapping[t];
@@ -184,8 +244,14 @@ int64_t oracle_write_cache(const uint16_t *k, const uint16_t *v, uint16_t *k_cac
             int64_t dst = page * s_block + h * s_head + row * s_token;
             int64_t src = (t * nkv + h) * (int64_t)hd;
             for (int d = 0; d < hd; ++d) {
-                k_cache[dst + d] = k[src + d];
-                v_cache[dst + d] = v[src + d];
+                if (kv_fp8) {
+                    float kx = (float)widen_bf16(k[src + d]), vx = (float)widen_bf16(v[src + d]);
+                    ((uint8_t *)k_cache)[dst + d] = oracle_e4m3_encode(kx / k_scale);
+                    ((uint8_t *)v_cache)[dst + d] = oracle_e4m3_encode(vx / v_scale);
+                } else {
+                    ((uint16_t *)k_cache)[dst + d] = k[src + d];
+                    ((uint16_t *)v_cache)[dst + d] = v[src + d];
+                }
             }
         }
     }
@@ -197,7 +263,7 @@ int64_t oracle_write_cache(const uint16_t *k, const uint16_t *v, uint16_t *k_cac
 typedef struct {
     double *out;               /* [B][nq][hd] */
     const uint16_t *q;         /* [B][nq][hd] */
-    const uint16_t *kc, *vc;   /* paged pools */
+    kv_pool kc, vc;            /* paged pools */
     int64_t s_block, s_head, s_token;
     const int32_t *bt;         /* [B][max_blocks] */
     const int32_t *seq_lens;   /* [B] */
@@ -227,7 +293,7 @@ static void decode_item(void *vctx, int64_t it) {
     int64_t *off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
     double *sc = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
     for (int64_t j = j0; j < L; ++j) off[j - j0] = paged_offset(c, b, kh, j);
-    attend_row(c->out + bh * c->hd, c->q + bh * c->hd, c->kc, c->vc, off, off, n,
+    attend_row(c->out + bh * c->hd, c->q + bh * c->hd, &c->kc, &c->vc, off, off, n,
                c->hd, c->scale, sc);
     free(off);
     free(sc);
@@ -239,20 +305,22 @@ static void decode_item(void *vctx, int64_t it) {
  * kh = h / (nq / nkv); the L = seq_lens[b] keys are token j at page
  * bt[b][j / bs], row j % bs.  out[b][h] = softmax(scale * q K^T) V; L == 0
  * gives zeros (the "seq_len == 0" branch of the same function).  With a
- * window > 0 only the last `window` keys are attended (R14).
+ * window > 0 only the last `window` keys are attended (R14).  With kv_fp8 the
+ * pools hold E4M3 codes read as code value * k_scale / v_scale (R15).
  * items (optional, n_items entries of b * nq + h) restricts the work to those
  * output rows; the others are left untouched.
  */
-int oracle_decode(double *out, const uint16_t *q, const uint16_t *k_cache,
-                  const uint16_t *v_cache, int64_t s_block, int64_t s_head,
+int oracle_decode(double *out, const uint16_t *q, const void *k_cache,
+                  const void *v_cache, int64_t s_block, int64_t s_head,
                   int64_t s_token, const int32_t *block_tables,
                   const int32_t *seq_lens, int num_seqs, int nq, int nkv, int hd,
                   int bs, int max_blocks, double scale, const int32_t *items,
-                  int64_t n_items, int nthreads, int window) {
+                  int64_t n_items, int nthreads, int window, int kv_fp8,
+                  double k_scale, double v_scale) {
     if (nkv <= 0 || nq % nkv != 0) return -1;
-    decode_ctx c = {out, q, k_cache, v_cache, s_block, s_head, s_token,
-                    block_tables, seq_lens, nq, nkv, hd, bs, max_blocks, scale, items,
-                    window};
+    decode_ctx c = {out, q, {k_cache, kv_fp8, k_scale}, {v_cache, kv_fp8, v_scale},
+                    s_block, s_head, s_token, block_tables, seq_lens, nq, nkv, hd, bs,
+                    max_blocks, scale, items, window};
     int64_t n = items ? n_items : (int64_t)num_seqs * nq;
     run_items(decode_item, &c, n, nthreads);
     return 0;
@@ -286,9 +354,9 @@ static void part_item(void *vctx, int64_t it) {
         /* m_p: max of the scaled scores in the partition (R4) */
         double mx = -INFINITY;
         for (int64_t j = j0; j < j1; ++j) {
-            const uint16_t *kr = d->kc + paged_offset(d, b, kh, j);
+            int64_t kr = paged_offset(d, b, kh, j);
             double s = 0.0;
-            for (int e = 0; e < d->hd; ++e) s += widen_bf16(qr[e]) * widen_bf16(kr[e]);
+            for (int e = 0; e < d->hd; ++e) s += widen_bf16(qr[e]) * pool_elem(&d->kc, kr + e);
             s *= d->scale;
             sc[j - j0] = s;
             if (s > mx) mx = s;
@@ -300,8 +368,8 @@ static void part_item(void *vctx, int64_t it) {
         for (int64_t j = j0; j < j1; ++j) {
             double w = exp(sc[j - j0] - mx);
             lsum += w;
-            const uint16_t *vr = d->vc + paged_offset(d, b, kh, j);
-            for (int e = 0; e < d->hd; ++e) op[e] += w * widen_bf16(vr[e]);
+            int64_t vr = paged_offset(d, b, kh, j);
+            for (int e = 0; e < d->hd; ++e) op[e] += w * pool_elem(&d->vc, vr + e);
         }
         for (int e = 0; e < d->hd; ++e) op[e] /= lsum;
         c->m[bh * c->max_parts + p] = mx;
@@ -317,19 +385,21 @@ static void part_item(void *vctx, int64_t it) {
  * for p >= ceil(L / part) are left untouched.  With a window > 0 (R14) the
  * partitions run from the one holding key L - window on, that first one over
  * its keys inside the window only; the earlier entries are left untouched.
+ * kv_fp8, k_scale, v_scale as in oracle_decode (R15).
  */
 int oracle_decode_partitions(double *m, double *l, double *o, const uint16_t *q,
-                             const uint16_t *k_cache, const uint16_t *v_cache,
+                             const void *k_cache, const void *v_cache,
                              int64_t s_block, int64_t s_head, int64_t s_token,
                              const int32_t *block_tables, const int32_t *seq_lens,
                              int num_seqs, int nq, int nkv, int hd, int bs,
                              int max_blocks, double scale, int part, int max_parts,
-                             int nthreads, int window) {
+                             int nthreads, int window, int kv_fp8, double k_scale,
+                             double v_scale) {
     if (nkv <= 0 || nq % nkv != 0 || part <= 0) return -1;
     part_ctx c;
-    decode_ctx d = {NULL, q, k_cache, v_cache, s_block, s_head, s_token,
-                    block_tables, seq_lens, nq, nkv, hd, bs, max_blocks, scale, NULL,
-                    window};
+    decode_ctx d = {NULL, q, {k_cache, kv_fp8, k_scale}, {v_cache, kv_fp8, v_scale},
+                    s_block, s_head, s_token, block_tables, seq_lens, nq, nkv, hd, bs,
+                    max_blocks, scale, NULL, window};
     c.d = d;
     c.m = m;
     c.l = l;
@@ -383,7 +453,7 @@ int oracle_merge_partitions(double *out, const double *m, const double *l,
 typedef struct {
     double *out;                  /* [total_qo][nq][hd] */
     const uint16_t *q;            /* [total_qo][nq][hd] */
-    const uint16_t *k, *v;        /* contiguous [total_kv][nkv][hd], or paged pools */
+    kv_pool k, v;                 /* bf16: contiguous [total_kv][nkv][hd], or paged pools */
     const int32_t *qo_indptr, *kv_indptr; /* [batch + 1] */
     const int32_t *bt;            /* NULL: contiguous; else [batch][max_blocks] */
     int max_blocks, bs;
@@ -426,7 +496,7 @@ static void prefill_item(void *vctx, int64_t it) {
         }
     }
     int64_t oidx = (row * c->nq + h) * (int64_t)c->hd;
-    attend_row(c->out + oidx, c->q + oidx, c->k, c->v, off, off, cnt, c->hd, c->scale, sc);
+    attend_row(c->out + oidx, c->q + oidx, &c->k, &c->v, off, off, cnt, c->hd, c->scale, sc);
     free(off);
     free(sc);
 }
@@ -452,7 +522,8 @@ int oracle_prefill(double *out, const uint16_t *q, const uint16_t *k, const uint
                    double scale, int causal, const int64_t *rows, int64_t n_rows,
                    int nthreads, int window) {
     if (nkv <= 0 || nq % nkv != 0 || batch <= 0) return -1;
-    prefill_ctx c = {out, q, k, v, qo_indptr, kv_indptr, block_tables, max_blocks, bs,
+    prefill_ctx c = {out, q, {k, 0, 1.0}, {v, 0, 1.0}, qo_indptr, kv_indptr, block_tables,
+                     max_blocks, bs,
                      s_block, s_head, s_token, batch, nq, nkv, hd, causal, scale, rows,
                      window};
     int64_t nr = rows ? n_rows : (int64_t)qo_indptr[batch];

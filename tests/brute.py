@@ -15,7 +15,8 @@ def widen(bits):
 
 
 def gather_paged(pool_bits, block_table_row, length, kv_head, block_size, strides):
-    """Contiguous [length, hd] float64 rows of one kv head, read token by token."""
+    """Contiguous [length, hd] float64 rows of one kv head, read token by token.  A
+    float64 pool holds values already; any other dtype holds bf16 bit patterns."""
     sb, sh, st = strides
     flat = pool_bits.reshape(-1)
     hd = None
@@ -28,6 +29,8 @@ def gather_paged(pool_bits, block_table_row, length, kv_head, block_size, stride
         rows.append(flat[base:base + hd])
     if not rows:
         return np.zeros((0, _hd_from(pool_bits)))
+    if pool_bits.dtype == np.float64:
+        return np.stack(rows)
     return widen(np.stack(rows))
 
 
@@ -98,3 +101,9 @@ def brute_prefill_contiguous(q_bits, k_bits, v_bits, qo_indptr, kv_indptr, nkv, 
             out[q0:q1, h] = dense_softmax_attention(q[q0:q1, h], k[k0:k1, h // g],
                                                     v[k0:k1, h // g], scale, vis)
     return out
+
+
+def brute_decode_values(q_bits, kc_vals, vc_vals, bt, seq_lens, nkv, bs, scale, strides):
+    """brute_decode over float64 pools of values (e.g. a dequantised fp8 cache)."""
+    return brute_decode(q_bits, np.asarray(kc_vals, np.float64), np.asarray(vc_vals, np.float64),
+                        bt, seq_lens, nkv, bs, scale, strides)

@@ -53,6 +53,14 @@ MUTATIONS = {
         "int64_t p0 = (L > 0 ? window_first(L - 1, window) : 0) / part;", "int64_t p0 = 0;"),
     "prefill_window_ignored": ("int64_t lo = window_first(i + (kv - qo), c->window);",
                                "int64_t lo = 0;"),
+    "e4m3_bias_off_by_one": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    "e4m3_subnormal_exponent": ("ldexp(m / 8.0, -6)", "ldexp(m / 8.0, -7)"),
+    "e4m3_ties_to_odd": ("(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    "fp8_write_multiplies_by_scale": ("oracle_e4m3_encode(kx / k_scale)",
+                                      "oracle_e4m3_encode(kx * k_scale)"),
+    "fp8_read_ignores_scale": (
+        "return oracle_e4m3_value(((const uint8_t *)p->base)[idx]) * p->scale;",
+        "return oracle_e4m3_value(((const uint8_t *)p->base)[idx]);"),
 }
 
 
@@ -157,8 +165,41 @@ def _check_window():
         np.testing.assert_allclose(got, ref, atol=1e-12, rtol=0)
 
 
+def _check_fp8():
+    import torch
+    table = np.array([float(torch.tensor([c], dtype=torch.uint8).view(torch.float8_e4m3fn)
+                            .float()[0]) for c in range(256)])
+    for c in range(256):
+        got = oracle.e4m3_value(c)
+        assert (np.isnan(got) and np.isnan(table[c])) or got == table[c], hex(c)
+    mids = np.array([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10], np.float32)
+    np.testing.assert_array_equal(oracle.e4m3_encode(mids), [0x38, 0x3A, 0x00, 0x02])
+    # write then decode through non-unit scales, against numpy / torch on the side
+    rng = np.random.default_rng(9)
+    nb, nkv, bs, hd, T = 6, 2, 16, 64, 40
+    kc = np.zeros((nb, nkv, bs, hd), np.uint8)
+    vc = np.zeros_like(kc)
+    k = W.float_to_bits(rng.standard_normal((T, nkv, hd)).astype(np.float32))
+    v = W.float_to_bits(rng.standard_normal((T, nkv, hd)).astype(np.float32))
+    slots = np.arange(T, dtype=np.int64) + 8
+    oracle.write_cache(k, v, kc, vc, slots, bs, kv_fp8=True, k_scale=0.05, v_scale=0.02)
+    kq = W.bits_to_float(k).astype(np.float32) / np.float32(0.05)
+    ref = torch.from_numpy(np.clip(kq, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8)
+    for t, s in enumerate(slots):
+        np.testing.assert_array_equal(kc[s // bs, :, s % bs], ref.numpy()[t])
+    w = W.make_decode("mut", [48], 4, 2, 64, seed=42, num_blocks=nb)
+    bt = np.array([[0, 1, 2, 3]], np.int32)
+    q = W.to_bits(w.tensors("cpu")["q"])
+    got = oracle.decode(q, kc, vc, bt, np.array([48], np.int32), 2, 16, 0.125, kv_fp8=True,
+                        k_scale=0.05, v_scale=0.02)
+    ref = brute.brute_decode_values(q, table[kc] * 0.05, table[vc] * 0.02, bt,
+                                    np.array([48], np.int32), 2, 16, 0.125,
+                                    oracle.hnd_strides(2, 16, 64))
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
 CHECKS = [_check_decode, _check_prefill, _check_split, _check_write, _check_large_logits,
-          _check_blocks, _check_window]
+          _check_blocks, _check_window, _check_fp8]
 
 
 def _run_checks_in_child(lib_path):
