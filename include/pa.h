@@ -33,14 +33,15 @@
  *    NULL = legacy default stream) and returns immediately.
  *  - bf16 tensors are passed as void pointers to IEEE bfloat16 data.
  *  - KV pools are addressed by element strides (stride_block, stride_head,
- *    stride_token); the head_dim axis is contiguous.  The default layout is
+ *    stride_token) in elements of the pool's type (bytes for an FP8 pool), each
+ *    a multiple of 16 bytes; the head_dim axis is contiguous.  The default layout is
  *    HND per page, [num_blocks][num_kv_heads][block_size][head_dim], i.e.
  *    strides (nkv*bs*hd, bs*hd, hd).  The NHD page layout
  *    [num_blocks][block_size][num_kv_heads][head_dim] is (bs*nkv*hd, hd, nkv*hd).
  *    K and V pools share one set of strides.
  *  - Supported shapes: head_dim in {64, 128, 256}; block_size == 16;
  *    num_q_heads % num_kv_heads == 0 with group size in {1, 2, 4, 8}.
- *    Pointers must be 16-byte aligned and strides multiples of 8 elements.
+ *    Pointers must be 16-byte aligned.
  *  - sliding_window (decode and prefill): a query at position pos attends only
  *    to keys j > pos - sliding_window, the sliding_window most recent keys
  *    including its own position ("paged_attn.py", forward_prefix's
@@ -77,6 +78,18 @@ typedef enum {
     PA_ERR_DEVICE_BOUNDS = 6  /* device-side index guard fired */
 } pa_status;
 
+/*
+ * KV cache element types ("paged_attn.py": kv_cache_dtype, k_scale, v_scale on
+ * write_to_paged_cache and forward_decode).  PA_KV_FP8_E4M3 pools hold one byte
+ * per element, an OCP FP8 E4M3 code (sign, 4 exponent bits with bias 7, 3
+ * mantissa bits, largest finite 448, no infinities): the cache write stores the
+ * code nearest to the fp32 quotient x / k_scale (v_scale for V), ties to even,
+ * saturating at +-448; the decode reads code value * k_scale (v_scale).  The
+ * scales must be positive and finite.  With PA_KV_BF16 they are ignored.
+ * Paged prefill reads bf16 pools only.
+ */
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+
 /* Tokens per split-KV partition ("paged_attn.py", _PARTITION_SIZE). */
 #define PA_PARTITION_TOKENS 512
 
@@ -84,19 +97,21 @@ typedef enum {
  * pa_write_cache -- reshape_and_cache.
  * For each token t in [0, num_tokens) with slot = slot_mapping[t] >= 0, copies
  * k[t][h][:] into k_cache at page slot / block_size, head h, row
- * slot % block_size (and v likewise), bit for bit.  slot < 0 skips the token
+ * slot % block_size (and v likewise): bit for bit into a PA_KV_BF16 pool, or as
+ * the E4M3 codes of the elements divided by k_scale (v_scale) into a
+ * PA_KV_FP8_E4M3 pool (see pa_kv_dtype).  slot < 0 skips the token
  * (padding).  Slots >= num_blocks * block_size are not written and set
  * PA_ERR_DEVICE_BOUNDS in the device status word.  Two tokens with the same
  * slot in one call give an unspecified winner.
  *   k, v          [num_tokens][num_kv_heads][head_dim] bf16, contiguous
- *   k_cache, v_cache  pools addressed by the strides (see conventions)
+ *   k_cache, v_cache  pools of kv_dtype addressed by the strides (see conventions)
  *   slot_mapping  [num_tokens] int64
  */
 int pa_write_cache(const void *k, const void *v, void *k_cache, void *v_cache,
                    const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
                    int head_dim, int block_size, int64_t num_blocks,
                    int64_t stride_block, int64_t stride_head, int64_t stride_token,
-                   void *stream);
+                   int kv_dtype, float k_scale, float v_scale, void *stream);
 
 /*
  * pa_decode -- single-pass paged GQA decode (one query token per sequence).
@@ -108,6 +123,8 @@ int pa_write_cache(const void *k, const void *v, void *k_cache, void *v_cache,
  *   block_tables  [num_seqs][max_blocks_per_seq] int32 (entries past
  *                 ceil(seq_len / block_size) are never read)
  *   seq_lens      [num_seqs] int32
+ *   k_cache, v_cache, kv_dtype, k_scale, v_scale  the pools and their element
+ *                 type (see pa_kv_dtype)
  * One CTA walks the whole sequence of its (b, kv head); suited to short
  * contexts or large batches.  Allocates nothing.
  */
@@ -116,7 +133,7 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
               int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
               int64_t stride_head, int64_t stride_token, float sm_scale, int sliding_window,
-              void *stream);
+              int kv_dtype, float k_scale, float v_scale, void *stream);
 
 /*
  * Bytes of workspace pa_decode_split needs (256-byte aligned sub-buffers):
@@ -152,8 +169,8 @@ int pa_decode_split(void *out, const void *q, const void *k_cache, const void *v
                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                     int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
                     int64_t stride_head, int64_t stride_token, float sm_scale,
-                    int sliding_window, int max_seq_len, void *workspace,
-                    size_t workspace_bytes, void *stream);
+                    int sliding_window, int kv_dtype, float k_scale, float v_scale,
+                    int max_seq_len, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * The two passes of pa_decode_split as separate calls (same arguments and
@@ -167,8 +184,9 @@ int pa_decode_partitions(const void *q, const void *k_cache, const void *v_cache
                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                          int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
                          int64_t stride_head, int64_t stride_token, float sm_scale,
-                         int sliding_window, int max_seq_len, void *workspace,
-                         size_t workspace_bytes, void *stream);
+                         int sliding_window, int kv_dtype, float k_scale, float v_scale,
+                         int max_seq_len, void *workspace, size_t workspace_bytes,
+                         void *stream);
 int pa_decode_merge(void *out, const int32_t *seq_lens, int num_seqs, int num_q_heads,
                     int head_dim, int max_seq_len, int sliding_window, const void *workspace,
                     size_t workspace_bytes, void *stream);
@@ -199,7 +217,8 @@ int pa_decode_split_static(void *out, const void *q, const void *k_cache, const 
                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                            int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
                            int64_t stride_head, int64_t stride_token, float sm_scale,
-                           int sliding_window, int max_seq_len, void *stream);
+                           int sliding_window, int kv_dtype, float k_scale, float v_scale,
+                           int max_seq_len, void *stream);
 
 /*
  * Bytes of workspace pa_ragged_prefill needs (a device-built tile schedule).

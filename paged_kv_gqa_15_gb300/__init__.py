@@ -20,6 +20,7 @@ _lib = None
 
 PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_WORKSPACE, PA_ERR_TIMEOUT, \
     PA_ERR_DEVICE_BOUNDS = range(7)
+PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1   # pa_kv_dtype
 STATUS_NAMES = {1: "INVALID", 2: "UNSUPPORTED", 3: "CUDA", 4: "WORKSPACE", 5: "TIMEOUT",
                 6: "DEVICE_BOUNDS"}
 
@@ -41,19 +42,19 @@ def load():
     lib = ctypes.CDLL(LIB_PATH)
     P, I, L, F, Z = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                      ctypes.c_size_t)
-    lib.pa_write_cache.argtypes = [P, P, P, P, P, L, I, I, I, L, L, L, L, P]
-    lib.pa_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, P]
+    lib.pa_write_cache.argtypes = [P, P, P, P, P, L, I, I, I, L, L, L, L, I, F, F, P]
+    lib.pa_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, I, F, F, P]
     lib.pa_decode_split_workspace_size.argtypes = [I, I, I, I]
     lib.pa_decode_split_workspace_size.restype = Z
     lib.pa_decode_split_workspace_offsets.argtypes = [I, I, I, I, P, P, P]
     lib.pa_decode_split_workspace_offsets.restype = None
-    lib.pa_decode_split.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, I, P,
-                                    Z, P]
-    lib.pa_decode_partitions.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, I, P,
-                                         Z, P]
+    lib.pa_decode_split.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, I, F,
+                                    F, I, P, Z, P]
+    lib.pa_decode_partitions.argtypes = [P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I, I, F,
+                                         F, I, P, Z, P]
     lib.pa_decode_merge.argtypes = [P, P, I, I, I, I, I, P, Z, P]
     lib.pa_decode_split_static.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, L, L, L, L, F, I,
-                                           I, P]
+                                           I, F, F, I, P]
     lib.pa_decode_split_static.restype = I
     lib.pa_ragged_prefill_workspace_size.argtypes = [I, I, I, I]
     lib.pa_ragged_prefill_workspace_size.restype = Z
@@ -98,6 +99,15 @@ def pool_strides(cache: torch.Tensor, layout: str = "HND"):
     s = cache.stride()
     assert cache.dim() == 4 and s[3] == 1, "pool must be 4-D with a contiguous head_dim"
     return (s[0], s[1], s[2]) if layout == "HND" else (s[0], s[2], s[1])
+
+
+def kv_dtype_of(cache: torch.Tensor) -> int:
+    """pa_kv_dtype of a pool tensor: bf16, or FP8 E4M3 codes (float8_e4m3fn or uint8)."""
+    if cache.dtype == torch.bfloat16:
+        return PA_KV_BF16
+    if cache.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        return PA_KV_FP8_E4M3
+    raise TypeError(f"unsupported KV cache dtype {cache.dtype}")
 
 
 def _pool_geometry(cache, layout):
@@ -183,17 +193,20 @@ def pa_swap_blocks(src, dst, block_mapping, stream=None):
                                  _stream(stream)))
 
 
-def pa_write_cache(k, v, k_cache, v_cache, slot_mapping, layout="HND", stream=None):
-    """reshape_and_cache: scatter k/v [T, nkv, hd] into the pools at slot_mapping [T]."""
+def pa_write_cache(k, v, k_cache, v_cache, slot_mapping, layout="HND", stream=None,
+                   k_scale=1.0, v_scale=1.0):
+    """reshape_and_cache: scatter k/v [T, nkv, hd] into the pools at slot_mapping [T];
+    an FP8 pool (float8_e4m3fn or uint8) stores the E4M3 codes of x / k_scale (v_scale)."""
     nb, nkv, bs, hd = _pool_geometry(k_cache, layout)
     sb, sh, st = pool_strides(k_cache, layout)
     _check(load().pa_write_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
                                  _ptr(slot_mapping), k.shape[0], nkv, hd, bs, nb, sb, sh, st,
+                                 kv_dtype_of(k_cache), float(k_scale), float(v_scale),
                                  _stream(stream)))
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale, layout="HND",
-              stream=None, sliding_window=0):
+              stream=None, sliding_window=0, k_scale=1.0, v_scale=1.0):
     """Single-pass paged GQA decode into out [B, nq, hd]; sliding_window > 0 keeps the
     last sliding_window keys of each sequence."""
     nb, nkv, bs, hd = _pool_geometry(k_cache, layout)
@@ -201,7 +214,8 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale, layout
     B, nq, _ = q.shape
     _check(load().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                             _ptr(seq_lens), B, nq, nkv, hd, bs, block_tables.shape[1], nb, sb,
-                            sh, st, float(sm_scale), int(sliding_window), _stream(stream)))
+                            sh, st, float(sm_scale), int(sliding_window), kv_dtype_of(k_cache),
+                            float(k_scale), float(v_scale), _stream(stream)))
 
 
 def decode_split_workspace_size(num_seqs, num_q_heads, head_dim, max_seq_len) -> int:
@@ -233,7 +247,8 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 
 def pa_decode_split(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale, max_seq_len,
-                    workspace, layout="HND", stream=None, sliding_window=0):
+                    workspace, layout="HND", stream=None, sliding_window=0, k_scale=1.0,
+                    v_scale=1.0):
     """Split-KV paged GQA decode (512-token partitions + LSE merge) into out [B, nq, hd]."""
     nb, nkv, bs, hd = _pool_geometry(k_cache, layout)
     sb, sh, st = pool_strides(k_cache, layout)
@@ -241,7 +256,8 @@ def pa_decode_split(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale, 
     _check(load().pa_decode_split(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(block_tables), _ptr(seq_lens), B, nq, nkv, hd, bs,
                                   block_tables.shape[1], nb, sb, sh, st, float(sm_scale),
-                                  int(sliding_window), int(max_seq_len), _ptr(workspace),
+                                  int(sliding_window), kv_dtype_of(k_cache), float(k_scale),
+                                  float(v_scale), int(max_seq_len), _ptr(workspace),
                                   workspace.numel(), _stream(stream)))
 
 
@@ -249,7 +265,8 @@ STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # PA_STATIC_SCRATCH_BYTES in include/pa
 
 
 def pa_decode_split_static(out, q, k_cache, v_cache, block_tables, seq_lens, sm_scale,
-                           max_seq_len, layout="HND", stream=None, sliding_window=0):
+                           max_seq_len, layout="HND", stream=None, sliding_window=0,
+                           k_scale=1.0, v_scale=1.0):
     """pa_decode_split with the library's fixed device scratch instead of a workspace,
     for callers that cannot allocate device memory.  Batches needing more than
     STATIC_SCRATCH_BYTES of partials are rejected; concurrent calls on one device race."""
@@ -259,12 +276,14 @@ def pa_decode_split_static(out, q, k_cache, v_cache, block_tables, seq_lens, sm_
     _check(load().pa_decode_split_static(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                          _ptr(block_tables), _ptr(seq_lens), B, nq, nkv, hd, bs,
                                          block_tables.shape[1], nb, sb, sh, st, float(sm_scale),
-                                         int(sliding_window), int(max_seq_len),
+                                         int(sliding_window), kv_dtype_of(k_cache),
+                                         float(k_scale), float(v_scale), int(max_seq_len),
                                          _stream(stream)))
 
 
 def pa_decode_partitions(q, k_cache, v_cache, block_tables, seq_lens, sm_scale, max_seq_len,
-                         workspace, layout="HND", stream=None, sliding_window=0):
+                         workspace, layout="HND", stream=None, sliding_window=0, k_scale=1.0,
+                         v_scale=1.0):
     """Split-KV pass 1: per-partition (m, l, o) into the workspace."""
     nb, nkv, bs, hd = _pool_geometry(k_cache, layout)
     sb, sh, st = pool_strides(k_cache, layout)
@@ -272,6 +291,7 @@ def pa_decode_partitions(q, k_cache, v_cache, block_tables, seq_lens, sm_scale, 
     _check(load().pa_decode_partitions(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                        _ptr(seq_lens), B, nq, nkv, hd, bs, block_tables.shape[1],
                                        nb, sb, sh, st, float(sm_scale), int(sliding_window),
+                                       kv_dtype_of(k_cache), float(k_scale), float(v_scale),
                                        int(max_seq_len), _ptr(workspace), workspace.numel(),
                                        _stream(stream)))
 

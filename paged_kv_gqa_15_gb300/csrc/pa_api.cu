@@ -77,14 +77,29 @@ int check_heads(int head_dim, int num_q_heads, int num_kv_heads) {
     return PA_OK;
 }
 
+// Element size in bytes of a KV cache dtype (0 for an unknown one).
+int kv_elem_bytes(int kv_dtype) {
+    return kv_dtype == PA_KV_BF16 ? 2 : (kv_dtype == PA_KV_FP8_E4M3 ? 1 : 0);
+}
+
+int check_kv_dtype(int kv_dtype, float k_scale, float v_scale) {
+    if (!kv_elem_bytes(kv_dtype)) return fail(PA_ERR_UNSUPPORTED, "kv_dtype %d", kv_dtype);
+    if (kv_dtype == PA_KV_FP8_E4M3 &&
+        (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY))
+        return fail(PA_ERR_INVALID, "fp8 cache scales must be positive and finite (%g, %g)",
+                    (double)k_scale, (double)v_scale);
+    return PA_OK;
+}
+
 int check_pool(int head_dim, int block_size, int64_t num_blocks, int num_kv_heads,
-               int64_t sb, int64_t sh, int64_t st) {
+               int64_t sb, int64_t sh, int64_t st, int elem_bytes = 2) {
     if (block_size != 16)
         return fail(PA_ERR_UNSUPPORTED, "block_size %d: only 16-token blocks", block_size);
     if (num_blocks <= 0) return fail(PA_ERR_INVALID, "num_blocks %lld", (long long)num_blocks);
-    if (sb <= 0 || sh <= 0 || st <= 0 || sb % 8 || sh % 8 || st % 8)
+    const int64_t q = 16 / elem_bytes;   // elements per 16 bytes
+    if (sb <= 0 || sh <= 0 || st <= 0 || sb % q || sh % q || st % q)
         return fail(PA_ERR_INVALID,
-                    "pool strides (%lld, %lld, %lld) must be positive multiples of 8 elements",
+                    "pool strides (%lld, %lld, %lld) must be positive multiples of 16 bytes",
                     (long long)sb, (long long)sh, (long long)st);
     if (st < head_dim)
         return fail(PA_ERR_INVALID, "token stride %lld < head_dim %d", (long long)st, head_dim);
@@ -98,11 +113,14 @@ int decode_common(pa::DecodeParams &p, void *out, const void *q, const void *k_c
                   const void *v_cache, const int32_t *block_tables, const int32_t *seq_lens,
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                   int max_blocks_per_seq, int64_t num_blocks, int64_t sb, int64_t sh, int64_t st,
-                  float sm_scale, int sliding_window) {
+                  float sm_scale, int sliding_window, int kv_dtype, float k_scale, float v_scale) {
     if (num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs %d", num_seqs);
     int rc = check_heads(head_dim, num_q_heads, num_kv_heads);
     if (rc) return rc;
-    rc = check_pool(head_dim, block_size, num_blocks, num_kv_heads, sb, sh, st);
+    rc = check_kv_dtype(kv_dtype, k_scale, v_scale);
+    if (rc) return rc;
+    rc = check_pool(head_dim, block_size, num_blocks, num_kv_heads, sb, sh, st,
+                    kv_elem_bytes(kv_dtype));
     if (rc) return rc;
     if (max_blocks_per_seq <= 0)
         return fail(PA_ERR_INVALID, "max_blocks_per_seq %d", max_blocks_per_seq);
@@ -130,6 +148,9 @@ int decode_common(pa::DecodeParams &p, void *out, const void *q, const void *k_c
     p.rows_contiguous = (st == head_dim) ? 1 : 0;
     p.max_seq_len = max_blocks_per_seq * 16;
     p.window = sliding_window > 0 ? sliding_window : 0;
+    p.kv_fp8 = kv_dtype == PA_KV_FP8_E4M3 ? 1 : 0;
+    p.k_scale = p.kv_fp8 ? k_scale : 1.f;
+    p.v_scale = p.kv_fp8 ? v_scale : 1.f;
     return PA_OK;
 }
 
@@ -161,13 +182,16 @@ int pa_get_device_status(int *status_h, void *stream) {
 int pa_write_cache(const void *k, const void *v, void *k_cache, void *v_cache,
                    const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
                    int head_dim, int block_size, int64_t num_blocks, int64_t stride_block,
-                   int64_t stride_head, int64_t stride_token, void *stream) {
+                   int64_t stride_head, int64_t stride_token, int kv_dtype, float k_scale,
+                   float v_scale, void *stream) {
     if (num_tokens < 0) return fail(PA_ERR_INVALID, "num_tokens %lld", (long long)num_tokens);
     if (num_kv_heads <= 0) return fail(PA_ERR_INVALID, "num_kv_heads %d", num_kv_heads);
     if (head_dim != 64 && head_dim != 128 && head_dim != 256)
         return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", head_dim);
-    int rc = check_pool(head_dim, block_size, num_blocks, num_kv_heads, stride_block,
-                        stride_head, stride_token);
+    int rc = check_kv_dtype(kv_dtype, k_scale, v_scale);
+    if (rc) return rc;
+    rc = check_pool(head_dim, block_size, num_blocks, num_kv_heads, stride_block, stride_head,
+                    stride_token, kv_elem_bytes(kv_dtype));
     if (rc) return rc;
     if (num_tokens > 0 && (!k || !v || !k_cache || !v_cache || !slot_mapping))
         return fail(PA_ERR_INVALID, "null pointer argument");
@@ -187,6 +211,9 @@ int pa_write_cache(const void *k, const void *v, void *k_cache, void *v_cache,
     p.num_kv_heads = num_kv_heads;
     p.head_dim = head_dim;
     p.block_size = block_size;
+    p.kv_fp8 = kv_dtype == PA_KV_FP8_E4M3 ? 1 : 0;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
     rc = status_ptr(&p.status);
     if (rc) return rc;
     cudaError_t e = pa::launch_write_cache(p, static_cast<cudaStream_t>(stream));
@@ -199,12 +226,12 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
               int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
               int64_t stride_head, int64_t stride_token, float sm_scale, int sliding_window,
-              void *stream) {
+              int kv_dtype, float k_scale, float v_scale, void *stream) {
     pa::DecodeParams p;
     int rc = decode_common(p, out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
                            num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                            num_blocks, stride_block, stride_head, stride_token, sm_scale,
-                           sliding_window);
+                           sliding_window, kv_dtype, k_scale, v_scale);
     if (rc) return rc;
     rc = status_ptr(&p.status);
     if (rc) return rc;
@@ -267,14 +294,15 @@ int pa_decode_partitions(const void *q, const void *k_cache, const void *v_cache
                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                          int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
                          int64_t stride_head, int64_t stride_token, float sm_scale,
-                         int sliding_window, int max_seq_len, void *workspace,
-                         size_t workspace_bytes, void *stream) {
+                         int sliding_window, int kv_dtype, float k_scale, float v_scale,
+                         int max_seq_len, void *workspace, size_t workspace_bytes,
+                         void *stream) {
     pa::DecodeParams p;
     // `out` is not written by this pass; q stands in for the alignment check.
     int rc = decode_common(p, const_cast<void *>(q), q, k_cache, v_cache, block_tables,
                            seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                            max_blocks_per_seq, num_blocks, stride_block, stride_head,
-                           stride_token, sm_scale, sliding_window);
+                           stride_token, sm_scale, sliding_window, kv_dtype, k_scale, v_scale);
     if (rc) return rc;
     p.out = nullptr;
     rc = split_setup(p, num_seqs, num_q_heads, head_dim, max_blocks_per_seq, max_seq_len,
@@ -320,13 +348,13 @@ int pa_decode_split(void *out, const void *q, const void *k_cache, const void *v
                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                     int max_blocks_per_seq, int64_t num_blocks, int64_t stride_block,
                     int64_t stride_head, int64_t stride_token, float sm_scale,
-                    int sliding_window, int max_seq_len, void *workspace,
-                    size_t workspace_bytes, void *stream) {
+                    int sliding_window, int kv_dtype, float k_scale, float v_scale,
+                    int max_seq_len, void *workspace, size_t workspace_bytes, void *stream) {
     pa::DecodeParams p;
     int rc = decode_common(p, out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
                            num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                            num_blocks, stride_block, stride_head, stride_token, sm_scale,
-                           sliding_window);
+                           sliding_window, kv_dtype, k_scale, v_scale);
     if (rc) return rc;
     rc = split_setup(p, num_seqs, num_q_heads, head_dim, max_blocks_per_seq, max_seq_len,
                      workspace, workspace_bytes);

@@ -57,6 +57,7 @@ extern "C" int pa_decode_split_static(void *out, const void *q, const void *k_ca
                                       int max_blocks_per_seq, int64_t num_blocks,
                                       int64_t stride_block, int64_t stride_head,
                                       int64_t stride_token, float sm_scale, int sliding_window,
+                                      int kv_dtype, float k_scale, float v_scale,
                                       int max_seq_len, void *stream) {
     const size_t need =
         pa_decode_split_workspace_size(num_seqs, num_q_heads, head_dim, max_seq_len);
@@ -71,6 +72,6 @@ extern "C" int pa_decode_split_static(void *out, const void *q, const void *k_ca
     return pa_decode_split(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
                            num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                            num_blocks, stride_block, stride_head, stride_token, sm_scale,
-                           sliding_window, max_seq_len, scratch,
+                           sliding_window, kv_dtype, k_scale, v_scale, max_seq_len, scratch,
                            static_cast<size_t>(PA_STATIC_SCRATCH_BYTES), stream);
 }

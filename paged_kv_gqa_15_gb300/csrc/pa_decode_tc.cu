@@ -607,7 +607,7 @@ cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
 
 bool decode_tc_supported(const DecodeParams &p, int head_dim) {
     const int g = p.num_kv_heads > 0 ? p.num_q_heads / p.num_kv_heads : 0;
-    return head_dim == kHD && (g == 4 || g == 8) && p.num_seqs <= kMaxSeqsTc &&
+    return !p.kv_fp8 && head_dim == kHD && (g == 4 || g == 8) && p.num_seqs <= kMaxSeqsTc &&
            (p.s_token * 2) % 16 == 0 && (p.s_head * 2) % 16 == 0 && (p.s_block * 2) % 16 == 0 &&
            (reinterpret_cast<uintptr_t>(p.k_cache) & 15) == 0 &&
            (reinterpret_cast<uintptr_t>(p.v_cache) & 15) == 0 &&

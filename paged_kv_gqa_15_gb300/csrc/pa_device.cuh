@@ -32,6 +32,19 @@ __host__ __device__ __forceinline__ int active_partitions_cap(int max_parts, int
     return cap < max_parts ? cap : max_parts;
 }
 
+// Two FP8 E4M3 codes (low 16 bits: the first in the low byte) as floats.  Every
+// E4M3 value is exactly an f16 value, and every f16 value a float.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two)));
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\t"
+        "cvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+    return make_float2(lo, hi);
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -16,6 +16,8 @@ struct WriteCacheParams {
     int64_t num_tokens, num_blocks;
     int64_t s_block, s_head, s_token;
     int num_kv_heads, head_dim, block_size;
+    int kv_fp8;                   // store FP8 E4M3 codes of x / scale (else bf16 bits)
+    float k_scale, v_scale;
     int *status;
 };
 
@@ -34,6 +36,8 @@ struct DecodeParams {
     float scale_log2;             // sm_scale * log2(e)
     int rows_contiguous;          // s_token == head_dim: one bulk copy per page
     int window;                   // sliding window in keys (> 0), or 0 for none
+    int kv_fp8;                   // the pools hold FP8 E4M3 codes (else bf16)
+    float k_scale, v_scale;       // FP8: element value = code value * scale
     int *status;
 };
 
@@ -68,6 +72,9 @@ int api_cuda_fail(cudaError_t e, const char *what);
 // zeros; false when the driver entry point or the encoding fails.
 bool encode_tensor_map_bf16(CUtensorMap *tm, const void *base, int rank, const cuuint64_t *dims,
                             const cuuint64_t *strides_bytes, const cuuint32_t *box);
+// The same for a tensor of bytes (FP8 E4M3 codes).
+bool encode_tensor_map_u8(CUtensorMap *tm, const void *base, int rank, const cuuint64_t *dims,
+                          const cuuint64_t *strides_bytes, const cuuint32_t *box);
 
 cudaError_t launch_write_cache(const WriteCacheParams &p, cudaStream_t stream);
 // Tensor-core partition pass of the split decode (head_dim 128, GQA group 4 or 8).
@@ -75,6 +82,9 @@ bool decode_tc_supported(const DecodeParams &p, int head_dim);
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
 // Returns cudaErrorNotSupported for an unsupported (head_dim, group) pair.
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaStream_t stream);
+// The CUDA-core decode over FP8 E4M3 caches (pa_decode_fp8.cu).
+cudaError_t launch_decode_fp8(const DecodeParams &p, int head_dim, bool split,
+                              cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams &p, int head_dim, cudaStream_t stream);
 cudaError_t launch_prefill(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream);
 

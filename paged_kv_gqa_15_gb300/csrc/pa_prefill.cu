@@ -269,7 +269,7 @@ struct PrefillItem {
     int j0;     // first key tile, kv_lo / BN: the item's key tiles are j0 .. j0 + n_kv - 1
 };
 
-template <bool PAGED, int BN>
+template <bool PAGED, int BN, bool WINDOW>
 __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, long long i) {
     PrefillItem w;
     const int2 tile = p.tiles[i / p.nq];
@@ -286,8 +286,9 @@ __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, long
     }
     w.q0 = ok ? tile.y * kBM : 0;
     w.work = ok && w.q0 < w.qo_len;
-    w.n_kv = w.work ? key_tiles(w.q0, w.qo_len, w.kv_len, p.causal, p.window, BN) : 0;
-    w.kv_lo = w.work ? window_first_key(w.q0, w.qo_len, w.kv_len, p.window) : 0;
+    const int window = WINDOW ? p.window : 0;
+    w.n_kv = w.work ? key_tiles(w.q0, w.qo_len, w.kv_len, p.causal, window, BN) : 0;
+    w.kv_lo = w.work ? window_first_key(w.q0, w.qo_len, w.kv_len, window) : 0;
     w.j0 = w.kv_lo / BN;
     return w;
 }
@@ -304,11 +305,14 @@ __device__ __forceinline__ PrefillItem end_item() {
 // Persistent: each CTA claims items of the heaviest-first list (item i = query
 // tile i / nq, head i % nq) one at a time from a global counter, so the load
 // balances itself; TMEM and barriers are set up once and the next item's
-// Q / K / V loads overlap the current item's tail.
-template <int HD, int BN, bool PAGED>
+// Q / K / V loads overlap the current item's tail.  WINDOW instantiates the
+// sliding-window form (items start at their window's key tile, rows get a lower
+// column bound); without it the window terms are compiled out.
+template <int HD, int BN, bool PAGED, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
     using C = PrefillCfg<HD, BN>;
+    const int window = WINDOW ? p.window : 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -405,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 } else {
                     const long long claimed = atomicAdd(p.item_counter, 1);
                     item_q[slot] =
-                        claimed < n_items ? prefill_item<PAGED, BN>(p, claimed) : end_item();
+                        claimed < n_items ? prefill_item<PAGED, BN, WINDOW>(p, claimed) : end_item();
                     mbar_arrive(&item_full[slot]);
                 }
             }
@@ -449,7 +453,8 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 tma_load_3d(smem + C::OFF_Q + lane * kBM * 128, &p.tm_q, lane * 64, w.h,
                             w.qo_start + w.q0, q_full);
             const int pages_seq = (w.kv_len + kBlockSize - 1) / kBlockSize;
-            const int page_lo = w.kv_lo / kBlockSize;
+            const int j0 = WINDOW ? w.j0 : 0;
+            const int page_lo = WINDOW ? w.kv_lo / kBlockSize : 0;
             // Loads key tile j (kv = 0) or value tile j (kv = 1) of this item into its
             // ring stage; g is the tile's index over all items of this CTA.
             auto load_tile = [&](int kv, int j, uint32_t g, int page) {
@@ -480,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 } else {
                     if (lane < C::QCH)
                         tma_load_3d(dst + lane * C::KV_CHUNK, tm, lane * 64, kh,
-                                    w.kv_start + (w.j0 + j) * BN, full);
+                                    w.kv_start + (j0 + j) * BN, full);
                 }
             };
             // The MMA warp consumes K_{j+1} (for S_{j+1}) before V_j (for P_j V_j), so K
@@ -490,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             // ahead of their use.
             int pg_cur = 0, raw_next = -2;
             if constexpr (PAGED) {
-                pg_cur = page_fix(page_raw(w.r, w.j0, pages_seq, page_lo));
-                if (w.n_kv > 1) raw_next = page_raw(w.r, w.j0 + 1, pages_seq, page_lo);
+                pg_cur = page_fix(page_raw(w.r, j0, pages_seq, page_lo));
+                if (w.n_kv > 1) raw_next = page_raw(w.r, j0 + 1, pages_seq, page_lo);
             }
             load_tile(0, 0, kv_it, pg_cur);
             for (int j = 0; j < w.n_kv && !stop; ++j) {
@@ -500,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                     if constexpr (PAGED) {
                         pg_next = page_fix(raw_next);
                         if (j + 2 < w.n_kv)
-                            raw_next = page_raw(w.r, w.j0 + j + 2, pages_seq, page_lo);
+                            raw_next = page_raw(w.r, j0 + j + 2, pages_seq, page_lo);
                     }
                     load_tile(0, j + 1, kv_it + j + 1, pg_next);
                 }
@@ -585,6 +590,9 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t base = kv_it;
+                // keys from the item's first tile on, and its first row in the window
+                const int kv_rel = WINDOW ? w.kv_len - w.j0 * BN : w.kv_len;
+                const int head = WINDOW ? w.kv_lo - w.j0 * BN : 0;
                 for (int j = 0; j < w.n_kv && ok; ++j) {
                     const uint32_t g = base + j;
                     const int s = g % C::KS;      // K stage
@@ -600,10 +608,9 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                                     kd + ((c * C::KV_CHUNK + inner) >> 4), idesc_s, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(&s_full[b]);
-                    if (j >= 1) issue_pv(g - 1, j - 1, w.kv_len - w.j0 * BN, w.kv_lo - w.j0 * BN);
+                    if (j >= 1) issue_pv(g - 1, j - 1, kv_rel, head);
                 }
-                issue_pv(base + w.n_kv - 1, w.n_kv - 1, w.kv_len - w.j0 * BN,
-                         w.kv_lo - w.j0 * BN);
+                issue_pv(base + w.n_kv - 1, w.n_kv - 1, kv_rel, head);
                 kv_it += w.n_kv;
                 ++q_it;
                 ++o_items;
@@ -659,14 +666,14 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                         tmem_load_64(tmem + t_lane + C::TM_S + s * BN + c * 64, chunk);
                     }
                 }
-                const int jj = w.j0 + j;               // key tile of the request
+                const int jj = WINDOW ? w.j0 + j : j;  // key tile of the request
                 // under a window, row q_pos sees keys j > q_pos - window only; the tile
                 // needs the lower mask when it starts before the last row's window
-                const bool need_lo = p.window > 0 && jj * BN < w.q0 + kBM + off - p.window;
+                const bool need_lo = WINDOW && jj * BN < w.q0 + kBM + off - window;
                 const bool need_mask = (jj + 1) * BN > w.kv_len ||
                                        (p.causal && (jj + 1) * BN - 1 > w.q0 + off) || need_lo;
                 const int lim = min(w.kv_len, p.causal ? q_pos + 1 : w.kv_len) - jj * BN;
-                const int lo = p.window > 0 ? q_pos - p.window + 1 - jj * BN : 0;
+                const int lo = WINDOW ? q_pos - window + 1 - jj * BN : 0;
                 float m_use, corr;
                 const bool grow = tile_max<BN>(sr, need_mask, lo, lim, scale, rs, m_use, corr);
                 if (j > 0 && __any_sync(kFullMask, grow)) {
@@ -776,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
 
 // ---- host side ----------------------------------------------------------------------
 
-template <int HD, int BN, bool PAGED>
+template <int HD, int BN, bool PAGED, bool WINDOW>
 cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream) {
     using C = PrefillCfg<HD, BN>;
     {
@@ -812,7 +819,7 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
                                                     p.status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const void *kern = reinterpret_cast<const void *>(prefill_kernel<HD, BN, PAGED>);
+    const void *kern = reinterpret_cast<const void *>(prefill_kernel<HD, BN, PAGED, WINDOW>);
     const uint32_t smem = C::SMEM;
     const int per_sm = C::CTAS_PER_SM, threads = kThreads;
     static int configured_device = -1;
@@ -848,24 +855,28 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
     return cudaGetLastError();
 }
 
+template <int HD, bool WINDOW>
+cudaError_t launch_prefill_hd(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream) {
+    return p.block_tables != nullptr ? launch_prefill_t<HD, 64, true, WINDOW>(p, L, stream)
+                                     : launch_prefill_t<HD, 64, false, WINDOW>(p, L, stream);
+}
+
+template <bool WINDOW>
+cudaError_t launch_prefill_w(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream) {
+    switch (L.head_dim) {
+        case 64: return launch_prefill_hd<64, WINDOW>(p, L, stream);
+        case 128: return launch_prefill_hd<128, WINDOW>(p, L, stream);
+        case 256: return launch_prefill_hd<256, WINDOW>(p, L, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(PrefillParams &p, const PrefillLaunch &L, cudaStream_t stream) {
     if (p.n_tiles == 0) return cudaSuccess;
-    const bool paged = p.block_tables != nullptr;
-    switch (L.head_dim) {
-        case 64:
-            return paged ? launch_prefill_t<64, 64, true>(p, L, stream)
-                         : launch_prefill_t<64, 64, false>(p, L, stream);
-        case 128:
-            return paged ? launch_prefill_t<128, 64, true>(p, L, stream)
-                         : launch_prefill_t<128, 64, false>(p, L, stream);
-        case 256:
-            return paged ? launch_prefill_t<256, 64, true>(p, L, stream)
-                         : launch_prefill_t<256, 64, false>(p, L, stream);
-        default:
-            return cudaErrorNotSupported;
-    }
+    return p.window > 0 ? launch_prefill_w<true>(p, L, stream)
+                        : launch_prefill_w<false>(p, L, stream);
 }
 
 }  // namespace pa

@@ -37,6 +37,7 @@ EncodeTiledFn encode_fn() {
 struct MapKey {
     const void *base;
     int rank;
+    int dtype;
     cuuint64_t dims[5];
     cuuint64_t strides[4];
     cuuint32_t box[5];
@@ -55,13 +56,17 @@ int cache_next = 0;
 
 }  // namespace
 
-bool encode_tensor_map_bf16(CUtensorMap *tm, const void *base, int rank, const cuuint64_t *dims,
-                            const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+namespace {
+
+bool encode_tensor_map(CUtensorMap *tm, CUtensorMapDataType dtype, const void *base, int rank,
+                       const cuuint64_t *dims, const cuuint64_t *strides_bytes,
+                       const cuuint32_t *box) {
     if (rank < 1 || rank > 5) return false;
     MapKey key;
     std::memset(&key, 0, sizeof key);
     key.base = base;
     key.rank = rank;
+    key.dtype = static_cast<int>(dtype);
     for (int i = 0; i < rank; ++i) {
         key.dims[i] = dims[i];
         key.box[i] = box[i];
@@ -79,7 +84,7 @@ bool encode_tensor_map_bf16(CUtensorMap *tm, const void *base, int rank, const c
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    if (fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
+    if (fn(tm, dtype, rank, const_cast<void *>(base), dims,
            strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
@@ -90,6 +95,20 @@ bool encode_tensor_map_bf16(CUtensorMap *tm, const void *base, int rank, const c
     e.key = key;
     e.map = *tm;
     return true;
+}
+
+}  // namespace
+
+bool encode_tensor_map_bf16(CUtensorMap *tm, const void *base, int rank, const cuuint64_t *dims,
+                            const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+    return encode_tensor_map(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims,
+                             strides_bytes, box);
+}
+
+bool encode_tensor_map_u8(CUtensorMap *tm, const void *base, int rank, const cuuint64_t *dims,
+                          const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+    return encode_tensor_map(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides_bytes,
+                             box);
 }
 
 }  // namespace pa

@@ -46,7 +46,7 @@ def _decode(lib, **kw):
     a.update(kw)
     return lib.pa_decode(a["out"], a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["B"], a["nq"],
                          a["nkv"], a["hd"], a["bs"], a["mb"], a["nb"], a["sb"], a["sh"], a["st"],
-                         a["scale"], 0, None)
+                         a["scale"], 0, 0, 1.0, 1.0, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -71,15 +71,15 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
 def test_split_rejects_small_workspace(lib):
     need = pa.decode_split_workspace_size(2, 8, 128, 1000)
     rc = lib.pa_decode_split(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 63, 100,
-                             2 * 16 * 128, 16 * 128, 128, 0.1, 0, 1000, ctypes.c_void_p(0x100000),
+                             2 * 16 * 128, 16 * 128, 128, 0.1, 0, 0, 1.0, 1.0, 1000, ctypes.c_void_p(0x100000),
                              need - 1, None)
     assert rc == pa.PA_ERR_WORKSPACE
     rc = lib.pa_decode_split(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 63, 100,
-                             2 * 16 * 128, 16 * 128, 128, 0.1, 0, 1000, ctypes.c_void_p(0x100010),
+                             2 * 16 * 128, 16 * 128, 128, 0.1, 0, 0, 1.0, 1.0, 1000, ctypes.c_void_p(0x100010),
                              need, None)
     assert rc == pa.PA_ERR_WORKSPACE                      # not 256-byte aligned
     rc = lib.pa_decode_split(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 10, 100,
-                             2 * 16 * 128, 16 * 128, 128, 0.1, 0, 1000, ctypes.c_void_p(0x100000),
+                             2 * 16 * 128, 16 * 128, 128, 0.1, 0, 0, 1.0, 1.0, 1000, ctypes.c_void_p(0x100000),
                              need, None)
     assert rc == pa.PA_ERR_INVALID                        # max_seq_len > table capacity
 
@@ -103,11 +103,16 @@ def test_write_cache_rejects_bad_arguments(lib):
         a = dict(ok)
         a.update(kw)
         return lib.pa_write_cache(FAKE, FAKE, FAKE, FAKE, FAKE, a["T"], a["nkv"], a["hd"],
-                                  a["bs"], a["nb"], a["sb"], a["sh"], a["st"], None)
+                                  a["bs"], a["nb"], a["sb"], a["sh"], a["st"], a.get("dt", 0),
+                                  a.get("ks", 1.0), a.get("vs", 1.0), None)
     assert call(hd=80) == pa.PA_ERR_UNSUPPORTED
     assert call(T=-1) == pa.PA_ERR_INVALID
     assert call(bs=8) == pa.PA_ERR_UNSUPPORTED
     assert call(sh=0) == pa.PA_ERR_INVALID
+    assert call(dt=2) == pa.PA_ERR_UNSUPPORTED                  # no such kv_dtype
+    assert call(dt=1, ks=0.0) == pa.PA_ERR_INVALID              # fp8 scales must be > 0
+    assert call(dt=1, vs=float("inf")) == pa.PA_ERR_INVALID
+    assert call(dt=1, sb=4096 + 8) == pa.PA_ERR_INVALID         # 16-byte stride rule
 
 
 def test_error_raises_with_message(lib):

@@ -31,7 +31,7 @@ def _static_call(lib, out, q, kc, vc, bt, sl, w, max_seq_len):
         ctypes.c_void_p(kc.data_ptr()), ctypes.c_void_p(vc.data_ptr()),
         ctypes.c_void_p(bt.data_ptr()), ctypes.c_void_p(sl.data_ptr()), w.batch,
         w.num_q_heads, w.num_kv_heads, w.head_dim, 16, bt.shape[1], w.num_blocks, sb, sh, st,
-        ctypes.c_float(w.scale), 0, max_seq_len,
+        ctypes.c_float(w.scale), 0, 0, ctypes.c_float(1.0), ctypes.c_float(1.0), max_seq_len,
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
@@ -74,7 +74,8 @@ def test_static_scratch_rejects_batches_beyond_its_size():
         ctypes.c_void_p(q64.data_ptr()), ctypes.c_void_p(q64.data_ptr()),
         ctypes.c_void_p(kc.data_ptr()), ctypes.c_void_p(vc.data_ptr()),
         ctypes.c_void_p(big.data_ptr()), ctypes.c_void_p(sl64.data_ptr()), 64, 32, 8, 128, 16,
-        8192, w.num_blocks, sb, sh, st, ctypes.c_float(w.scale), 0, 131072,
+        8192, w.num_blocks, sb, sh, st, ctypes.c_float(w.scale), 0, 0, ctypes.c_float(1.0),
+        ctypes.c_float(1.0), 131072,
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == pa.PA_ERR_WORKSPACE
     assert b"PA_STATIC_SCRATCH_BYTES" in lib.pa_last_error()
