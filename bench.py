@@ -185,9 +185,18 @@ class ClockSampler:
 # GPU arms
 # ---------------------------------------------------------------------------------------
 
+# FP8 caches hold E4M3 codes of x / FP8_SCALE: N(0, 1) inputs then use the format's
+# range (|x| / FP8_SCALE up to 448 for |x| <= 7) and read back as code value * FP8_SCALE.
+FP8_SCALE = 1.0 / 64
+
+
 def decode_setup(w, dev, split=True):
     import paged_kv_gqa_15_gb300 as pa
     t = w.tensors(dev)
+    if w.kv_fp8:   # input preparation, outside any timed region
+        for name in ("k_cache", "v_cache"):
+            t[name] = (t[name].float() / FP8_SCALE).to(torch.float8_e4m3fn)
+            torch.cuda.empty_cache()
     s = {"t": t,
          "bt": torch.from_numpy(w.block_tables).to(dev),
          "sl": torch.from_numpy(w.seq_lens).to(dev),
@@ -206,21 +215,22 @@ def decode_step(w, s, stream, evs=None):
     n = 0
     if evs is not None:
         evs.append(_ev(stream))
+    scales = dict(k_scale=FP8_SCALE, v_scale=FP8_SCALE) if w.kv_fp8 else {}
     if w.new_token_write:
         pa.pa_write_cache(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], s["slots"],
-                          stream=stream)
+                          stream=stream, **scales)
         n += 1
         if evs is not None:
             evs.append(_ev(stream))
     if not w.split:   # the workload's decode is one pass over each sequence
         pa.pa_decode(s["out"], t["q"], t["k_cache"], t["v_cache"], s["bt"], s["sl"], w.scale,
-                     stream=stream, sliding_window=w.window)
+                     stream=stream, sliding_window=w.window, **scales)
         if evs is not None:
             evs.append(_ev(stream))
         return n + 1
     L = max(w.max_seq_len, 1)
     pa.pa_decode_partitions(t["q"], t["k_cache"], t["v_cache"], s["bt"], s["sl"], w.scale, L,
-                            s["ws"], stream=stream, sliding_window=w.window)
+                            s["ws"], stream=stream, sliding_window=w.window, **scales)
     if evs is not None:
         evs.append(_ev(stream))
     pa.pa_decode_merge(s["out"], s["sl"], L, s["ws"], stream=stream, sliding_window=w.window)
@@ -295,7 +305,7 @@ def time_steps(step, steps, warmup, stream, device, labels, flush=False):
 
 
 def decode_footprint(w):
-    return 2 * w.num_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2
+    return 2 * w.num_blocks * w.num_kv_heads * w.block_size * w.head_dim * (1 if w.kv_fp8 else 2)
 
 
 def prefill_footprint(w):
@@ -318,8 +328,8 @@ def bench_decode(w, steps, warmup, dev, stream, peaks, peak_kind):
     kv = w.kv_bytes()
     value, ms_max = aggregate_throughput(kv, ms, dev)
     kern_ms = per["decode_partitions" if w.split else "decode"]
-    src = ("pa_decode_tc.cu", "pa_tcgen05.cuh", "pa_device.cuh") if w.split else \
-        ("pa_decode.cu", "pa_device.cuh")
+    src = (("pa_decode_tc_fp8.cu" if w.kv_fp8 else "pa_decode_tc.cu"), "pa_tcgen05.cuh",
+           "pa_device.cuh") if w.split else ("pa_decode_kernel.cuh", "pa_device.cuh")
     res = {
         "value": value / 1e9, "unit": "GB/s", "ms_per_step": ms_max,
         "kv_bytes_per_step": kv, "launches": launches,
@@ -539,12 +549,13 @@ def oracle_decode_time(w, t_host, seqs, nthreads):
     seqs = np.asarray(seqs)
     t0 = time.perf_counter()
     oracle.decode(q[seqs], kc, vc, w.block_tables[seqs], w.seq_lens[seqs], w.num_kv_heads,
-                  w.block_size, w.scale, nthreads=nthreads, window=w.window)
+                  w.block_size, w.scale, nthreads=nthreads, window=w.window, kv_fp8=w.kv_fp8,
+                  k_scale=FP8_SCALE, v_scale=FP8_SCALE)
     dt = time.perf_counter() - t0
     lens = w.seq_lens[seqs].astype(np.int64)
     if w.window > 0:
         lens = np.minimum(lens, w.window)
-    kv = int(lens.sum()) * w.num_kv_heads * w.head_dim * 4
+    kv = int(lens.sum()) * w.num_kv_heads * w.head_dim * 2 * (1 if w.kv_fp8 else 2)
     return dt, kv
 
 
@@ -564,9 +575,20 @@ def oracle_decode_sample(w, t_host, target_s=12.0, nthreads=None):
     return kv / dt / 1e9, dt, n, passes, nthreads
 
 
+def host_pool(w, pool):
+    """Host copy of a pool for the oracle: bf16 bits, or E4M3 codes of an fp8
+    workload (quantised here if the pool is still bf16)."""
+    from paged_kv_gqa_15_gb300 import workloads as W
+    if not w.kv_fp8:
+        return W.to_bits(pool)
+    if pool.dtype == torch.bfloat16:
+        pool = (pool.float() / FP8_SCALE).to(torch.float8_e4m3fn)
+    return pool.cpu().view(torch.uint8).numpy()
+
+
 def host_decode_inputs(w, t):
     from paged_kv_gqa_15_gb300 import workloads as W
-    return W.to_bits(t["q"]), W.to_bits(t["k_cache"]), W.to_bits(t["v_cache"])
+    return W.to_bits(t["q"]), host_pool(w, t["k_cache"]), host_pool(w, t["v_cache"])
 
 
 def run_reference(args, w, rank):
@@ -578,7 +600,7 @@ def run_reference(args, w, rank):
     import oracle
     from paged_kv_gqa_15_gb300 import workloads as W
     t = w.tensors("cpu")
-    host = (W.to_bits(t["q"]), W.to_bits(t["k_cache"]), W.to_bits(t["v_cache"]))
+    host = host_decode_inputs(w, t)
     th = oracle.default_threads()
     per_step = 90.0 / max(args.steps + args.warmup, 1)
     one, _ = oracle_decode_time(w, host, [0], th)
@@ -629,7 +651,9 @@ def workload_config(w):
                 "block_size": w.block_size,
                 "seq_lens": f"U[{int(w.seq_lens.min())},{int(w.seq_lens.max())}] seed {w.seed}",
                 "num_blocks": w.num_blocks, "kv_bytes_per_step": w.kv_bytes(),
-                "sliding_window": w.window or None, "l2": l2_note(decode_footprint(w))}
+                "sliding_window": w.window or None,
+                "kv_cache_dtype": "fp8_e4m3" if w.kv_fp8 else "bf16",
+                "kv_scales": FP8_SCALE if w.kv_fp8 else None, "l2": l2_note(decode_footprint(w))}
     return {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "causal": w.causal,
             "paged": w.paged, "total_qo": w.total_qo, "total_kv": w.total_kv,
@@ -648,6 +672,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama8b_decode")
     ap.add_argument("--extra", default="long_context_decode,tiny_decode,ragged_prefill,"
                                        "chunked_paged_prefill,window_decode,window_prefill,"
+                                       "llama8b_decode_fp8,long_context_decode_fp8,"
                                        "copy_blocks_fork,swap_blocks",
                     help="other workloads measured in the same run (N=1 only); 'none' for none")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -1,0 +1,715 @@
+// pa_decode_tc_fp8.cu -- split-KV paged GQA decode on the Blackwell tensor cores over
+// an FP8 E4M3 KV cache, for head_dim 128 and GQA groups of 4 or 8 query heads.
+//
+// What it computes is the partition pass of the split decode ("paged_attn.py", the V2
+// branch of forward_decode, with kv_cache_dtype "fp8", k_scale and v_scale): as the
+// bf16 tensor-core decode (pa_decode_tc.cu), with every K element worth its E4M3 code
+// value times k_scale and every V element its code value times v_scale.
+//
+// GB300 design, on top of the bf16 tensor-core decode:
+//  * Pages stream as bytes: a 128-token tile is 16 KB, half the bf16 traffic.
+//  * S^T = K Q^T runs on the 8-bit tensor cores (tcgen05.mma kind::f8f6f4) straight
+//    from the TMA tile.  Q is split per head into two E4M3 rows, hi = e4m3(q s) and
+//    lo = e4m3(q s - hi), with s a power of two that puts max|q s| in [128, 256): the
+//    pair holds q to about 2^-8 relative, close to its bf16 input, so K needs no
+//    conversion.  The MMA's N = 16 columns hold the G hi rows and the G lo rows; the
+//    softmax adds each pair and divides by s.
+//  * O^T = V^T P takes V as an MN-major operand, so four converter warps turn each V
+//    tile into f16 (exact for every E4M3 value) in the 128-byte-swizzled layout of a
+//    TMA-loaded 16-bit tile, writing zeros for rows outside the partition's tokens; P
+//    is f16 and the MMA is kind::f16.  k_scale scales the scores, v_scale the outputs.
+//  * Warps: 0 Q and K producer, 1 MMA issuer, 2-5 softmax and epilogue, 6 V producer,
+//    7-10 V converters.  The softmax warps compute the per-head Q scale themselves
+//    (the same function of q as the producer), so no scale crosses between warps.
+//    Every wait is bounded.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+constexpr unsigned kMask = 0xffffffffu;
+constexpr int kHD = 128;
+constexpr int kTok = 128;                      // tokens per tile (MMA M of S^T)
+constexpr int kTiles = kPartition / kTok;      // tiles per partition
+constexpr int kPagesPerTile = kTok / kBlockSize;
+constexpr int kN = 16;                         // MMA N: G hi and G lo rows of Q, padded
+constexpr int kThreads = 352;                  // 11 warps
+constexpr int kKStages = 4;                    // fp8 K tile ring
+constexpr int kV8Stages = 4;                   // fp8 V tile ring
+constexpr int kV16Stages = 2;                  // converted f16 V tile ring
+constexpr uint32_t kTile8Bytes = kTok * 128;   // 128 tokens x 128 one-byte dims
+constexpr uint32_t kTile16Chunk = kTok * 128;  // one 64-dim chunk of a 16-bit tile
+constexpr uint32_t kTile16Bytes = 2 * kTile16Chunk;
+constexpr uint32_t kQBytes = kN * 128;         // Q rows: 16 x 128 bytes
+constexpr uint32_t kSmallChunk = kN * 128;     // one 64-column chunk of P (16 rows)
+constexpr uint32_t kPTile = 2 * kSmallChunk;   // P of one tile
+constexpr uint32_t kPBytes = kTiles * kPTile;
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffV8 = kOffK + kKStages * kTile8Bytes;
+constexpr uint32_t kOffV16 = kOffV8 + kV8Stages * kTile8Bytes;
+constexpr uint32_t kOffQ = kOffV16 + kV16Stages * kTile16Bytes;   // two Q buffers
+constexpr uint32_t kOffP = kOffQ + 2 * kQBytes;                  // one P buffer (see below)
+constexpr uint32_t kOffRed = kOffP + kPBytes;                    // float [2][4 warps][16]
+constexpr uint32_t kOffQinv = kOffRed + 2 * 4 * kN * 4;          // float [2][16]
+constexpr uint32_t kOffPref = kOffQinv + 2 * kN * 4;             // int [MAXB + 1]
+constexpr int kMaxSeqs = 2048;
+constexpr uint32_t kOffBar = kOffPref + (kMaxSeqs + 8) * 4;
+constexpr uint32_t kSmem = kOffBar + 512 + 1024;                 // + realignment slack
+constexpr uint32_t kTmemCols = 256;            // S: 2 x 4 tiles x 16; O: 2 x 16
+constexpr uint32_t kTmS = 0, kTmO = 128;
+static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+static_assert((2 * (kKStages + kV8Stages + kV16Stages) + 17) * 8 <= 512, "barriers fit");
+static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms on 1 KB boundaries");
+
+struct DecodeTc8Params {
+    CUtensorMap tm_k;   // pool bytes as (hd, 16 rows, nkv, blocks), box {128, 16, 1, 1}
+    CUtensorMap tm_v;
+    DecodeParams d;
+};
+
+__device__ __forceinline__ int seq_len8(const DecodeParams &p, int b, bool flag) {
+    int L = p.seq_lens[b];
+    if (L < 0) L = 0;
+    int cap = p.max_blocks * kBlockSize;
+    if (p.max_seq_len < cap) cap = p.max_seq_len;
+    if (L > cap) {
+        if (flag) atomicOr(p.status, kStatusBounds);
+        L = cap;
+    }
+    return L;
+}
+
+// The k-th item of this CTA: (b, kh, partition); false when there is none.
+__device__ __forceinline__ bool item8(const DecodeParams &p, const int *pref, long long total,
+                                      int k, int &b, int &kh, int &part) {
+    const long long i = static_cast<long long>(blockIdx.x) + static_cast<long long>(k) * gridDim.x;
+    if (i >= total) return false;
+    kh = static_cast<int>(i % p.num_kv_heads);
+    const int j = static_cast<int>(i / p.num_kv_heads);
+    int lo = 0, hi = p.num_seqs;          // largest b with pref[b] <= j
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pref[mid] <= j) lo = mid; else hi = mid;
+    }
+    b = lo;
+    part = j - pref[b];
+    if (p.window > 0)   // items count from the partition holding the window's first key
+        part += window_start(seq_len8(p, b, false), p.window) / kPartition;
+    return true;
+}
+
+// Tokens [t0 + t_lo, t0 + n_tok) of the partition at t0, in tiles i_lo .. n_tiles - 1.
+struct Span8 {
+    int t0, n_tok, t_lo, i_lo, n_tiles;
+};
+
+__device__ __forceinline__ Span8 span8(const DecodeParams &p, int b, int part) {
+    const int L = seq_len8(p, b, false);
+    Span8 s;
+    s.t0 = part * kPartition;
+    s.n_tok = min(kPartition, L - s.t0);
+    s.t_lo = max(0, window_start(L, p.window) - s.t0);
+    s.i_lo = s.t_lo / kTok;
+    s.n_tiles = (s.n_tok + kTok - 1) / kTok;
+    return s;
+}
+
+// The power of two s with max|q| * s in [128, 256) (1 for a zero or NaN maximum):
+// q * s then spans E4M3's top binades, and the hi / lo split keeps ~8 bits of q.
+__device__ __forceinline__ float q_split_scale(float m) {
+    if (!(m > 0.f)) return 1.f;
+    int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xffu);
+    if (e == 0) e = 1;                    // subnormal maximum: treat as 2^-126
+    int k = 7 - (e - 127);
+    k = max(-126, min(127, k));
+    return __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+}
+
+// Max |x| over one 16-byte chunk (8 bf16) of q, then over the 16 lanes of a half warp
+// (the 16 chunks of one head's 128 dims).  Every lane of the warp must call it.
+__device__ __forceinline__ float head_max(const uint4 &raw) {
+    float f[8];
+    unpack_bf16x8(raw, f);
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    if (f[0] != f[0] || f[1] != f[1] || f[2] != f[2] || f[3] != f[3] || f[4] != f[4] ||
+        f[5] != f[5] || f[6] != f[6] || f[7] != f[7])
+        m = __int_as_float(0x7fc00000);   // NaN: the scale stays 1, NaN flows on
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) {
+        const float o = __shfl_xor_sync(kMask, m, off);
+        m = (m != m || o != o) ? __int_as_float(0x7fc00000) : fmaxf(m, o);
+    }
+    return m;
+}
+
+// E4M3 codes of (x1, x0) packed as (high byte, low byte), round to nearest, saturating.
+__device__ __forceinline__ uint16_t e4m3x2(float x1, float x0) {
+    uint16_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(x1), "f"(x0));
+    return h;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc8_kernel(const __grid_constant__ DecodeTc8Params prm) {
+    const DecodeParams &p = prm.d;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float *red = reinterpret_cast<float *>(smem + kOffRed);
+    float *qinv = reinterpret_cast<float *>(smem + kOffQinv);
+    int *pref = reinterpret_cast<int *>(smem + kOffPref);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    // Items are numbered e per CTA; item e uses the Q, S and O buffers e % 2.
+    uint64_t *k_full = bars;                       // fp8 K tile landed (TMA)
+    uint64_t *k_empty = k_full + kKStages;         // its score MMAs are done (commit)
+    uint64_t *v8_full = k_empty + kKStages;        // fp8 V tile landed (TMA)
+    uint64_t *v8_empty = v8_full + kV8Stages;      // the converters have read it (4 arrivals)
+    uint64_t *v16_full = v8_empty + kV8Stages;     // f16 V tile written (4 arrivals)
+    uint64_t *v16_empty = v16_full + kV16Stages;   // its P.V MMAs are done (commit)
+    uint64_t *q_full = v16_empty + kV16Stages;     // [2] Q rows written
+    uint64_t *q_empty = q_full + 2;                // [2] the item's score MMAs are done
+    uint64_t *s_full = q_empty + 2;                // [2] S^T of all the item's tiles (commit)
+    uint64_t *s_free = s_full + 2;                 // [2] softmax has read S^T (4 arrivals)
+    uint64_t *p_full = s_free + 2;                 // [2] P written (4 arrivals)
+    uint64_t *o_full = p_full + 2;                 // [2] O^T done (commit)
+    uint64_t *o_free = o_full + 2;                 // [2] epilogue has read O^T (4 arrivals)
+    uint64_t *drain = o_free + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(drain + 2);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // a programmatic dependent of the cache write: start up, then wait for it
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    for (int b = threadIdx.x; b < p.num_seqs; b += kThreads) {
+        const int L = seq_len8(p, b, blockIdx.x == 0);
+        pref[b + 1] = (L + kPartition - 1) / kPartition - window_start(L, p.window) / kPartition;
+    }
+    if (threadIdx.x == 0) pref[0] = 0;
+    // Q rows 2G .. 15 and P rows G .. 15 stay zero (padding of the MMA's N)
+    for (uint32_t i = threadIdx.x; i < (2 * kQBytes + kPBytes) / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < kV8Stages; ++s) {
+            mbar_init(&v8_full[s], 1);
+            mbar_init(&v8_empty[s], 4);
+        }
+        for (int s = 0; s < kV16Stages; ++s) {
+            mbar_init(&v16_full[s], 4);
+            mbar_init(&v16_empty[s], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&q_full[x], 1);
+            mbar_init(&q_empty[x], 1);
+            mbar_init(&s_full[x], 1);
+            mbar_init(&s_free[x], 4);
+            mbar_init(&p_full[x], 4);
+            mbar_init(&o_full[x], 1);
+            mbar_init(&o_free[x], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    fence_proxy_async_smem();   // the zeroed padding is read by the tensor core
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 1; base <= p.num_seqs; base += 32) {
+            const int idx = base + lane;
+            int v = idx <= p.num_seqs ? pref[idx] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(kMask, v, off);
+                if (lane >= off) v += u;
+            }
+            if (idx <= p.num_seqs) pref[idx] = v + carry;
+            carry += __shfl_sync(kMask, v, 31);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const long long total = static_cast<long long>(pref[p.num_seqs]) * p.num_kv_heads;
+    const int nq = p.num_q_heads;
+
+    if (warp == 0 || warp == 6) {
+        // ------------- producers: warp 0 Q rows and K tiles, warp 6 V tiles -------------
+        const bool is_v = warp == 6;
+        const int NS = is_v ? kV8Stages : kKStages;
+        uint64_t *full = is_v ? v8_full : k_full;
+        uint64_t *empty = is_v ? v8_empty : k_empty;
+        uint8_t *ring = smem + (is_v ? kOffV8 : kOffK);
+        const CUtensorMap *tm = is_v ? &prm.tm_v : &prm.tm_k;
+        if (lane == 0) prefetch_tensormap(tm);
+        const uint64_t policy = l2_policy_evict_first();
+        uint32_t it = 0;
+        int stop = 0;
+        int b, kh, part;
+        // the Q producer reads each item's q one item ahead, so the load's latency does
+        // not hold up the item's K tiles
+        auto q_chunks = [&](int bb, int kk, uint4 (&dst)[G / 2]) {
+            const uint4 *qg = reinterpret_cast<const uint4 *>(
+                static_cast<const __nv_bfloat16 *>(p.q) + (static_cast<int64_t>(bb) * nq + kk * G) * kHD);
+#pragma unroll
+            for (int i = 0; i < G / 2; ++i) dst[i] = __ldg(qg + lane + 32 * i);
+        };
+        uint4 qnext[G / 2];
+        if (!is_v && item8(p, pref, total, 0, b, kh, part)) q_chunks(b, kh, qnext);
+        for (int e = 0; !stop && item8(p, pref, total, e, b, kh, part); ++e) {
+            const Span8 sp = span8(p, b, part);
+            if (!is_v) {
+                // Q of the group as E4M3 hi / lo rows: row g = hi of head g, row G + g its
+                // lo; bytes of each 128-byte row swizzled in 16-byte units by row % 8
+                const int x = e & 1;
+                if (lane == 0 && !mbar_wait(&q_empty[x], ((e >> 1) & 1) ^ 1u, p.status, abort_flag))
+                    stop = 1;
+                stop = __shfl_sync(kMask, stop, 0);
+                if (stop) break;
+                uint8_t *qb = smem + kOffQ + x * kQBytes;
+                uint4 qcur[G / 2];
+#pragma unroll
+                for (int i = 0; i < G / 2; ++i) qcur[i] = qnext[i];
+                {
+                    int b1, kh1, part1;
+                    if (item8(p, pref, total, e + 1, b1, kh1, part1)) q_chunks(b1, kh1, qnext);
+                }
+#pragma unroll
+                for (int i = 0; i < G / 2; ++i) {
+                    const int c = lane + 32 * i;                   // head c / 16, dims (c % 16) * 8
+                    const uint4 raw = qcur[i];
+                    const float s = q_split_scale(head_max(raw));
+                    float f[8];
+                    unpack_bf16x8(raw, f);
+                    uint32_t hw[2], lw[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint16_t hp[2], lp[2];
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const float a0 = f[4 * h + 2 * j] * s, a1 = f[4 * h + 2 * j + 1] * s;
+                            hp[j] = e4m3x2(a1, a0);
+                            const float2 back = e4m3x2_to_float2(hp[j]);
+                            lp[j] = e4m3x2(a1 - back.y, a0 - back.x);
+                        }
+                        hw[h] = hp[0] | (static_cast<uint32_t>(hp[1]) << 16);
+                        lw[h] = lp[0] | (static_cast<uint32_t>(lp[1]) << 16);
+                    }
+                    const int g = c >> 4, d0 = (c & 15) * 8;
+                    const int rh = g, rl = G + g;
+                    *reinterpret_cast<uint2 *>(qb + rh * 128 + ((((d0 >> 4) ^ (rh & 7))) << 4) + (d0 & 15)) =
+                        make_uint2(hw[0], hw[1]);
+                    *reinterpret_cast<uint2 *>(qb + rl * 128 + ((((d0 >> 4) ^ (rl & 7))) << 4) + (d0 & 15)) =
+                        make_uint2(lw[0], lw[1]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_full[x]);
+            }
+            // page ids of the partition, one per lane (past the sequence, before the window
+            // or bad: an out-of-range box that reads zeros); the V producer flags nothing
+            const int np = (sp.n_tok + kBlockSize - 1) / kBlockSize;
+            const int pg_lo = sp.t_lo / kBlockSize;
+            int page = (lane >= pg_lo && lane < np)
+                           ? p.block_tables[static_cast<int64_t>(b) * p.max_blocks +
+                                            sp.t0 / kBlockSize + lane]
+                           : -2;
+            const bool bad = page != -2 && (page < 0 || page >= p.num_blocks);
+            if (!is_v && __any_sync(kMask, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
+            if (page == -2 || bad) page = static_cast<int>(p.num_blocks);
+            for (int i = sp.i_lo; i < sp.n_tiles; ++i, ++it) {
+                const int s = it % NS;
+                if (lane == 0) {
+                    if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1u, p.status, abort_flag))
+                        stop = 1;
+                    else
+                        mbar_arrive_expect_tx(&full[s], kTile8Bytes);
+                }
+                stop = __shfl_sync(kMask, stop, 0);
+                if (stop) break;
+                // lane l < 8 loads page l of the tile: 16 rows of 128 bytes
+                const int pg = __shfl_sync(kMask, page, (i * kPagesPerTile + (lane & 7)) & 31);
+                if (lane < kPagesPerTile)   // K / V are read once: evict them first
+                    tma_load_4d_hint(ring + s * kTile8Bytes + lane * kBlockSize * 128, tm, 0, 0,
+                                     kh, pg, &full[s], policy);
+            }
+        }
+        // never leave the CTA with copies still landing in its shared memory
+        if (lane == 0 && (stop || *abort_flag)) {
+            for (uint32_t k = (it > static_cast<uint32_t>(NS) ? it - NS : 0); k < it; ++k) {
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&full[k % NS], (k / NS) & 1u))
+                    if (global_timer_ns() - t0 > kWaitLimitNs) break;
+            }
+        }
+    } else if (warp >= 7) {
+        // ------------------- V converters: E4M3 tile -> f16 tile, one row each -------------------
+        const int t = threadIdx.x - 7 * 32;       // token row of the tile
+        uint32_t it8 = 0, it16 = 0;
+        bool ok = true;
+        int b, kh, part;
+        for (int e = 0; ok && item8(p, pref, total, e, b, kh, part); ++e) {
+            const Span8 sp = span8(p, b, part);
+            for (int i = sp.i_lo; ok && i < sp.n_tiles; ++i, ++it8, ++it16) {
+                const int s8 = it8 % kV8Stages, s16 = it16 % kV16Stages;
+                ok = mbar_wait(&v8_full[s8], (it8 / kV8Stages) & 1, p.status, abort_flag) &&
+                     mbar_wait(&v16_empty[s16], ((it16 / kV16Stages) & 1) ^ 1u, p.status,
+                               abort_flag);
+                if (__any_sync(kMask, !ok)) {
+                    ok = false;
+                    break;
+                }
+                // rows outside [t_lo, n_tok) become zeros, whatever the pool held there
+                const int tok = i * kTok + t;
+                const bool valid = tok >= sp.t_lo && tok < sp.n_tok;
+                const uint8_t *src = smem + kOffV8 + s8 * kTile8Bytes + t * 128;
+                uint8_t *dst = smem + kOffV16 + s16 * kTile16Bytes + t * 128;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {             // dims 16u .. 16u + 15
+                    const uint4 raw = valid ? *reinterpret_cast<const uint4 *>(src + ((u ^ (t & 7)) << 4))
+                                            : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                    uint32_t h[8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * j])
+                            : "h"(static_cast<unsigned short>(w[j] & 0xffffu)));
+                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * j + 1])
+                            : "h"(static_cast<unsigned short>(w[j] >> 16)));
+                    }
+                    const int chunk = u >> 2, unit = (u & 3) * 2;   // 8 f16 dims per 16-byte unit
+                    uint8_t *row = dst + chunk * kTile16Chunk;
+                    *reinterpret_cast<uint4 *>(row + ((unit ^ (t & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+                    *reinterpret_cast<uint4 *>(row + (((unit + 1) ^ (t & 7)) << 4)) =
+                        make_uint4(h[4], h[5], h[6], h[7]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&v8_empty[s8]);
+                    mbar_arrive(&v16_full[s16]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // -------------------------------- MMA issuer --------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_f32(kTok, kN, 0, 0, false, false);   // E4M3 x E4M3
+            constexpr uint32_t idesc_o = idesc_f32(kHD, kN, 0, 0, true, false);     // f16 x f16
+            const uint64_t ring_k = smem_desc_sw128(smem_addr(smem + kOffK), 16, 1024);
+            const uint64_t ring_v = smem_desc_sw128(smem_addr(smem + kOffV16), kTile16Chunk, 1024);
+            const uint64_t q_desc = smem_desc_sw128(smem_addr(smem + kOffQ), 16, 1024);
+            const uint64_t p_desc = smem_desc_sw128(smem_addr(smem + kOffP), 16, 1024);
+            uint32_t kit = 0, vit = 0;
+            bool ok = true;
+            auto item_span = [&](int e) -> Span8 {
+                int b, kh, part;
+                if (!item8(p, pref, total, e, b, kh, part)) {
+                    Span8 none = {};
+                    none.n_tiles = -1;
+                    return none;
+                }
+                return span8(p, b, part);
+            };
+            // S^T = K Q^T for every tile of item e, into S buffer e % 2
+            auto issue_s = [&](int e, const Span8 &sp) {
+                const int x = e & 1;
+                const uint32_t use = e >> 1;
+                ok = ok && mbar_wait(&q_full[x], use & 1, p.status, abort_flag);
+                if (ok && e >= 2) ok = mbar_wait(&s_free[x], (use - 1) & 1, p.status, abort_flag);
+                if (!ok) return;
+                tc_fence_after_sync();
+                const uint64_t qd = q_desc + ((x * kQBytes) >> 4);
+                for (int i = sp.i_lo; i < sp.n_tiles && ok; ++i, ++kit) {
+                    const int s = kit % kKStages;
+                    ok = mbar_wait(&k_full[s], (kit / kKStages) & 1, p.status, abort_flag);
+                    if (!ok) return;
+                    tc_fence_after_sync();
+                    const uint64_t kd = ring_k + ((s * kTile8Bytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kHD / 32; ++kk)   // 32 one-byte dims per MMA
+                        mma_f8_ss(tmem + kTmS + x * 64 + i * kN, kd + ((kk * 32) >> 4),
+                                  qd + ((kk * 32) >> 4), idesc_s, kk > 0 ? 1u : 0u);
+                    tc_commit(&k_empty[s]);
+                }
+                if (!ok) return;
+                tc_commit(&s_full[x]);
+                tc_commit(&q_empty[x]);
+            };
+            // O^T = V^T P over the converted tiles of item e
+            auto issue_pv = [&](int e, const Span8 &sp) {
+                const int x = e & 1;
+                const uint32_t use = e >> 1;
+                ok = ok && mbar_wait(&p_full[x], use & 1, p.status, abort_flag);
+                if (ok && e >= 2) ok = mbar_wait(&o_free[x], (use - 1) & 1, p.status, abort_flag);
+                if (!ok) return;
+                tc_fence_after_sync();
+                for (int i = sp.i_lo; i < sp.n_tiles && ok; ++i, ++vit) {
+                    const int s = vit % kV16Stages;
+                    ok = mbar_wait(&v16_full[s], (vit / kV16Stages) & 1, p.status, abort_flag);
+                    if (!ok) return;
+                    tc_fence_after_sync();
+                    const uint64_t vd = ring_v + ((s * kTile16Bytes) >> 4);
+                    const uint64_t pd = p_desc + ((i * kPTile) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kTok / 16; ++kk)
+                        mma_bf16_ss(tmem + kTmO + x * kN, vd + ((kk * 16 * 128) >> 4),
+                                    pd + (((kk / 4) * kSmallChunk + (kk % 4) * 32) >> 4), idesc_o,
+                                    (i > sp.i_lo || kk > 0) ? 1u : 0u);
+                    tc_commit(&v16_empty[s]);
+                }
+                if (!ok) return;
+                tc_commit(&o_full[x]);
+            };
+            // the scores of item e + 1 are issued before the P.V of item e
+            Span8 cur = item_span(0);
+            if (cur.n_tiles > 0) issue_s(0, cur);
+            for (int e = 0; ok && cur.n_tiles > 0; ++e) {
+                const Span8 next = item_span(e + 1);
+                if (next.n_tiles > 0) issue_s(e + 1, next);
+                issue_pv(e, cur);
+                cur = next;
+            }
+            tc_commit(drain);   // never release TMEM / smem with MMAs in flight
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(drain, 0)) {
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(p.status, kStatusTimeout);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // --------------------------- softmax + epilogue ---------------------------
+        // Thread row (0..127) is TMEM lane `row`: token `row` of every tile for S^T,
+        // dim `row` for O^T.  The 4 warps always run the same barrier sequence.
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int sid = (warp - 2) * 32 + lane;          // 0..127 across the softmax warps
+        const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+        const float q_mul = p.scale_log2 * p.k_scale;    // log2 units, k_scale folded in
+        bool ok = true;
+        int b, kh, part;
+        // The per-head Q scales of an item, computed as the producer computes them, into
+        // qinv[e % 2]: item 0's here, item e + 1's while item e waits for its O^T (the
+        // item's last barrier publishes them).
+        auto q_scales = [&](int e, int bb, int kk) {
+            if (sid < 16 * G) {                              // warp-uniform
+                const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q) +
+                                          (static_cast<int64_t>(bb) * nq + kk * G) * kHD;
+                const float s = q_split_scale(head_max(__ldg(reinterpret_cast<const uint4 *>(qg) + sid)));
+                if ((lane & 15) == 0) qinv[(e & 1) * kN + (sid >> 4)] = 1.f / s;  // exact
+            }
+        };
+        if (item8(p, pref, total, 0, b, kh, part)) q_scales(0, b, kh);
+        named_barrier(1, 128);
+        for (int e = 0; item8(p, pref, total, e, b, kh, part); ++e) {
+            const Span8 sp = span8(p, b, part);
+            const int x = e & 1;
+            const uint32_t use = e >> 1;
+            const float *qi = qinv + x * kN;
+            float sc[kTiles][G];
+            bool got = mbar_wait(&s_full[x], use & 1, p.status, abort_flag);
+            got = !__any_sync(kMask, !got);
+            if (got) tc_fence_after_sync();
+#pragma unroll
+            for (int i = 0; i < kTiles; ++i) {
+                const bool tile = got && i >= sp.i_lo && i * kTok < sp.n_tok;
+                uint32_t v[16];
+                if (tile) {
+                    if constexpr (G == 8) {
+                        tmem_load_16(tmem + t_lane + kTmS + x * 64 + i * kN, v);
+                    } else {
+                        uint32_t (&v8)[8] = *reinterpret_cast<uint32_t (*)[8]>(v);
+                        tmem_load_8(tmem + t_lane + kTmS + x * 64 + i * kN, v8);
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < 16; ++g) v[g] = 0u;
+                }
+                const int tok = i * kTok + row;
+                const bool valid = tile && tok < sp.n_tok && tok >= sp.t_lo;
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    sc[i][g] = valid ? (__uint_as_float(v[g]) + __uint_as_float(v[G + g])) *
+                                           (qi[g] * q_mul)
+                                     : -INFINITY;
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[x]);
+            float *rm = red + quad * kN;
+            float *rl = red + 4 * kN + quad * kN;
+            float mx[G], sm[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float m = fmaxf(fmaxf(sc[0][g], sc[1][g]), fmaxf(sc[2][g], sc[3][g]));
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kMask, m, off));
+                mx[g] = m;
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) rm[g] = mx[g];
+            }
+            named_barrier(1, 128);
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                mx[g] = fmaxf(fmaxf(red[g], red[kN + g]), fmaxf(red[2 * kN + g], red[3 * kN + g]));
+            float pv[kTiles][G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float s = 0.f;
+#pragma unroll
+                for (int i = 0; i < kTiles; ++i) {
+                    pv[i][g] = sc[i][g] == -INFINITY ? 0.f : exp2f(sc[i][g] - mx[g]);
+                    s += pv[i][g];
+                }
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kMask, s, off);
+                sm[g] = s;
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) rl[g] = sm[g];
+            }
+            // P (f16), K-major by head, as the bf16 decode lays it out
+            uint8_t *pb = smem + kOffP + (row / 64) * kSmallChunk + (row % 8) * 2;
+#pragma unroll
+            for (int i = 0; i < kTiles; ++i)
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    *reinterpret_cast<__half *>(pb + i * kPTile + g * 128 +
+                                                ((((row % 64) / 8) ^ g) << 4)) =
+                        __float2half_rn(pv[i][g]);
+            fence_proxy_async_smem();
+            named_barrier(1, 128);   // also publishes the sums
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                sm[g] = red[4 * kN + g] + red[5 * kN + g] + red[6 * kN + g] + red[7 * kN + g];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[x]);
+            {
+                int b1, kh1, part1;
+                if (item8(p, pref, total, e + 1, b1, kh1, part1)) q_scales(e + 1, b1, kh1);
+            }
+            bool done = got && mbar_wait(&o_full[x], use & 1, p.status, abort_flag);
+            done = !__any_sync(kMask, !done);
+            uint32_t o[8];
+            if (done) {
+                tc_fence_after_sync();
+                tmem_load_8(tmem + t_lane + kTmO + x * kN, o);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[x]);
+            if (done) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const int64_t r = (static_cast<int64_t>(b) * nq + kh * G + g) * p.max_parts + part;
+                    p.part_o[r * kHD + row] = __uint_as_float(o[g]) / sm[g] * p.v_scale;
+                    if (row == 0) {
+                        p.part_m[r] = mx[g] * kLn2;
+                        p.part_l[r] = sm[g];
+                    }
+                }
+            }
+            ok = !named_barrier_or(1, 128, !(got && done));
+            if (!ok) break;
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int G>
+cudaError_t launch_tc8(const DecodeParams &p, cudaStream_t stream) {
+    DecodeTc8Params prm;
+    prm.d = p;
+    {
+        const cuuint64_t dims[4] = {kHD, kBlockSize, static_cast<cuuint64_t>(p.num_kv_heads),
+                                    static_cast<cuuint64_t>(p.num_blocks)};
+        const cuuint64_t str[3] = {static_cast<cuuint64_t>(p.s_token),
+                                   static_cast<cuuint64_t>(p.s_head),
+                                   static_cast<cuuint64_t>(p.s_block)};
+        const cuuint32_t box[4] = {128, kBlockSize, 1, 1};
+        if (!encode_tensor_map_u8(&prm.tm_k, p.k_cache, 4, dims, str, box) ||
+            !encode_tensor_map_u8(&prm.tm_v, p.v_cache, 4, dims, str, box))
+            return cudaErrorInvalidValue;
+    }
+    auto kern = decode_tc8_kernel<G>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    static int sms = 0;
+    if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 152;
+    const long long slots = static_cast<long long>(p.num_seqs) * p.num_kv_heads *
+                            active_partitions_cap(p.max_parts, p.window);
+    long long n = sms;
+    if (slots < n) n = slots;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n > 0 ? n : 1));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {&prm};
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(kern), args);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_tc8_supported(const DecodeParams &p, int head_dim) {
+    const int g = p.num_kv_heads > 0 ? p.num_q_heads / p.num_kv_heads : 0;
+    return p.kv_fp8 && head_dim == kHD && (g == 4 || g == 8) && p.num_seqs <= kMaxSeqs &&
+           p.s_token % 16 == 0 && p.s_head % 16 == 0 && p.s_block % 16 == 0 &&
+           (reinterpret_cast<uintptr_t>(p.k_cache) & 15) == 0 &&
+           (reinterpret_cast<uintptr_t>(p.v_cache) & 15) == 0 &&
+           (reinterpret_cast<uintptr_t>(p.q) & 15) == 0;
+}
+
+cudaError_t launch_decode_tc8(const DecodeParams &p, cudaStream_t stream) {
+    if (p.num_seqs == 0) return cudaSuccess;
+    switch (p.num_q_heads / p.num_kv_heads) {
+        case 4: return launch_tc8<4>(p, stream);
+        case 8: return launch_tc8<8>(p, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace pa

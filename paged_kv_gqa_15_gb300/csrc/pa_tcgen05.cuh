@@ -80,6 +80,32 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
 }
 
+// D[tmem] (+)= A[smem desc] x B[smem desc]; kind::f8f6f4 (8-bit float operands as the
+// instruction descriptor gives, fp32 accumulator, K = 32 per instruction).
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor with an fp32 accumulator and the given A / B formats: for
+// kind::f16 format 0 is f16 and 1 bf16; for kind::f8f6f4 format 0 is E4M3.
+__host__ __device__ constexpr uint32_t idesc_f32(int M, int N, uint32_t a_fmt, uint32_t b_fmt,
+                                                 bool a_mn, bool b_mn) {
+    return (1u << 4)                               // D format: f32
+           | (a_fmt << 7)                          // A format
+           | (b_fmt << 10)                         // B format
+           | ((a_mn ? 1u : 0u) << 15)              // A major
+           | ((b_mn ? 1u : 0u) << 16)              // B major
+           | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
+}
+static_assert(idesc_f32(128, 16, 1, 1, true, false) == idesc_bf16_f32(128, 16, true, false),
+              "idesc_f32 encodes the bf16 descriptor the same way");
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand whose swizzle
 // atoms (8 rows x 128 B) start on 1024-byte boundaries.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,

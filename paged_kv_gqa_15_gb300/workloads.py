@@ -111,6 +111,7 @@ class DecodeWorkload:
     split: bool = False
     slot_mapping: Optional[np.ndarray] = None  # int64 [B] when new_token_write
     window: int = 0               # sliding window in keys (0: none)
+    kv_fp8: bool = False          # the pools hold FP8 E4M3 codes (one byte per element)
 
     @property
     def batch(self):
@@ -137,7 +138,8 @@ class DecodeWorkload:
 
     def kv_bytes(self):
         """Algorithmic decode bytes: K and V of every visible token."""
-        return self.visible_tokens() * self.num_kv_heads * self.head_dim * 2 * 2
+        elem = 1 if self.kv_fp8 else 2
+        return self.visible_tokens() * self.num_kv_heads * self.head_dim * 2 * elem
 
     def tensors(self, device="cpu"):
         """q, k_cache, v_cache (and k_new, v_new if new_token_write) as bf16 tensors."""
@@ -155,13 +157,13 @@ class DecodeWorkload:
 
 def make_decode(name, seq_lens, num_q_heads, num_kv_heads, head_dim, seed,
                 block_size=BLOCK_SIZE, num_blocks=None, new_token_write=False, split=False,
-                max_blocks=None, window=0):
+                max_blocks=None, window=0, kv_fp8=False):
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, np.int32)
     bt, nb = assign_pages(seq_lens, block_size, rng, num_blocks=num_blocks,
                           max_blocks=max_blocks)
     w = DecodeWorkload(name, seq_lens, bt, nb, num_q_heads, num_kv_heads, head_dim,
-                       block_size, seed, new_token_write, split, window=window)
+                       block_size, seed, new_token_write, split, window=window, kv_fp8=kv_fp8)
     if new_token_write:
         w.slot_mapping = slots_for_positions(bt, np.maximum(seq_lens.astype(np.int64) - 1, 0),
                                              block_size)
@@ -310,6 +312,22 @@ def chunked_paged_prefill():
                         seed=1004, paged=True, chunk_write=True)
 
 
+def llama8b_decode_fp8():
+    """llama8b_decode over an FP8 E4M3 cache (the same sequences and pages)."""
+    rng = np.random.default_rng(1001)
+    lens = rng.integers(512, 4096, size=64, endpoint=True)
+    return make_decode("llama8b_decode_fp8_b64_h32kv8_d128", lens, 32, 8, 128, seed=1001,
+                       new_token_write=True, split=True, kv_fp8=True)
+
+
+def long_context_decode_fp8():
+    """long_context_decode over an FP8 E4M3 cache (the same sequences and pages)."""
+    rng = np.random.default_rng(1002)
+    lens = rng.integers(32768, 131072, size=8, endpoint=True)
+    return make_decode("long_split_decode_fp8_b8_h32kv8_d128", lens, 32, 8, 128, seed=1002,
+                       split=True, kv_fp8=True)
+
+
 def window_decode():
     """Sliding-window decode shaped like Mistral-7B (32 q / 8 kv heads, hd 128, a
     4096-key window): batch 32, seq_lens U[8192, 32768], split-KV."""
@@ -335,5 +353,7 @@ WORKLOADS = {
     "ragged_prefill": ragged_prefill,
     "chunked_paged_prefill": chunked_paged_prefill,
     "window_decode": window_decode,
+    "llama8b_decode_fp8": llama8b_decode_fp8,
+    "long_context_decode_fp8": long_context_decode_fp8,
     "window_prefill": window_prefill,
 }

@@ -155,12 +155,31 @@ def test_fp8_partials_match_oracle_partitions():
     po, pm, pl = pa.decode_split_workspace_views(ws, w.batch, 32, 128, L)
     m, l, o = oracle.decode_partitions(q, kc, vc, w.block_tables, w.seq_lens, 8, 16, w.scale, P,
                                        kv_fp8=True, k_scale=KS, v_scale=VS)
+    # The tensor-core fp8 path multiplies K by q carried as two E4M3 codes per element
+    # (hi = e4m3(q s), lo = e4m3(q s - hi), s a power of two with max|q s| in [128, 256)),
+    # which is q to within |dq| <= 2^-8 |q| + 2^-17 max|q|.  A score then moves by at most
+    # db_j = sm_scale * sum_d |dq_d| |k_jd|; m by the largest db_j of the partition, l by a
+    # factor within exp(+-2 db), and o (a weighted mean of V) by 2 db max|V|, plus P's f16
+    # rounding (2^-11 per weight).
+    qf = W.bits_to_float(q).astype(np.float64)
+    table = np.array([float(torch.tensor([c], dtype=torch.uint8).view(torch.float8_e4m3fn)
+                            .float()) if c & 0x7F != 0x7F else 0.0 for c in range(256)])
+    kf = table[kc] * KS                        # NaN codes sit only in unread stale rows
+    vmax = float(np.abs(table[vc] * VS).max())
     for b, Lb in enumerate(w.seq_lens):
         n = (int(Lb) + 511) // 512
         gm, gl, go = (x[b, :, :n].cpu().numpy().astype(np.float64) for x in (pm, pl, po))
-        np.testing.assert_allclose(gm, m[b, :, :n], atol=1e-4, rtol=0)
-        np.testing.assert_allclose(gl, l[b, :, :n], rtol=1e-4, atol=0)
-        np.testing.assert_allclose(go, o[b, :, :n], atol=2.0 ** -9 * 8 + 1e-4, rtol=0)
+        for h in range(32):
+            kh = h // 4
+            dq = 2.0 ** -8 * np.abs(qf[b, h]) + 2.0 ** -17 * np.abs(qf[b, h]).max()
+            for pidx in range(n):
+                j0, j1 = pidx * 512, min(Lb, pidx * 512 + 512)
+                rows = np.array([kf[w.block_tables[b, j // 16], kh, j % 16] for j in range(j0, j1)])
+                db = w.scale * (np.abs(rows) @ dq).max()
+                assert abs(gm[h, pidx] - m[b, h, pidx]) <= db + 1e-4, (b, h, pidx)
+                assert abs(gl[h, pidx] / l[b, h, pidx] - 1) <= np.expm1(2 * db) + 1e-4, (b, h, pidx)
+                np.testing.assert_allclose(go[h, pidx], o[b, h, pidx],
+                                           atol=(2 * db + 2.0 ** -10) * vmax + 1e-5, rtol=0)
     assert_close_bf16(out, ref, what="fp8 split")
 
 
