@@ -18,8 +18,10 @@
 //    tile into f16 (exact for every E4M3 value) in the 128-byte-swizzled layout of a
 //    TMA-loaded 16-bit tile, writing zeros for rows outside the partition's tokens; P
 //    is f16 and the MMA is kind::f16.  k_scale scales the scores, v_scale the outputs.
-//  * Warps: 0 Q and K producer, 1 MMA issuer, 2-5 softmax and epilogue, 6 V producer,
-//    7-10 V converters.  The softmax warps compute the per-head Q scale themselves
+//  * Warps: 0 Q and K producer, 1 score-MMA issuer, 2-5 softmax and epilogue, 6 V
+//    producer, 7-10 V converters, 11 P.V-MMA issuer.  With two issuing threads the
+//    score MMAs of later items never queue behind the P.V of an item whose softmax is
+//    still running (tcgen05.commit tracks each thread's own MMAs).  The softmax warps compute the per-head Q scale themselves
 //    (the same function of q as the producer), so no scale crosses between warps.
 //    Every wait is bounded.
 #include <cuda.h>
@@ -38,7 +40,7 @@ constexpr int kTok = 128;                      // tokens per tile (MMA M of S^T)
 constexpr int kTiles = kPartition / kTok;      // tiles per partition
 constexpr int kPagesPerTile = kTok / kBlockSize;
 constexpr int kN = 16;                         // MMA N: G hi and G lo rows of Q, padded
-constexpr int kThreads = 352;                  // 11 warps
+constexpr int kThreads = 384;                  // 12 warps
 constexpr int kKStages = 4;                    // fp8 K tile ring
 constexpr int kV8Stages = 4;                   // fp8 V tile ring
 constexpr int kV16Stages = 2;                  // converted f16 V tile ring
@@ -63,7 +65,7 @@ constexpr uint32_t kSmem = kOffBar + 512 + 1024;                 // + realignmen
 constexpr uint32_t kTmemCols = 256;            // S: 2 x 4 tiles x 16; O: 2 x 16
 constexpr uint32_t kTmS = 0, kTmO = 128;
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-static_assert((2 * (kKStages + kV8Stages + kV16Stages) + 17) * 8 <= 512, "barriers fit");
+static_assert((2 * (kKStages + kV8Stages + kV16Stages) + 18) * 8 <= 512, "barriers fit");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms on 1 KB boundaries");
 
 struct DecodeTc8Params {
@@ -181,9 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *p_full = s_free + 2;                 // [2] P written (4 arrivals)
     uint64_t *o_full = p_full + 2;                 // [2] O^T done (commit)
     uint64_t *o_free = o_full + 2;                 // [2] epilogue has read O^T (4 arrivals)
-    uint64_t *drain = o_free + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(drain + 2);
+    uint64_t *drain = o_free + 2;                  // [2] S issuer, P.V issuer
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(drain + 3);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -220,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&o_full[x], 1);
             mbar_init(&o_free[x], 4);
         }
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -360,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (global_timer_ns() - t0 > kWaitLimitNs) break;
             }
         }
-    } else if (warp >= 7) {
+    } else if (warp >= 7 && warp <= 10) {
         // ------------------- V converters: E4M3 tile -> f16 tile, one row each -------------------
         const int t = threadIdx.x - 7 * 32;       // token row of the tile
         uint32_t it8 = 0, it16 = 0;
@@ -409,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // -------------------------------- MMA issuer --------------------------------
+    } else if (warp == 1 || warp == 11) {
+        // ------------- MMA issuers: warp 1 the scores, warp 11 the P.V -------------
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f32(kTok, kN, 0, 0, false, false);   // E4M3 x E4M3
             constexpr uint32_t idesc_o = idesc_f32(kHD, kN, 0, 0, true, false);     // f16 x f16
@@ -479,18 +482,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) return;
                 tc_commit(&o_full[x]);
             };
-            // the scores of item e + 1 are issued before the P.V of item e
-            Span8 cur = item_span(0);
-            if (cur.n_tiles > 0) issue_s(0, cur);
-            for (int e = 0; ok && cur.n_tiles > 0; ++e) {
-                const Span8 next = item_span(e + 1);
-                if (next.n_tiles > 0) issue_s(e + 1, next);
-                issue_pv(e, cur);
-                cur = next;
+            // two issuing threads: the scores of later items never queue behind the P.V
+            // of an item whose softmax is still running
+            for (int e = 0; ok; ++e) {
+                const Span8 cur = item_span(e);
+                if (cur.n_tiles <= 0) break;
+                if (warp == 1) issue_s(e, cur); else issue_pv(e, cur);
             }
-            tc_commit(drain);   // never release TMEM / smem with MMAs in flight
+            uint64_t *my_drain = &drain[warp == 1 ? 0 : 1];
+            tc_commit(my_drain);   // never release TMEM / smem with MMAs in flight
             const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(drain, 0)) {
+            while (!mbar_try_wait(my_drain, 0)) {
                 if (global_timer_ns() - t0 > kWaitLimitNs) {
                     atomicOr(p.status, kStatusTimeout);
                     break;
