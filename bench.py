@@ -43,13 +43,17 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # for the source file hash they were measured on (otherwise reported as null).
 TRAFFIC = {
     # ncu capture of one decode_tc_kernel<4> launch on the Llama-8B decode workload:
-    # dram__bytes_read.sum 568.32 MB + dram__bytes_write.sum 5.33 MB
+    # dram__bytes_read.sum 568.32 MB + dram__bytes_write.sum 5.44 MB
     "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
-        "src": "a4b0745b68763b53", "bytes_per_launch": 573654784},
+        "src": "63dff5344a34bf6e", "bytes_per_launch": 573760768},
     # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
-    # causal prefill: dram__bytes_read.sum 297.11 MB + dram__bytes_write.sum 109.05 MB
+    # causal prefill: dram__bytes_read.sum 295.56 MB + dram__bytes_write.sum 108.80 MB
     "ragged_prefill:ragged_prefill_r16_h32kv8_d128": {
-        "src": "0b6e207836ee269d", "bytes_per_launch": 406167040},
+        "src": "f54cff3896e5ae59", "bytes_per_launch": 404355072},
+    # ncu capture of one decode_tc8_kernel<4> launch on the Llama-8B decode workload over
+    # an FP8 cache: dram__bytes_read.sum 284.47 MB + dram__bytes_write.sum 4.59 MB
+    "decode_partitions:llama8b_decode_fp8_b64_h32kv8_d128": {
+        "src": "b8bee7ea1167d865", "bytes_per_launch": 289066240},
 }
 
 

@@ -26,7 +26,10 @@
 //    S, P and O are double-buffered across items.  K and V tiles stream through
 //    separate rings, each filled by its own producer warp: an item's V tiles wait
 //    in their ring for its softmax while the next item's K tiles (and score MMAs)
-//    go ahead, so HBM keeps streaming through the softmax.  Every wait is bounded.
+//    go ahead, so HBM keeps streaming through the softmax.  Two threads issue the
+//    MMAs -- warp 1 the scores, warp 7 the P.V (tcgen05.commit tracks each thread's
+//    own MMAs) -- so the score MMAs of later items never queue behind the P.V of an
+//    item whose softmax is still running.  Every wait is bounded.
 //  * Sliding window (keys j >= L - window): the item list holds only partitions
 //    that reach into the window; in the one holding L - window, tiles wholly before
 //    it are skipped, pages before it inside its first tile are read as zero boxes
@@ -46,7 +49,7 @@ constexpr int kTok = 128;                      // tokens per tile (MMA M of S^T)
 constexpr int kTiles = kPartition / kTok;      // tiles per partition
 constexpr int kPagesPerTile = kTok / kBlockSize;
 constexpr int kN = 16;                         // MMA N: query heads, zero-padded
-constexpr int kThreadsTc = 224;                // K producer, MMA, 4 softmax, V producer
+constexpr int kThreadsTc = 256;                // K producer, MMA, 4 softmax, V producer, P.V MMA
 constexpr int kKStages = 2;                    // K tile ring
 constexpr int kVStages = 4;                    // V tile ring: a whole partition
 constexpr uint32_t kTileChunk = kTok * 128;    // one 64-column chunk of a tile
@@ -155,9 +158,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     uint64_t *p_full = bars + 20;
     uint64_t *o_full = bars + 22;
     uint64_t *o_free = bars + 24;
-    uint64_t *drain = bars + 26;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 27);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 28);
+    uint64_t *drain = bars + 26;   // [2] S issuer, P.V issuer
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 28);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 29);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -191,7 +194,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             mbar_init(&o_full[b], 1);
             mbar_init(&o_free[b], 4);
         }
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -293,8 +297,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     if (global_timer_ns() - t0 > kWaitLimitNs) break;
             }
         }
-    } else if (warp == 1) {
-        // -------------------------------- MMA issuer --------------------------------
+    } else if (warp == 1 || warp == 7) {
+        // ------------- MMA issuers: warp 1 the scores, warp 7 the P.V -------------
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kTok, kN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kHD, kN, true, false);
@@ -399,17 +403,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             // Software pipeline: the scores of item e + 1 are issued before the P.V of
             // item e, so they run while item e's softmax does and the K ring keeps
             // draining (the S buffers alternate; s_free guards their reuse).
-            TcSpan cur = item_span(0);
-            if (cur.n_tiles > 0) issue_s(0, cur);
-            for (int e = 0; ok && cur.n_tiles > 0; ++e) {
-                const TcSpan next = item_span(e + 1);
-                if (next.n_tiles > 0) issue_s(e + 1, next);
-                issue_pv(e, cur);
-                cur = next;
+            for (int e = 0; ok; ++e) {
+                const TcSpan cur = item_span(e);
+                if (cur.n_tiles <= 0) break;
+                if (warp == 1) issue_s(e, cur); else issue_pv(e, cur);
             }
-            tc_commit(drain);   // never release TMEM / smem with MMAs in flight
+            uint64_t *my_drain = &drain[warp == 1 ? 0 : 1];
+            tc_commit(my_drain);   // never release TMEM / smem with MMAs in flight
             const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(drain, 0)) {
+            while (!mbar_try_wait(my_drain, 0)) {
                 if (global_timer_ns() - t0 > kWaitLimitNs) {
                     atomicOr(p.status, kStatusTimeout);
                     break;

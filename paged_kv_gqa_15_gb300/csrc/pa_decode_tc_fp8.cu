@@ -21,9 +21,11 @@
 //  * Warps: 0 Q and K producer, 1 score-MMA issuer, 2-5 softmax and epilogue, 6 V
 //    producer, 7-10 V converters, 11 P.V-MMA issuer.  With two issuing threads the
 //    score MMAs of later items never queue behind the P.V of an item whose softmax is
-//    still running (tcgen05.commit tracks each thread's own MMAs).  The softmax warps compute the per-head Q scale themselves
-//    (the same function of q as the producer), so no scale crosses between warps.
-//    Every wait is bounded.
+//    still running (tcgen05.commit tracks each thread's own MMAs).  P is double
+//    buffered and each item's epilogue waits until the next item's P is written, so
+//    one item's P.V overlaps the next item's softmax.  The softmax warps compute the
+//    per-head Q scale themselves (the same function of q as the producer), so no
+//    scale crosses between warps.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -42,7 +44,7 @@ constexpr int kPagesPerTile = kTok / kBlockSize;
 constexpr int kN = 16;                         // MMA N: G hi and G lo rows of Q, padded
 constexpr int kThreads = 384;                  // 12 warps
 constexpr int kKStages = 4;                    // fp8 K tile ring
-constexpr int kV8Stages = 4;                   // fp8 V tile ring
+constexpr int kV8Stages = 3;                   // fp8 V tile ring
 constexpr int kV16Stages = 2;                  // converted f16 V tile ring
 constexpr uint32_t kTile8Bytes = kTok * 128;   // 128 tokens x 128 one-byte dims
 constexpr uint32_t kTile16Chunk = kTok * 128;  // one 64-dim chunk of a 16-bit tile
@@ -55,8 +57,8 @@ constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV8 = kOffK + kKStages * kTile8Bytes;
 constexpr uint32_t kOffV16 = kOffV8 + kV8Stages * kTile8Bytes;
 constexpr uint32_t kOffQ = kOffV16 + kV16Stages * kTile16Bytes;   // two Q buffers
-constexpr uint32_t kOffP = kOffQ + 2 * kQBytes;                  // one P buffer (see below)
-constexpr uint32_t kOffRed = kOffP + kPBytes;                    // float [2][4 warps][16]
+constexpr uint32_t kOffP = kOffQ + 2 * kQBytes;                  // two P buffers
+constexpr uint32_t kOffRed = kOffP + 2 * kPBytes;                // float [2][4 warps][16]
 constexpr uint32_t kOffQinv = kOffRed + 2 * 4 * kN * 4;          // float [2][16]
 constexpr uint32_t kOffPref = kOffQinv + 2 * kN * 4;             // int [MAXB + 1]
 constexpr int kMaxSeqs = 2048;
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 0) pref[0] = 0;
     // Q rows 2G .. 15 and P rows G .. 15 stay zero (padding of the MMA's N)
-    for (uint32_t i = threadIdx.x; i < (2 * kQBytes + kPBytes) / 16; i += kThreads)
+    for (uint32_t i = threadIdx.x; i < (2 * kQBytes + 2 * kPBytes) / 16; i += kThreads)
         reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKStages; ++s) {
@@ -471,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) return;
                     tc_fence_after_sync();
                     const uint64_t vd = ring_v + ((s * kTile16Bytes) >> 4);
-                    const uint64_t pd = p_desc + ((i * kPTile) >> 4);
+                    const uint64_t pd = p_desc + ((x * kPBytes + i * kPTile) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kTok / 16; ++kk)
                         mma_bf16_ss(tmem + kTmO + x * kN, vd + ((kk * 16 * 128) >> 4),
@@ -524,6 +526,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         if (item8(p, pref, total, 0, b, kh, part)) q_scales(0, b, kh);
         named_barrier(1, 128);
+        // The epilogue of an item (O^T from TMEM, normalised, to the partials) is deferred
+        // until the next item's P is written, so that the P.V of one item overlaps the
+        // softmax of the next; its inputs wait in these registers.
+        bool have_prev = false, prev_got = false;
+        int prev_b = 0, prev_kh = 0, prev_part = 0, prev_x = 0;
+        uint32_t prev_use = 0;
+        float prev_sm[G], prev_mx[G];
+        auto epilogue = [&]() -> bool {
+            bool done = prev_got && mbar_wait(&o_full[prev_x], prev_use & 1, p.status, abort_flag);
+            done = !__any_sync(kMask, !done);
+            uint32_t o[8];
+            if (done) {
+                tc_fence_after_sync();
+                tmem_load_8(tmem + t_lane + kTmO + prev_x * kN, o);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[prev_x]);
+            if (done) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const int64_t r =
+                        (static_cast<int64_t>(prev_b) * nq + prev_kh * G + g) * p.max_parts + prev_part;
+                    p.part_o[r * kHD + row] = __uint_as_float(o[g]) / prev_sm[g] * p.v_scale;
+                    if (row == 0) {
+                        p.part_m[r] = prev_mx[g] * kLn2;
+                        p.part_l[r] = prev_sm[g];
+                    }
+                }
+            }
+            return done;
+        };
         for (int e = 0; item8(p, pref, total, e, b, kh, part); ++e) {
             const Span8 sp = span8(p, b, part);
             const int x = e & 1;
@@ -594,8 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int g = 0; g < G; ++g) rl[g] = sm[g];
             }
-            // P (f16), K-major by head, as the bf16 decode lays it out
-            uint8_t *pb = smem + kOffP + (row / 64) * kSmallChunk + (row % 8) * 2;
+            // P (f16) into buffer e % 2, K-major by head, as the bf16 decode lays it out;
+            // the P.V of item e - 2 that read this buffer finished before that item's
+            // epilogue, which ran in the previous iteration
+            uint8_t *pb = smem + kOffP + x * kPBytes + (row / 64) * kSmallChunk + (row % 8) * 2;
 #pragma unroll
             for (int i = 0; i < kTiles; ++i)
 #pragma unroll
@@ -614,30 +650,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int b1, kh1, part1;
                 if (item8(p, pref, total, e + 1, b1, kh1, part1)) q_scales(e + 1, b1, kh1);
             }
-            bool done = got && mbar_wait(&o_full[x], use & 1, p.status, abort_flag);
-            done = !__any_sync(kMask, !done);
-            uint32_t o[8];
-            if (done) {
-                tc_fence_after_sync();
-                tmem_load_8(tmem + t_lane + kTmO + x * kN, o);
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[x]);
-            if (done) {
+            // item e - 1's epilogue runs now, while the P.V of item e can start
+            const bool done = !have_prev || epilogue();
+            have_prev = true;
+            prev_b = b;
+            prev_kh = kh;
+            prev_part = part;
+            prev_x = x;
+            prev_use = use;
+            prev_got = got;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const int64_t r = (static_cast<int64_t>(b) * nq + kh * G + g) * p.max_parts + part;
-                    p.part_o[r * kHD + row] = __uint_as_float(o[g]) / sm[g] * p.v_scale;
-                    if (row == 0) {
-                        p.part_m[r] = mx[g] * kLn2;
-                        p.part_l[r] = sm[g];
-                    }
-                }
+            for (int g = 0; g < G; ++g) {
+                prev_sm[g] = sm[g];
+                prev_mx[g] = mx[g];
             }
             ok = !named_barrier_or(1, 128, !(got && done));
             if (!ok) break;
         }
+        if (ok && have_prev) epilogue();
     }
     tc_fence_before_sync();
     __syncthreads();

@@ -72,3 +72,27 @@ def test_reference_arm_prints_one_json_line():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_window_and_fp8_accounting():
+    """Algorithmic work of the windowed and fp8 workloads: visible (query, key) pairs
+    counted against a brute-force mask, and fp8 decode bytes half of bf16."""
+    import numpy as np
+    from paged_kv_gqa_15_gb300 import workloads as W
+    for causal in (True, False):
+        for window in (0, 1, 5, 40):
+            w = W.make_prefill("acc", [3, 17, 40], [9, 17, 60], 4, 2, 64, seed=1, causal=causal,
+                               window=window)
+            n = 0
+            for qo, kv in zip(w.qo_lens, w.kv_lens):
+                for i in range(qo):
+                    pos = i + kv - qo
+                    for j in range(kv):
+                        ok = (j <= pos or not causal) and (window <= 0 or j > pos - window)
+                        n += ok
+            assert w.visible_pairs() == n, (causal, window)
+    a = W.make_decode("b", [100, 7000], 32, 8, 128, seed=2)
+    f = W.make_decode("f", [100, 7000], 32, 8, 128, seed=2, kv_fp8=True)
+    assert f.kv_bytes() * 2 == a.kv_bytes()
+    wdw = W.make_decode("w", [100, 7000], 32, 8, 128, seed=2, window=4096)
+    assert wdw.visible_tokens() == 100 + 4096
