@@ -91,20 +91,41 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(const __grid_constant__
     const int p0 = window_start(L, p.window) / kPartition;
     const int np = (L + kPartition - 1) / kPartition - p0;   // <= 32 for this kernel
     const int64_t row0 = (static_cast<int64_t>(b) * nq + h) * p.max_parts + p0;
-    const float mi = lane < np ? p.part_m[row0 + lane] : -INFINITY;
+    // Every load is issued before any result is needed: m_p and l_p of partition `lane`,
+    // and the partial outputs of the first kChunk partitions, so the merge costs one
+    // memory round trip rather than one per dependent step.
+    constexpr int kChunk = 8;
+    const bool mine = lane < np;
+    const float mi = mine ? p.part_m[row0 + lane] : -INFINITY;
+    const float li = mine ? p.part_l[row0 + lane] : 0.f;
+    float2 ov[kChunk][DPL / 2];
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i)
+#pragma unroll
+        for (int d = 0; d < DPL; d += 2)
+            ov[i][d / 2] = i < np ? *reinterpret_cast<const float2 *>(
+                                        p.part_o + (row0 + i) * HD + lane * DPL + d)
+                                  : make_float2(0.f, 0.f);
     float M = mi;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    const float wi = (lane < np && mi != -INFINITY) ? p.part_l[row0 + lane] * exp2f((mi - M) * kLog2e)
-                                                     : 0.f;
+    const float wi = (mine && mi != -INFINITY) ? li * exp2f((mi - M) * kLog2e) : 0.f;
     float W = wi;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) W += __shfl_xor_sync(kFull, W, off);
     float acc[DPL];
 #pragma unroll
     for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < np; ++i) {
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+        const float w = __shfl_sync(kFull, wi, i);
+#pragma unroll
+        for (int d = 0; d < DPL; d += 2) {
+            acc[d] = fmaf(w, ov[i][d / 2].x, acc[d]);
+            acc[d + 1] = fmaf(w, ov[i][d / 2].y, acc[d + 1]);
+        }
+    }
+    for (int i = kChunk; i < np; ++i) {           // more than kChunk partitions
         const float w = __shfl_sync(kFull, wi, i);
         const float *o = p.part_o + (row0 + i) * HD + lane * DPL;
 #pragma unroll
