@@ -266,10 +266,10 @@ def flush_l2(stream, device):
 def time_steps(step, steps, warmup, stream, device, labels, flush=False):
     """Warm up, then time exactly `steps` steps with CUDA events on `stream`.
     Without flush the step time comes from one pass with events only around the whole
-    loop (nothing between a step's kernels, so back-to-back launches may overlap as in
-    use); a second pass of `steps` steps with an event after every kernel gives the
-    per-kernel times.  With flush, L2 is flushed before every step outside the timed
-    intervals and the step time is the sum of its kernels' intervals.
+    loop; with flush, L2 is flushed before every step, outside the timed intervals, and
+    each step is timed on its own between two events.  Either way no event sits between
+    a step's kernels, so the dependent launches overlap as in use.  A second pass of
+    `steps` steps with an event after every kernel gives the per-kernel times.
     Returns (ms per step, {label: avg ms}, launches per timed pass)."""
     import torch.distributed as dist
     for _ in range(warmup):
@@ -280,7 +280,6 @@ def time_steps(step, steps, warmup, stream, device, labels, flush=False):
     if dist.is_available() and dist.is_initialized():
         dist.barrier()
     torch.cuda.synchronize()
-    ms_whole = None
     if not flush:
         start = _ev(stream)
         for _ in range(steps):
@@ -288,6 +287,15 @@ def time_steps(step, steps, warmup, stream, device, labels, flush=False):
         end = _ev(stream)
         torch.cuda.synchronize()
         ms_whole = start.elapsed_time(end) / steps
+    else:
+        spans = []
+        for _ in range(steps):
+            flush_l2(stream, device)
+            a = _ev(stream)
+            step(None)
+            spans.append((a, _ev(stream)))
+        torch.cuda.synchronize()
+        ms_whole = sum(a.elapsed_time(b) for a, b in spans) / steps
     all_evs = []
     launches = 0
     for _ in range(steps):
@@ -304,8 +312,7 @@ def time_steps(step, steps, warmup, stream, device, labels, flush=False):
         for i, l in enumerate(labels):
             per[l] += evs[i].elapsed_time(evs[i + 1])
     per = {l: v / steps for l, v in per.items()}
-    ms = sum(per.values()) if flush else ms_whole
-    return ms, per, launches
+    return ms_whole, per, launches
 
 
 def decode_footprint(w):

@@ -515,16 +515,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         int b, kh, part;
         // The per-head Q scales of an item, computed as the producer computes them, into
         // qinv[e % 2]: item 0's here, item e + 1's while item e waits for its O^T (the
-        // item's last barrier publishes them).
-        auto q_scales = [&](int e, int bb, int kk) {
+        // item's last barrier publishes them).  Thread sid < 16 G holds one 16-byte chunk
+        // of q, loaded two items ahead so that the load's latency stays off this chain.
+        auto q_chunk = [&](int e) -> uint4 {
+            int bb, kk, pp;
+            if (sid >= 16 * G || !item8(p, pref, total, e, bb, kk, pp)) return make_uint4(0u, 0u, 0u, 0u);
+            const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q) +
+                                      (static_cast<int64_t>(bb) * nq + kk * G) * kHD;
+            return __ldg(reinterpret_cast<const uint4 *>(qg) + sid);
+        };
+        auto q_scales = [&](int e, const uint4 &raw) {
             if (sid < 16 * G) {                              // warp-uniform
-                const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q) +
-                                          (static_cast<int64_t>(bb) * nq + kk * G) * kHD;
-                const float s = q_split_scale(head_max(__ldg(reinterpret_cast<const uint4 *>(qg) + sid)));
+                const float s = q_split_scale(head_max(raw));
                 if ((lane & 15) == 0) qinv[(e & 1) * kN + (sid >> 4)] = 1.f / s;  // exact
             }
         };
-        if (item8(p, pref, total, 0, b, kh, part)) q_scales(0, b, kh);
+        q_scales(0, q_chunk(0));
+        uint4 q_ahead = q_chunk(1);
         named_barrier(1, 128);
         // The epilogue of an item (O^T from TMEM, normalised, to the partials) is deferred
         // until the next item's P is written, so that the P.V of one item overlaps the
@@ -646,10 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm[g] = red[4 * kN + g] + red[5 * kN + g] + red[6 * kN + g] + red[7 * kN + g];
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[x]);
-            {
-                int b1, kh1, part1;
-                if (item8(p, pref, total, e + 1, b1, kh1, part1)) q_scales(e + 1, b1, kh1);
-            }
+            q_scales(e + 1, q_ahead);   // unused past the last item
+            q_ahead = q_chunk(e + 2);
             // item e - 1's epilogue runs now, while the P.V of item e can start
             const bool done = !have_prev || epilogue();
             have_prev = true;
