@@ -18,14 +18,15 @@
 //    tile into f16 (exact for every E4M3 value) in the 128-byte-swizzled layout of a
 //    TMA-loaded 16-bit tile, writing zeros for rows outside the partition's tokens; P
 //    is f16 and the MMA is kind::f16.  k_scale scales the scores, v_scale the outputs.
-//  * Warps: 0 Q and K producer, 1 score-MMA issuer, 2-5 softmax and epilogue, 6 V
+//  * Warps: 0 K producer, 1 score-MMA issuer, 2-5 softmax, Q rows and epilogue, 6 V
 //    producer, 7-10 V converters, 11 P.V-MMA issuer.  With two issuing threads the
 //    score MMAs of later items never queue behind the P.V of an item whose softmax is
 //    still running (tcgen05.commit tracks each thread's own MMAs).  P is double
 //    buffered and each item's epilogue waits until the next item's P is written, so
-//    one item's P.V overlaps the next item's softmax.  The softmax warps compute the
-//    per-head Q scale themselves (the same function of q as the producer), so no
-//    scale crosses between warps.  Every wait is bounded.
+//    one item's P.V overlaps the next item's softmax.  The softmax warps also split q
+//    into the Q rows, two items ahead, so the K producer does nothing but stream
+//    tiles: with the split on the producer, that warp's serial work per item set the
+//    whole kernel's pace.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -67,7 +68,7 @@ constexpr uint32_t kSmem = kOffBar + 512 + 1024;                 // + realignmen
 constexpr uint32_t kTmemCols = 256;            // S: 2 x 4 tiles x 16; O: 2 x 16
 constexpr uint32_t kTmS = 0, kTmO = 128;
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-static_assert((2 * (kKStages + kV8Stages + kV16Stages) + 18) * 8 <= 512, "barriers fit");
+static_assert((2 * (kKStages + kV8Stages + kV16Stages) + 16) * 8 <= 512, "barriers fit");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms on 1 KB boundaries");
 
 struct DecodeTc8Params {
@@ -160,6 +161,35 @@ __device__ __forceinline__ uint16_t e4m3x2(float x1, float x0) {
     return h;
 }
 
+// Chunk c (head c / 16, dims (c % 16) * 8 .. + 7) of one item's q, already scaled by s,
+// as E4M3 hi / lo codes into the Q rows at qb: row g = hi of head g, row G + g its lo;
+// the bytes of each 128-byte row are swizzled in 16-byte units by row % 8.
+template <int G>
+__device__ __forceinline__ void store_q_split(uint8_t *qb, int c, const uint4 &raw, float s) {
+    float f[8];
+    unpack_bf16x8(raw, f);
+    uint32_t hw[2], lw[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint16_t hp[2], lp[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float a0 = f[4 * h + 2 * j] * s, a1 = f[4 * h + 2 * j + 1] * s;
+            hp[j] = e4m3x2(a1, a0);
+            const float2 back = e4m3x2_to_float2(hp[j]);
+            lp[j] = e4m3x2(a1 - back.y, a0 - back.x);
+        }
+        hw[h] = hp[0] | (static_cast<uint32_t>(hp[1]) << 16);
+        lw[h] = lp[0] | (static_cast<uint32_t>(lp[1]) << 16);
+    }
+    const int g = c >> 4, d0 = (c & 15) * 8;
+    const int rh = g, rl = G + g;
+    *reinterpret_cast<uint2 *>(qb + rh * 128 + (((d0 >> 4) ^ (rh & 7)) << 4) + (d0 & 15)) =
+        make_uint2(hw[0], hw[1]);
+    *reinterpret_cast<uint2 *>(qb + rl * 128 + (((d0 >> 4) ^ (rl & 7)) << 4) + (d0 & 15)) =
+        make_uint2(lw[0], lw[1]);
+}
+
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc8_kernel(const __grid_constant__ DecodeTc8Params prm) {
@@ -178,9 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *v8_empty = v8_full + kV8Stages;      // the converters have read it (4 arrivals)
     uint64_t *v16_full = v8_empty + kV8Stages;     // f16 V tile written (4 arrivals)
     uint64_t *v16_empty = v16_full + kV16Stages;   // its P.V MMAs are done (commit)
-    uint64_t *q_full = v16_empty + kV16Stages;     // [2] Q rows written
-    uint64_t *q_empty = q_full + 2;                // [2] the item's score MMAs are done
-    uint64_t *s_full = q_empty + 2;                // [2] S^T of all the item's tiles (commit)
+    uint64_t *q_full = v16_empty + kV16Stages;     // [2] Q rows written (4 arrivals)
+    uint64_t *s_full = q_full + 2;                 // [2] S^T of all the item's tiles (commit)
     uint64_t *s_free = s_full + 2;                 // [2] softmax has read S^T (4 arrivals)
     uint64_t *p_full = s_free + 2;                 // [2] P written (4 arrivals)
     uint64_t *o_full = p_full + 2;                 // [2] O^T done (commit)
@@ -216,8 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&v16_empty[s], 1);
         }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(&q_full[x], 1);
-            mbar_init(&q_empty[x], 1);
+            mbar_init(&q_full[x], 4);
             mbar_init(&s_full[x], 1);
             mbar_init(&s_free[x], 4);
             mbar_init(&p_full[x], 4);
@@ -257,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nq = p.num_q_heads;
 
     if (warp == 0 || warp == 6) {
-        // ------------- producers: warp 0 Q rows and K tiles, warp 6 V tiles -------------
+        // ------------------- producers: warp 0 K tiles, warp 6 V tiles -------------------
         const bool is_v = warp == 6;
         const int NS = is_v ? kV8Stages : kKStages;
         uint64_t *full = is_v ? v8_full : k_full;
@@ -269,66 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t it = 0;
         int stop = 0;
         int b, kh, part;
-        // the Q producer reads each item's q one item ahead, so the load's latency does
-        // not hold up the item's K tiles
-        auto q_chunks = [&](int bb, int kk, uint4 (&dst)[G / 2]) {
-            const uint4 *qg = reinterpret_cast<const uint4 *>(
-                static_cast<const __nv_bfloat16 *>(p.q) + (static_cast<int64_t>(bb) * nq + kk * G) * kHD);
-#pragma unroll
-            for (int i = 0; i < G / 2; ++i) dst[i] = __ldg(qg + lane + 32 * i);
-        };
-        uint4 qnext[G / 2];
-        if (!is_v && item8(p, pref, total, 0, b, kh, part)) q_chunks(b, kh, qnext);
         for (int e = 0; !stop && item8(p, pref, total, e, b, kh, part); ++e) {
             const Span8 sp = span8(p, b, part);
-            if (!is_v) {
-                // Q of the group as E4M3 hi / lo rows: row g = hi of head g, row G + g its
-                // lo; bytes of each 128-byte row swizzled in 16-byte units by row % 8
-                const int x = e & 1;
-                if (lane == 0 && !mbar_wait(&q_empty[x], ((e >> 1) & 1) ^ 1u, p.status, abort_flag))
-                    stop = 1;
-                stop = __shfl_sync(kMask, stop, 0);
-                if (stop) break;
-                uint8_t *qb = smem + kOffQ + x * kQBytes;
-                uint4 qcur[G / 2];
-#pragma unroll
-                for (int i = 0; i < G / 2; ++i) qcur[i] = qnext[i];
-                {
-                    int b1, kh1, part1;
-                    if (item8(p, pref, total, e + 1, b1, kh1, part1)) q_chunks(b1, kh1, qnext);
-                }
-#pragma unroll
-                for (int i = 0; i < G / 2; ++i) {
-                    const int c = lane + 32 * i;                   // head c / 16, dims (c % 16) * 8
-                    const uint4 raw = qcur[i];
-                    const float s = q_split_scale(head_max(raw));
-                    float f[8];
-                    unpack_bf16x8(raw, f);
-                    uint32_t hw[2], lw[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint16_t hp[2], lp[2];
-#pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            const float a0 = f[4 * h + 2 * j] * s, a1 = f[4 * h + 2 * j + 1] * s;
-                            hp[j] = e4m3x2(a1, a0);
-                            const float2 back = e4m3x2_to_float2(hp[j]);
-                            lp[j] = e4m3x2(a1 - back.y, a0 - back.x);
-                        }
-                        hw[h] = hp[0] | (static_cast<uint32_t>(hp[1]) << 16);
-                        lw[h] = lp[0] | (static_cast<uint32_t>(lp[1]) << 16);
-                    }
-                    const int g = c >> 4, d0 = (c & 15) * 8;
-                    const int rh = g, rl = G + g;
-                    *reinterpret_cast<uint2 *>(qb + rh * 128 + ((((d0 >> 4) ^ (rh & 7))) << 4) + (d0 & 15)) =
-                        make_uint2(hw[0], hw[1]);
-                    *reinterpret_cast<uint2 *>(qb + rl * 128 + ((((d0 >> 4) ^ (rl & 7))) << 4) + (d0 & 15)) =
-                        make_uint2(lw[0], lw[1]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&q_full[x]);
-            }
             // page ids of the partition, one per lane (past the sequence, before the window
             // or bad: an out-of-range box that reads zeros); the V producer flags nothing
             const int np = (sp.n_tok + kBlockSize - 1) / kBlockSize;
@@ -457,7 +427,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) return;
                 tc_commit(&s_full[x]);
-                tc_commit(&q_empty[x]);
             };
             // O^T = V^T P over the converted tiles of item e
             auto issue_pv = [&](int e, const Span8 &sp) {
@@ -513,10 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float q_mul = p.scale_log2 * p.k_scale;    // log2 units, k_scale folded in
         bool ok = true;
         int b, kh, part;
-        // The per-head Q scales of an item, computed as the producer computes them, into
-        // qinv[e % 2]: item 0's here, item e + 1's while item e waits for its O^T (the
-        // item's last barrier publishes them).  Thread sid < 16 G holds one 16-byte chunk
-        // of q, loaded two items ahead so that the load's latency stays off this chain.
+        // These warps also write each item's Q rows (E4M3 hi / lo, R16) into Q buffer
+        // e % 2 and its per-head scales into qinv[e % 2]: items 0 and 1 here, item e + 2
+        // once item e's P is written (item e's score MMAs, the last reader of that
+        // buffer, are complete: this warp has waited for them), so the producer warp
+        // does nothing but stream K tiles.  Thread sid < 16 G holds one 16-byte chunk of
+        // q, loaded an item before it is split so that the load's latency stays off
+        // this chain.
         auto q_chunk = [&](int e) -> uint4 {
             int bb, kk, pp;
             if (sid >= 16 * G || !item8(p, pref, total, e, bb, kk, pp)) return make_uint4(0u, 0u, 0u, 0u);
@@ -524,14 +496,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       (static_cast<int64_t>(bb) * nq + kk * G) * kHD;
             return __ldg(reinterpret_cast<const uint4 *>(qg) + sid);
         };
-        auto q_scales = [&](int e, const uint4 &raw) {
-            if (sid < 16 * G) {                              // warp-uniform
+        auto q_write = [&](int e, const uint4 &raw) {
+            int bb, kk, pp;
+            if (!item8(p, pref, total, e, bb, kk, pp)) return;   // uniform over the CTA
+            if (sid < 16 * G) {                                  // warp-uniform
                 const float s = q_split_scale(head_max(raw));
                 if ((lane & 15) == 0) qinv[(e & 1) * kN + (sid >> 4)] = 1.f / s;  // exact
+                store_q_split<G>(smem + kOffQ + (e & 1) * kQBytes, sid, raw, s);
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_full[e & 1]);
         };
-        q_scales(0, q_chunk(0));
-        uint4 q_ahead = q_chunk(1);
+        q_write(0, q_chunk(0));
+        q_write(1, q_chunk(1));
+        uint4 q_ahead = q_chunk(2);
         named_barrier(1, 128);
         // The epilogue of an item (O^T from TMEM, normalised, to the partials) is deferred
         // until the next item's P is written, so that the P.V of one item overlaps the
@@ -653,8 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm[g] = red[4 * kN + g] + red[5 * kN + g] + red[6 * kN + g] + red[7 * kN + g];
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[x]);
-            q_scales(e + 1, q_ahead);   // unused past the last item
-            q_ahead = q_chunk(e + 2);
+            q_write(e + 2, q_ahead);
+            q_ahead = q_chunk(e + 3);
             // item e - 1's epilogue runs now, while the P.V of item e can start
             const bool done = !have_prev || epilogue();
             have_prev = true;
