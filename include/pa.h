@@ -221,7 +221,8 @@ int pa_decode_split_static(void *out, const void *q, const void *k_cache, const 
                            int max_seq_len, void *stream);
 
 /*
- * Bytes of workspace pa_ragged_prefill needs (a device-built tile schedule).
+ * Bytes of workspace pa_ragged_prefill needs: 256 bytes of work counters, then room
+ * for a device-built tile schedule.
  */
 size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_heads,
                                         int head_dim);
@@ -243,8 +244,14 @@ size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_
  *         request r is token j of block_tables[r] (as in pa_decode); the
  *         kv_indptr values only give the lengths.
  *   qo_indptr_h, kv_indptr_h  [batch+1] int32 HOST copies (used to size and
- *         order the launch); qo_indptr_d, kv_indptr_d the same on the device.
- *   workspace  >= pa_ragged_prefill_workspace_size() bytes, 256-byte aligned.
+ *         order the launch: up to 1024 query tiles, the heaviest-first work list
+ *         is built from them on the host and passed with the launch); qo_indptr_d,
+ *         kv_indptr_d the same on the device, which must hold the same values.
+ *   workspace  >= pa_ragged_prefill_workspace_size() bytes, 256-byte aligned, owned
+ *         by the caller and used by one call at a time.  Its first 8 bytes are the
+ *         launch's work counters: they must be zero before the first call (allocate
+ *         it zeroed), and every call leaves them zero.  After a call that reported
+ *         PA_ERR_TIMEOUT through pa_get_device_status, zero them again.
  *   sm_scale must be positive and finite (PA_ERR_INVALID otherwise).
  */
 int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,

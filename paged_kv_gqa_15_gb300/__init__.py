@@ -240,8 +240,9 @@ def decode_split_workspace_views(workspace, num_seqs, num_q_heads, head_dim, max
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
-    """A 256-byte-aligned uint8 device buffer of at least nbytes."""
-    buf = torch.empty(max(int(nbytes), 1) + 256, dtype=torch.uint8, device=device)
+    """A zeroed, 256-byte-aligned uint8 device buffer of at least nbytes (the prefill's
+    work counters must start at zero)."""
+    buf = torch.zeros(max(int(nbytes), 1) + 256, dtype=torch.uint8, device=device)
     off = (-buf.data_ptr()) % 256
     return buf[off:off + max(int(nbytes), 1)]
 

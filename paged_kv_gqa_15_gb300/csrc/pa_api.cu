@@ -464,6 +464,8 @@ int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
     L.q = q;
     L.k = k;
     L.v = v;
+    L.qo_indptr_h = qo_indptr_h;
+    L.kv_indptr_h = kv_indptr_h;
     L.total_qo = total_qo_rows;
     L.total_kv = total_kv_rows;
     L.s_block = stride_block;

@@ -41,6 +41,10 @@ struct DecodeParams {
     int *status;
 };
 
+// Work lists of up to this many query tiles are ordered on the host and passed inline
+// in the kernel's parameters (4 KB); longer ones are ordered by a one-CTA kernel.
+constexpr int kPrefillInlineTiles = 1024;
+
 struct PrefillParams {
     CUtensorMap tm_q;   // q [total_qo][nq][hd] as (hd, nq, rows), 128-row boxes
     CUtensorMap tm_k;   // ragged: (hd, nkv, rows); paged: (hd, 16, nkv, blocks)
@@ -48,17 +52,24 @@ struct PrefillParams {
     void *o;
     const int32_t *qo_indptr, *kv_indptr;  // device [batch + 1]
     const int32_t *block_tables;           // paged mode, else nullptr
-    const int2 *tiles;                     // (request, q tile), heaviest first
-    int *item_counter;                     // next unclaimed work item (zeroed per call)
+    const int2 *tiles;                     // (request, q tile), heaviest first (device list)
+    // [0] the next unclaimed work item, [1] CTAs done; zero when a launch starts (the
+    // last CTA to finish clears both)
+    int *item_counter;
     int64_t num_blocks;
     int batch, nq, nkv, max_blocks, n_tiles, causal;
     int window;                            // sliding window in keys (> 0), or 0 for none
     float scale_log2;
     int *status;
+    // > 0: the work list is inline_tiles[0 .. n_inline - 1], each request | tile << 16,
+    // heaviest first, and `tiles` is unused
+    int n_inline;
+    uint32_t inline_tiles[kPrefillInlineTiles];
 };
 
 struct PrefillLaunch {
     const void *q, *k, *v;
+    const int32_t *qo_indptr_h, *kv_indptr_h;   // host copies of the indptrs
     int64_t total_qo, total_kv;
     int64_t s_block, s_head, s_token;
     int head_dim;

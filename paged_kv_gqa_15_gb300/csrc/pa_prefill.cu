@@ -34,6 +34,8 @@
 //  * A one-CTA prologue kernel sorts the (request, q-tile) work items by their
 //    number of key tiles, heaviest first, into the caller's workspace.
 //  * Every mbarrier wait is bounded (PA_ERR_TIMEOUT instead of a hang).
+#include <algorithm>
+
 #include <cuda.h>
 
 #include "pa_device.cuh"
@@ -187,17 +189,21 @@ struct PrefillCfg {
 // First key any row of the query tile at q0 sees under a sliding window of `window`
 // keys (row i at position i + kv_len - qo_len sees keys j > position - window); 0
 // without a window.
-__device__ __forceinline__ int window_first_key(int q0, int qo_len, int kv_len, int window) {
+__host__ __device__ __forceinline__ int window_first_key(int q0, int qo_len, int kv_len, int window) {
     if (window <= 0) return 0;
-    return max(0, q0 + (kv_len - qo_len) - window + 1);
+    const int k = q0 + (kv_len - qo_len) - window + 1;
+    return k > 0 ? k : 0;
 }
 
 // Number of key tiles a query tile needs (its work): bottom-right causal, from the
 // tile holding the window's first key.
-__device__ __forceinline__ int key_tiles(int q0, int qo_len, int kv_len, int causal, int window,
-                                         int bn) {
+__host__ __device__ __forceinline__ int key_tiles(int q0, int qo_len, int kv_len, int causal,
+                                                  int window, int bn) {
     int kv_end = kv_len;
-    if (causal) kv_end = min(kv_len, max(0, q0 + kBM + (kv_len - qo_len)));
+    if (causal) {
+        const int last = q0 + kBM + (kv_len - qo_len);   // one past the last row's last key
+        kv_end = last < 0 ? 0 : (last < kv_len ? last : kv_len);
+    }
     const int n = (kv_end + bn - 1) / bn - window_first_key(q0, qo_len, kv_len, window) / bn;
     return n > 0 ? n : 0;
 }
@@ -211,7 +217,10 @@ __global__ void __launch_bounds__(1024) prefill_schedule_kernel(
     const int tid = threadIdx.x;
     // the prefill kernel may launch now (it sets up, then waits for this grid)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (tid == 0) *item_counter = 0;  // the prefill kernel claims items from here
+    if (tid == 0) {   // the prefill kernel claims items from [0]; [1] counts its CTAs done
+        item_counter[0] = 0;
+        item_counter[1] = 0;
+    }
     for (int i = tid; i < kSchedBuckets; i += blockDim.x) hist[i] = 0;
     if (tid == 0) total_sh = 0;
     __syncthreads();
@@ -272,7 +281,13 @@ struct PrefillItem {
 template <bool PAGED, int BN, bool WINDOW>
 __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, long long i) {
     PrefillItem w;
-    const int2 tile = p.tiles[i / p.nq];
+    int2 tile;
+    if (p.n_inline > 0) {
+        const uint32_t v = p.inline_tiles[i / p.nq];
+        tile = make_int2(static_cast<int>(v & 0xffffu), static_cast<int>(v >> 16));
+    } else {
+        tile = p.tiles[i / p.nq];
+    }
     w.h = static_cast<int>(i % p.nq);
     w.r = tile.x;
     w.qo_start = w.qo_len = w.kv_start = w.kv_len = 0;
@@ -408,8 +423,9 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                     stop = 1;
                 } else {
                     const long long claimed = atomicAdd(p.item_counter, 1);
-                    item_q[slot] =
-                        claimed < n_items ? prefill_item<PAGED, BN, WINDOW>(p, claimed) : end_item();
+                    item_q[slot] = claimed >= 0 && claimed < n_items
+                                       ? prefill_item<PAGED, BN, WINDOW>(p, claimed)
+                                       : end_item();
                     mbar_arrive(&item_full[slot]);
                 }
             }
@@ -513,6 +529,15 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 pg_cur = pg_next;
             }
             kv_it += w.n_kv;
+        }
+        // This CTA claims nothing more; the last CTA to get here clears the claim and
+        // done counters, so every launch leaves them zero for the next one.
+        if (lane == 0) {
+            __threadfence();
+            if (atomicAdd(p.item_counter + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+                p.item_counter[0] = 0;
+                p.item_counter[1] = 0;
+            }
         }
     } else if (warp == 1) {
         // -------------------------------- MMA issuer --------------------------------
@@ -813,12 +838,38 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
         if (!encode_tensor_map_bf16(&p.tm_k, L.k, 4, dims, str, box)) return cudaErrorInvalidValue;
         if (!encode_tensor_map_bf16(&p.tm_v, L.v, 4, dims, str, box)) return cudaErrorInvalidValue;
     }
-    prefill_schedule_kernel<<<1, 1024, 0, stream>>>(p.qo_indptr, p.kv_indptr, p.batch, p.causal,
-                                                    p.window, BN, p.n_tiles,
-                                                    const_cast<int2 *>(p.tiles), p.item_counter,
-                                                    p.status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    // The heaviest-first work list: for up to kPrefillInlineTiles query tiles it is built
+    // here, from the host indptrs, and travels in the kernel's parameters (a stable sort
+    // by key-tile count, heaviest first); longer lists are built on the device by a
+    // one-CTA kernel, which also clears the counters.
+    cudaError_t e = cudaSuccess;
+    if (p.n_tiles <= kPrefillInlineTiles && p.batch <= 65536) {
+        struct Tile {
+            int key;
+            uint32_t code;
+        };
+        Tile list[kPrefillInlineTiles];
+        int n = 0;
+        for (int r = 0; r < p.batch; ++r) {
+            const int qo_len = L.qo_indptr_h[r + 1] - L.qo_indptr_h[r];
+            const int kv_len = L.kv_indptr_h[r + 1] - L.kv_indptr_h[r];
+            const int nt = (qo_len + kBM - 1) / kBM;
+            for (int t = 0; t < nt && n < kPrefillInlineTiles; ++t)
+                list[n++] = {key_tiles(t * kBM, qo_len, kv_len, p.causal, p.window, BN),
+                             static_cast<uint32_t>(r) | (static_cast<uint32_t>(t) << 16)};
+        }
+        std::stable_sort(list, list + n, [](const Tile &a, const Tile &b) { return a.key > b.key; });
+        for (int i = 0; i < n; ++i) p.inline_tiles[i] = list[i].code;
+        p.n_inline = n;
+    } else {
+        p.n_inline = 0;
+        prefill_schedule_kernel<<<1, 1024, 0, stream>>>(p.qo_indptr, p.kv_indptr, p.batch,
+                                                        p.causal, p.window, BN, p.n_tiles,
+                                                        const_cast<int2 *>(p.tiles),
+                                                        p.item_counter, p.status);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const void *kern = reinterpret_cast<const void *>(prefill_kernel<HD, BN, PAGED, WINDOW>);
     const uint32_t smem = C::SMEM;
     const int per_sm = C::CTAS_PER_SM, threads = kThreads;

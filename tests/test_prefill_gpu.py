@@ -312,3 +312,41 @@ def test_rejects_non_positive_scale():
         pa.pa_ragged_prefill(o, t["q"].to(DEV), t["k"].to(DEV), t["v"].to(DEV), w.qo_indptr,
                              w.kv_indptr, torch.from_numpy(w.qo_indptr).to(DEV),
                              torch.from_numpy(w.kv_indptr).to(DEV), 0.0)
+
+
+# ---- work list: built on the host (<= 1024 query tiles) or by the schedule kernel ------
+
+def test_work_list_longer_than_the_inline_limit():
+    # 1100 one-tile requests: the work list is built on the device, not on the host
+    rng = np.random.default_rng(40)
+    lens = rng.integers(1, 129, size=1100)
+    o, ref, _ = _contig_case(lens, lens, 4, 2, 64, seed=41)
+    assert pa.device_status() == 0
+    assert_close_bf16(o, ref, what="1100 query tiles")
+
+
+def test_calls_leave_the_work_counters_zero():
+    # one workspace through host-built and device-built work lists, alternately: each
+    # launch must find its counters at zero and leave them so
+    small = W.make_prefill("s", [130, 5, 300], [200, 5, 300], 8, 2, 128, seed=42)
+    rng = np.random.default_rng(43)
+    many_lens = rng.integers(1, 129, size=1100)
+    many = W.make_prefill("m", many_lens, many_lens, 4, 2, 128, seed=44)
+    size = max(pa.ragged_prefill_workspace_size(w.batch, w.total_qo, w.num_q_heads, 128)
+               for w in (small, many))
+    ws = pa.alloc_workspace(size, DEV)
+    for w in (small, many, small, many):
+        t = w.tensors("cpu")
+        q, k, v = (W.to_bits(t[n]) for n in ("q", "k", "v"))
+        o = torch.full((w.total_qo, w.num_q_heads, 128), float("nan"), dtype=torch.bfloat16,
+                       device=DEV)
+        pa.pa_ragged_prefill(o, _to_dev(q), _to_dev(k), _to_dev(v), w.qo_indptr, w.kv_indptr,
+                             torch.from_numpy(w.qo_indptr).to(DEV),
+                             torch.from_numpy(w.kv_indptr).to(DEV), w.scale, causal=True,
+                             workspace=ws)
+        torch.cuda.synchronize()
+        assert int(ws[:8].view(torch.int32).abs().sum()) == 0
+        ref = oracle.prefill(q, k, v, w.qo_indptr, w.kv_indptr, w.num_kv_heads, w.scale,
+                             causal=True)
+        assert_close_bf16(o, ref, what=f"batch {w.batch}")
+    assert pa.device_status() == 0
