@@ -47,9 +47,9 @@ TRAFFIC = {
     "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
         "src": "63dff5344a34bf6e", "bytes_per_launch": 573760768},
     # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
-    # causal prefill: dram__bytes_read.sum 295.56 MB + dram__bytes_write.sum 108.80 MB
+    # causal prefill: dram__bytes_read.sum 301.79 MB + dram__bytes_write.sum 108.98 MB
     "ragged_prefill:ragged_prefill_r16_h32kv8_d128": {
-        "src": "f54cff3896e5ae59", "bytes_per_launch": 404355072},
+        "src": "afc53ed4209d9487", "bytes_per_launch": 410771456},
     # ncu capture of one decode_tc8_kernel<4> launch on the Llama-8B decode workload over
     # an FP8 cache: dram__bytes_read.sum 284.47 MB + dram__bytes_write.sum 4.68 MB
     "decode_partitions:llama8b_decode_fp8_b64_h32kv8_d128": {
@@ -254,13 +254,17 @@ _flush_buf = {}
 
 
 def flush_l2(stream, device):
-    """Overwrites a buffer much larger than L2 on `stream` (evicts the workload)."""
+    """Overwrites a buffer much larger than L2 on `stream` (evicts the workload), then
+    reads it back: the read evicts the buffer's own dirty lines, so their write-backs
+    happen here and not inside the next timed step, which starts with L2 holding only
+    clean lines of the flush buffer."""
     buf = _flush_buf.get(str(device))
     if buf is None:
         buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
         _flush_buf[str(device)] = buf
     with torch.cuda.stream(stream):
         buf.fill_(1)
+        buf.sum(dtype=torch.int64)
 
 
 def time_steps(step, steps, warmup, stream, device, labels, flush=False):
@@ -710,8 +714,8 @@ def run_reference(args, w, rank):
 
 def l2_note(footprint):
     if footprint < L2_FLUSH_BYTES:
-        return ("inputs %.0f MB: L2 flushed (512 MB write) before every timed step, outside "
-                "the kernel intervals" % (footprint / 1e6))
+        return ("inputs %.0f MB: L2 flushed (512 MB written, then read back) before every "
+                "timed step, outside the timed intervals" % (footprint / 1e6))
     return "inputs larger than L2 (%.0f MB > 129 MB); no flush" % (footprint / 1e6)
 
 
