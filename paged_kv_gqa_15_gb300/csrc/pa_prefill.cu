@@ -448,10 +448,16 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             if (__any_sync(kFullMask, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
             return (raw == -2 || bad) ? static_cast<int>(p.num_blocks) : raw;
         };
+        // Item k + 1 is claimed and published once item k's first K tile is on its way,
+        // so the claim's atomic and the item's indptr reads overlap item k's loads
+        // instead of stalling the producer between items.
+        PrefillItem w = claim(0);
         for (uint32_t k = 0; !stop; ++k) {
-            const PrefillItem w = claim(k);
             if (stop || w.n_kv < 0) break;
-            if (w.n_kv == 0) continue;
+            if (w.n_kv == 0) {
+                w = claim(k + 1);
+                continue;
+            }
             const int kh = w.h / group;
 
             if (lane == 0) {
@@ -515,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 if (w.n_kv > 1) raw_next = page_raw(w.r, j0 + 1, pages_seq, page_lo);
             }
             load_tile(0, 0, kv_it, pg_cur);
+            const PrefillItem next = stop ? end_item() : claim(k + 1);
             for (int j = 0; j < w.n_kv && !stop; ++j) {
                 int pg_next = 0;
                 if (j + 1 < w.n_kv) {
@@ -529,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 pg_cur = pg_next;
             }
             kv_it += w.n_kv;
+            w = next;
         }
         // This CTA claims nothing more; the last CTA to get here clears the claim and
         // done counters, so every launch leaves them zero for the next one.
