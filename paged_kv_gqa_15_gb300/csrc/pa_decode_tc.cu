@@ -164,15 +164,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // a programmatic dependent of the cache write: start up, then wait for it
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    // prefix over sequences of their partition counts (the compact item list)
-    for (int b = threadIdx.x; b < p.num_seqs; b += kThreadsTc) {
-        const int L = tc_seq_len(p, b, blockIdx.x == 0);
-        pref[b + 1] = (L + kPartition - 1) / kPartition - window_start(L, p.window) / kPartition;
-    }
-    if (threadIdx.x == 0) pref[0] = 0;
+    // The set-up that reads no global memory (barriers, the zeroed padding, TMEM, the
+    // tensor maps, which are launch parameters) runs before the wait; as a programmatic
+    // dependent of the cache write it then overlaps that kernel.  Everything that reads
+    // global memory (sequence lengths, block tables, q, the pools) comes after it.
     // rows g .. 15 of the Q^T and P buffers stay zero (padding of the MMA's N)
     for (uint32_t i = threadIdx.x; i < (2 * kQBytes + kPBytes) / 16; i += kThreadsTc)
         reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -200,6 +195,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         fence_mbar_init();
     }
     fence_proxy_async_smem();   // the zeroed padding is read by the tensor core
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&prm.tm_k);
+        prefetch_tensormap(&prm.tm_v);
+        prefetch_tensormap(&prm.tm_q);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // prefix over sequences of their partition counts (the compact item list)
+    for (int b = threadIdx.x; b < p.num_seqs; b += kThreadsTc) {
+        const int L = tc_seq_len(p, b, blockIdx.x == 0);
+        pref[b + 1] = (L + kPartition - 1) / kPartition - window_start(L, p.window) / kPartition;
+    }
+    if (threadIdx.x == 0) pref[0] = 0;
     __syncthreads();
     if (warp == 0) {
         int carry = 0;
@@ -215,10 +227,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             carry += __shfl_sync(kFullMaskTc, v, 31);
         }
     }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
-    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -233,10 +241,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         uint64_t *empty = is_v ? v_empty : k_empty;
         uint8_t *ring = smem + (is_v ? kOffV : kOffK);
         const CUtensorMap *tm = is_v ? &prm.tm_v : &prm.tm_k;
-        if (lane == 0) {
-            prefetch_tensormap(tm);
-            if (!is_v) prefetch_tensormap(&prm.tm_q);
-        }
         const uint64_t policy = l2_policy_evict_first();
         uint32_t it = 0;   // ring uses
         int stop = 0;

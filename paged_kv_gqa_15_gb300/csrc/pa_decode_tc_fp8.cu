@@ -220,14 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // a programmatic dependent of the cache write: start up, then wait for it
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    for (int b = threadIdx.x; b < p.num_seqs; b += kThreads) {
-        const int L = seq_len8(p, b, blockIdx.x == 0);
-        pref[b + 1] = (L + kPartition - 1) / kPartition - window_start(L, p.window) / kPartition;
-    }
-    if (threadIdx.x == 0) pref[0] = 0;
+    // The set-up that reads no global memory (barriers, the zeroed padding, TMEM, the
+    // tensor maps, which are launch parameters) runs before the wait; as a programmatic
+    // dependent of the cache write it then overlaps that kernel.  Everything that reads
+    // global memory (sequence lengths, block tables, q, the pools) comes after it.
     // Q rows 2G .. 15 and P rows G .. 15 stay zero (padding of the MMA's N)
     for (uint32_t i = threadIdx.x; i < (2 * kQBytes + 2 * kPBytes) / 16; i += kThreads)
         reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -258,6 +254,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     fence_proxy_async_smem();   // the zeroed padding is read by the tensor core
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&prm.tm_k);
+        prefetch_tensormap(&prm.tm_v);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    for (int b = threadIdx.x; b < p.num_seqs; b += kThreads) {
+        const int L = seq_len8(p, b, blockIdx.x == 0);
+        pref[b + 1] = (L + kPartition - 1) / kPartition - window_start(L, p.window) / kPartition;
+    }
+    if (threadIdx.x == 0) pref[0] = 0;
     __syncthreads();
     if (warp == 0) {
         int carry = 0;
@@ -272,10 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (idx <= p.num_seqs) pref[idx] = v + carry;
             carry += __shfl_sync(kMask, v, 31);
         }
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -292,7 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t *empty = is_v ? v8_empty : k_empty;
         uint8_t *ring = smem + (is_v ? kOffV8 : kOffK);
         const CUtensorMap *tm = is_v ? &prm.tm_v : &prm.tm_k;
-        if (lane == 0) prefetch_tensormap(tm);
         const uint64_t policy = l2_policy_evict_first();
         uint32_t it = 0;
         int stop = 0;
