@@ -45,15 +45,15 @@ TRAFFIC = {
     # ncu capture of one decode_tc_kernel<4> launch on the Llama-8B decode workload:
     # dram__bytes_read.sum 568.32 MB + dram__bytes_write.sum 5.44 MB
     "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
-        "src": "63dff5344a34bf6e", "bytes_per_launch": 573760768},
+        "src": "f91443e61d25a31b", "bytes_per_launch": 573758464},
     # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
-    # causal prefill: dram__bytes_read.sum 301.79 MB + dram__bytes_write.sum 108.98 MB
+    # causal prefill: dram__bytes_read.sum 299.62 MB + dram__bytes_write.sum 108.65 MB
     "ragged_prefill:ragged_prefill_r16_h32kv8_d128": {
-        "src": "afc53ed4209d9487", "bytes_per_launch": 410771456},
+        "src": "b01b37981a907722", "bytes_per_launch": 408266752},
     # ncu capture of one decode_tc8_kernel<4> launch on the Llama-8B decode workload over
-    # an FP8 cache: dram__bytes_read.sum 284.47 MB + dram__bytes_write.sum 4.68 MB
+    # an FP8 cache: dram__bytes_read.sum 284.47 MB + dram__bytes_write.sum 4.72 MB
     "decode_partitions:llama8b_decode_fp8_b64_h32kv8_d128": {
-        "src": "107347d0291f77df", "bytes_per_launch": 289143296},
+        "src": "a9c251812034d7df", "bytes_per_launch": 289189888},
 }
 
 
