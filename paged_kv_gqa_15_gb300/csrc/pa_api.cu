@@ -378,7 +378,7 @@ size_t pa_ragged_prefill_workspace_size(int batch, int total_qo_rows, int num_q_
     (void)head_dim;
     const size_t tiles = static_cast<size_t>(total_qo_rows > 0 ? total_qo_rows : 0) / 128 +
                          static_cast<size_t>(batch > 0 ? batch : 0) + 1;
-    return 256 + round256(tiles * 8);  // work-item counter, then the tile schedule
+    return 256 + round256(tiles * 8);  // work counters, then room for a device-built list
 }
 
 int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,

@@ -31,8 +31,11 @@
 //  * Causal tile skipping: a query tile stops at the last key tile any of its
 //    rows can see; per-element masking only on tiles that cross the diagonal
 //    or the end of the keys.
-//  * A one-CTA prologue kernel sorts the (request, q-tile) work items by their
-//    number of key tiles, heaviest first, into the caller's workspace.
+//  * The (request, q-tile) work items are ordered by their number of key tiles,
+//    heaviest first: on the host for up to 1024 query tiles (the list then travels
+//    in the kernel's parameters), otherwise by a one-CTA kernel into the caller's
+//    workspace.  The producer claims item k + 1 once item k's first K tile is on its
+//    way, and the last CTA to finish clears the work counters for the next launch.
 //  * Every mbarrier wait is bounded (PA_ERR_TIMEOUT instead of a hang).
 #include <algorithm>
 
@@ -407,10 +410,11 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             prefetch_tensormap(&p.tm_k);
             prefetch_tensormap(&p.tm_v);
         }
-        // This grid is launched as a programmatic dependent of the schedule kernel:
-        // the set-up above overlaps it, and the work list and item counter it writes
-        // are read only after it has completed.  The other warps see items only
-        // through this warp.
+        // This grid is launched as a programmatic dependent of the kernel before it
+        // (the schedule kernel, when the work list is built on the device): the
+        // set-up above overlaps it, and nothing it may write (the work list, the
+        // counters, q, k, v, the pools) is read before it has completed.  The other
+        // warps see items only through this warp.
         asm volatile("griddepcontrol.wait;" ::: "memory");
         uint32_t kv_it = 0;
         int stop = 0;
