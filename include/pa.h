@@ -343,6 +343,16 @@ int pa_swap_blocks(const void *const *src_pools, void *const *dst_pools, int num
  */
 int pa_get_device_status(int *status_h, void *stream);
 
+/*
+ * pa_selftest_wait_timeout -- exercises the bounded wait that every kernel's
+ * pipeline uses.  One thread waits on an mbarrier that nothing completes; after
+ * about 1 s (the per-wait limit) it records PA_ERR_TIMEOUT in the device status
+ * word and the kernel returns.  No memory is touched but that word; the context
+ * stays usable.  Enqueued on `stream`; returns PA_OK, or PA_ERR_CUDA when the
+ * launch fails.
+ */
+int pa_selftest_wait_timeout(void *stream);
+
 /* Thread-local description of the last error returned on this thread. */
 const char *pa_last_error(void);
 

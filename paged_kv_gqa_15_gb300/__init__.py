@@ -61,6 +61,7 @@ def load():
     lib.pa_ragged_prefill.argtypes = [P, P, P, P, P, P, P, P, P, I, I, L, L, L, L, I, I, I, I, I,
                                       I, F, I, I, P, Z, P]
     lib.pa_get_device_status.argtypes = [P, P]
+    lib.pa_selftest_wait_timeout.argtypes = [P]
     lib.pa_block_table_sync.argtypes = [P, P, P, I, I, P, P]
     lib.pa_block_table_sync.restype = I
     lib.pa_copy_blocks.argtypes = [P, I, P, L, L, L, P]
@@ -340,6 +341,12 @@ def pa_ragged_prefill(o, q, k, v, qo_indptr_h, kv_indptr_h, qo_indptr_d, kv_indp
         _ptr(block_tables), mb, bs, nb, sb, sh, st, batch, total_qo, total_kv, nq, nkv, hd,
         float(sm_scale), 1 if causal else 0, int(sliding_window), _ptr(workspace),
         workspace.numel(), _stream(stream)))
+
+
+def selftest_wait_timeout(stream=None):
+    """Runs one bounded wait that nothing completes (about 1 s); the device status
+    then holds the PA_ERR_TIMEOUT bit."""
+    _check(load().pa_selftest_wait_timeout(_stream(stream)))
 
 
 def device_status(stream=None) -> int:

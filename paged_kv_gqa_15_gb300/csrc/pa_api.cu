@@ -6,6 +6,7 @@
 #include <cstring>
 
 #include "../../include/pa.h"
+#include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace {
@@ -176,6 +177,31 @@ int pa_get_device_status(int *status_h, void *stream) {
     if (e != cudaSuccess) return cuda_fail(e, "read status");
     e = cudaMemset(ptr, 0, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "clear status");
+    return PA_OK;
+}
+
+namespace {
+// One thread waits, bounded, on an mbarrier that nothing arrives on: the wait every
+// kernel's pipeline uses, run out on purpose.
+__global__ void wait_timeout_selftest_kernel(int *status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        pa::mbar_init(&bar, 1);
+        abort_flag = 0;
+        pa::fence_mbar_init();
+        (void)pa::mbar_wait(&bar, 0, status, &abort_flag);
+    }
+}
+}  // namespace
+
+int pa_selftest_wait_timeout(void *stream) {
+    int *status = nullptr;
+    int rc = status_ptr(&status);
+    if (rc) return rc;
+    wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
     return PA_OK;
 }
 
