@@ -249,6 +249,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const TcSpan sp = tc_span(p, b, part);
             const int t0 = sp.t0;
             const int n_tiles = sp.n_tiles;
+            // page ids of the partition, one per lane (past the sequence, before the
+            // window or bad: an out-of-range box that reads zeros); read before the Q load
+            // is issued, so the read and that load overlap
+            const int np = (sp.n_tok + kBlockSize - 1) / kBlockSize;
+            const int pg_lo = sp.t_lo / kBlockSize;
+            int page = (lane >= pg_lo && lane < np)
+                           ? p.block_tables[static_cast<int64_t>(b) * p.max_blocks +
+                                            t0 / kBlockSize + lane]
+                           : -2;
             if (!is_v) {
                 const int qb = e & 1;
                 if (lane == 0) {
@@ -263,15 +272,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     tma_load_3d(smem + kOffQ + qb * kQBytes + lane * kSmallChunk, &prm.tm_q,
                                 lane * 64, kh * G, b, &q_full[qb]);
             }
-            // page ids of the partition, one per lane (past the sequence, before the
-            // window or bad: an out-of-range box that reads zeros); the V producer flags
-            // nothing twice
-            const int np = (sp.n_tok + kBlockSize - 1) / kBlockSize;
-            const int pg_lo = sp.t_lo / kBlockSize;
-            int page = (lane >= pg_lo && lane < np)
-                           ? p.block_tables[static_cast<int64_t>(b) * p.max_blocks +
-                                            t0 / kBlockSize + lane]
-                           : -2;
+            // bad ids are flagged by the K producer only
             const bool bad = page != -2 && (page < 0 || page >= p.num_blocks);
             if (!is_v && __any_sync(kFullMaskTc, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
             if (page == -2 || bad) page = static_cast<int>(p.num_blocks);
