@@ -43,9 +43,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # for the source file hash they were measured on (otherwise reported as null).
 TRAFFIC = {
     # ncu capture of one decode_tc_kernel<4> launch on the Llama-8B decode workload:
-    # dram__bytes_read.sum 568.32 MB + dram__bytes_write.sum 5.44 MB
+    # dram__bytes_read.sum 568.32 MB + dram__bytes_write.sum 5.49 MB
     "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
-        "src": "f91443e61d25a31b", "bytes_per_launch": 573758464},
+        "src": "23c62bb4aa65e8f7", "bytes_per_launch": 573813760},
     # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
     # causal prefill: dram__bytes_read.sum 299.62 MB + dram__bytes_write.sum 108.65 MB
     # (captured on source b01b37981a907722; re-keyed after a comment-only edit)
