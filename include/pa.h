@@ -11,7 +11,10 @@
  *                       per-partition max / sum / partial output, then a
  *                       log-sum-exp merge ("paged_attn.py", forward_decode, V2
  *                       branch; "libmir-cuda attention/mod.rs",
- *                       SplitPagedAttention and its workspace)
+ *                       SplitPagedAttention and its workspace); its two halves
+ *                       are also exposed as pa_decode_partitions and
+ *                       pa_decode_merge, and pa_decode_split_static runs it on a
+ *                       library-owned scratch buffer (no caller workspace)
  *   pa_ragged_prefill   ragged (varlen) causal prefill of many requests in one
  *                       launch through qo_indptr / kv_indptr, over contiguous
  *                       or paged K/V ("spark_runtime/flashinfer.rs",
@@ -24,6 +27,12 @@
  *                       V pools ("paged_attn.py", PagedAttention.copy_blocks)
  *   pa_swap_blocks      page copies between pools on the device and in pinned
  *                       host memory ("paged_attn.py", PagedAttention.swap_blocks)
+ *   pa_selftest_wait_timeout  one bounded pipeline wait run out on purpose, to
+ *                       check the PA_ERR_TIMEOUT path (no page defines it)
+ *
+ * The decode entry points take kv_dtype (PA_KV_BF16 or PA_KV_FP8_E4M3) with
+ * k_scale / v_scale; pa_write_cache quantises into an FP8 pool with the same
+ * arguments ("paged_attn.py", kv_cache_dtype, k_scale and v_scale).
  *
  * Conventions shared by every entry point:
  *  - All data pointers are DEVICE pointers of the current CUDA device unless
