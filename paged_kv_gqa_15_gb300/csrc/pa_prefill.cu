@@ -50,7 +50,6 @@ namespace {
 
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr int kBM = 128;              // query rows per tile (MMA M)
-constexpr int kThreads = 192;         // 6 warps
 constexpr int kSchedBuckets = 2048;
 
 constexpr uint32_t pow2_at_least(uint32_t x) {
@@ -154,6 +153,17 @@ __device__ __forceinline__ void tile_exp(const uint32_t (&sr)[BN], float scale, 
     rs.l += lsum_t.x + lsum_t.y;
 }
 
+// Paged K/V at head_dim 256: a key tile is 32 two-kilobyte TMA boxes (K and V: 4
+// pages x 4 column chunks), and one warp issuing them all set the pace, so a second
+// producer warp (warp 6) issues the V tiles.  Contiguous K/V move as 8 KB boxes and
+// do not need it (a split measured 7 % slower there); at head_dim <= 128 two CTAs
+// share an SM and their registers leave no room for a seventh warp.
+template <int HD, bool PAGED>
+struct ProducerSplit {
+    static constexpr bool value = HD == 256 && PAGED;
+    static constexpr int threads = value ? 224 : 192;
+};
+
 template <int HD, int BN>
 struct PrefillCfg {
     static constexpr int QCH = HD / 64;                       // 128-byte column chunks
@@ -165,6 +175,7 @@ struct PrefillCfg {
     // by a softmax-side arrival on k_empty) hides more of the TMA latency.
     static constexpr int KS = HD == 256 ? 3 : 2;
     static constexpr int VS = 2;                              // V ring stages
+
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
@@ -327,9 +338,10 @@ __device__ __forceinline__ PrefillItem end_item() {
 // sliding-window form (items start at their window's key tile, rows get a lower
 // column bound); without it the window terms are compiled out.
 template <int HD, int BN, bool PAGED, bool WINDOW>
-__global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
+__global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<HD, BN>::CTAS_PER_SM)
     prefill_kernel(const __grid_constant__ PrefillParams p) {
     using C = PrefillCfg<HD, BN>;
+    constexpr bool SPLIT = ProducerSplit<HD, PAGED>::value;
     const int window = WINDOW ? p.window : 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -389,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
         mbar_init(drain, 1);
         for (int k = 0; k < 4; ++k) {
             mbar_init(&item_full[k], 1);
-            mbar_init(&item_empty[k], 5);
+            mbar_init(&item_empty[k], SPLIT ? 6 : 5);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -403,8 +415,12 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------- TMA producer -------------------------------
+    if (warp == 0 || (SPLIT && warp == 6)) {
+        // ------------------------------- TMA producers -------------------------------
+        // Warp 0 claims the items and loads Q, K (and, unless split, V); with a split
+        // producer warp 6 loads V, taking the items from the queue like the consumers.
+        const bool v_only = SPLIT && warp == 6;
+        const bool loads_v = !SPLIT || v_only;
         if (lane == 0) {
             prefetch_tensormap(&p.tm_q);
             prefetch_tensormap(&p.tm_k);
@@ -417,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
         // warps see items only through this warp.
         asm volatile("griddepcontrol.wait;" ::: "memory");
         uint32_t kv_it = 0;
+        uint32_t n_q = 0, n_k = 0, n_v = 0;   // copies issued (for the drain on an abort)
         int stop = 0;
         // Claims the k-th item of this CTA, decodes it and publishes it to the MMA
         // and softmax warps; an item with n_kv == -1 ends the list.
@@ -437,6 +454,18 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             stop = __shfl_sync(kFullMask, stop, 0);
             return stop ? end_item() : item_q[slot];
         };
+        // The V-only producer's k-th item, read from the queue the claimer fills.
+        auto take = [&](uint32_t k) -> PrefillItem {
+            const int slot = k & 3;
+            if (lane == 0 && !mbar_wait(&item_full[slot], (k >> 2) & 1, p.status, abort_flag))
+                stop = 1;
+            stop = __shfl_sync(kFullMask, stop, 0);
+            if (stop) return end_item();
+            const PrefillItem it = item_q[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[slot]);
+            return it;
+        };
         // Block-table entry of page `lane` of key tile j (lanes < BN / 16); -2 for
         // lanes and pages past the sequence or wholly before the window (those entries
         // are never looked up).  Issued a tile early, checked at use.
@@ -455,16 +484,16 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
         // Item k + 1 is claimed and published once item k's first K tile is on its way,
         // so the claim's atomic and the item's indptr reads overlap item k's loads
         // instead of stalling the producer between items.
-        PrefillItem w = claim(0);
+        PrefillItem w = v_only ? take(0) : claim(0);
         for (uint32_t k = 0; !stop; ++k) {
             if (stop || w.n_kv < 0) break;
             if (w.n_kv == 0) {
-                w = claim(k + 1);
+                w = v_only ? take(k + 1) : claim(k + 1);
                 continue;
             }
             const int kh = w.h / group;
 
-            if (lane == 0) {
+            if (!v_only && lane == 0) {
                 // Q is reused once the previous item's last S (tile kv_it - 1) is done
                 if (kv_it > 0 && !mbar_wait(&s_full[(kv_it - 1) & 1], ((kv_it - 1) >> 1) & 1,
                                             p.status, abort_flag)) {
@@ -475,9 +504,12 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             }
             stop = __shfl_sync(kFullMask, stop, 0);
             if (stop) break;
-            if (lane < C::QCH)   // one 64-column chunk of Q per lane
-                tma_load_3d(smem + C::OFF_Q + lane * kBM * 128, &p.tm_q, lane * 64, w.h,
-                            w.qo_start + w.q0, q_full);
+            if (!v_only) {
+                if (lane < C::QCH)   // one 64-column chunk of Q per lane
+                    tma_load_3d(smem + C::OFF_Q + lane * kBM * 128, &p.tm_q, lane * 64, w.h,
+                                w.qo_start + w.q0, q_full);
+                ++n_q;
+            }
             const int pages_seq = (w.kv_len + kBlockSize - 1) / kBlockSize;
             const int j0 = WINDOW ? w.j0 : 0;
             const int page_lo = WINDOW ? w.kv_lo / kBlockSize : 0;
@@ -499,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 }
                 stop = __shfl_sync(kFullMask, stop, 0);   // also orders lane 0 before the copies
                 if (stop) return;
+                ++(kv ? n_v : n_k);
                 // One box per lane, so a tile's boxes leave in one warp instruction: lane
                 // l copies 64-column chunk l % QCH of page l / QCH (paged) or chunk l.
                 if constexpr (PAGED) {
@@ -524,8 +557,8 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                 pg_cur = page_fix(page_raw(w.r, j0, pages_seq, page_lo));
                 if (w.n_kv > 1) raw_next = page_raw(w.r, j0 + 1, pages_seq, page_lo);
             }
-            load_tile(0, 0, kv_it, pg_cur);
-            const PrefillItem next = stop ? end_item() : claim(k + 1);
+            if (!v_only) load_tile(0, 0, kv_it, pg_cur);
+            const PrefillItem next = (stop || v_only) ? end_item() : claim(k + 1);
             for (int j = 0; j < w.n_kv && !stop; ++j) {
                 int pg_next = 0;
                 if (j + 1 < w.n_kv) {
@@ -534,17 +567,33 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
                         if (j + 2 < w.n_kv)
                             raw_next = page_raw(w.r, j0 + j + 2, pages_seq, page_lo);
                     }
-                    load_tile(0, j + 1, kv_it + j + 1, pg_next);
+                    if (!v_only) load_tile(0, j + 1, kv_it + j + 1, pg_next);
                 }
-                if (!stop) load_tile(1, j, kv_it + j, pg_cur);
+                if (!stop && loads_v) load_tile(1, j, kv_it + j, pg_cur);
                 pg_cur = pg_next;
             }
             kv_it += w.n_kv;
-            w = next;
+            // the V-only producer takes its next item only after this one's tiles
+            w = v_only ? (stop ? end_item() : take(k + 1)) : next;
+        }
+        // never leave the CTA with copies still landing in its shared memory
+        if (lane == 0 && (stop || *abort_flag)) {
+            auto settle = [&](uint64_t *full, int ns, uint32_t n) {
+                for (uint32_t g = n > static_cast<uint32_t>(ns) ? n - ns : 0; g < n; ++g) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (!mbar_try_wait(&full[g % ns], (g / ns) & 1u))
+                        if (global_timer_ns() - t0 > kWaitLimitNs) break;
+                }
+            };
+            if (!v_only) {
+                settle(q_full, 1, n_q);
+                settle(k_full, C::KS, n_k);
+            }
+            if (loads_v) settle(v_full, C::VS, n_v);
         }
         // This CTA claims nothing more; the last CTA to get here clears the claim and
         // done counters, so every launch leaves them zero for the next one.
-        if (lane == 0) {
+        if (!v_only && lane == 0) {
             __threadfence();
             if (atomicAdd(p.item_counter + 1, 1) == static_cast<int>(gridDim.x) - 1) {
                 p.item_counter[0] = 0;
@@ -663,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, PrefillCfg<HD, BN>::CTAS_PER_SM)
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // ----------------------------- softmax + epilogue -----------------------------
         const int quad = warp & 3;                  // TMEM lane quadrant of this warp
         const int row = quad * 32 + lane;           // query row within the tile
@@ -884,7 +933,7 @@ cudaError_t launch_prefill_t(PrefillParams &p, const PrefillLaunch &L, cudaStrea
     }
     const void *kern = reinterpret_cast<const void *>(prefill_kernel<HD, BN, PAGED, WINDOW>);
     const uint32_t smem = C::SMEM;
-    const int per_sm = C::CTAS_PER_SM, threads = kThreads;
+    const int per_sm = C::CTAS_PER_SM, threads = ProducerSplit<HD, PAGED>::threads;
     static int configured_device = -1;
     int dev = 0;
     e = cudaGetDevice(&dev);
