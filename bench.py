@@ -48,8 +48,9 @@ TRAFFIC = {
         "src": "23c62bb4aa65e8f7", "bytes_per_launch": 573813760},
     # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
     # causal prefill: dram__bytes_read.sum 294.99 MB + dram__bytes_write.sum 108.21 MB
+    # (captured on source 024cc71c5a1bbe51; re-keyed after a comment-only edit)
     "ragged_prefill:ragged_prefill_r16_h32kv8_d128": {
-        "src": "024cc71c5a1bbe51", "bytes_per_launch": 403205632},
+        "src": "3ff2430e17fafd35", "bytes_per_launch": 403205632},
     # ncu capture of one decode_tc8_kernel<4> launch on the Llama-8B decode workload over
     # an FP8 cache: dram__bytes_read.sum 284.47 MB + dram__bytes_write.sum 4.72 MB
     "decode_partitions:llama8b_decode_fp8_b64_h32kv8_d128": {

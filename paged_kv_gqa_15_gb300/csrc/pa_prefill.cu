@@ -13,7 +13,7 @@
 //    (request, 128-row query tile, query head) each -- from a heaviest-first
 //    list through a global counter; the producer decodes each claimed item once
 //    and hands it to the other warps through a 4-deep shared-memory queue.
-//    6 warps per CTA:
+//    6 warps per CTA (7 for paged K/V at head_dim 256, see warp 6):
 //      warp 0   TMA producer: Q once per item, then K_j / V_j tiles (128-byte
 //               swizzle) into 2-stage rings, K one tile ahead of V (the order the
 //               MMA warp consumes them); paged mode issues one box per 16-token
@@ -25,6 +25,9 @@
 //               (K / Q reuse, O rescale, O final) is read off those two barriers
 //      warps 2-5  softmax: one query row per thread, read S from TMEM, mask,
 //               exp2, write P (bf16) over S in TMEM; epilogue O / l -> bf16
+//      warp 6   paged head_dim 256 only: a second TMA producer that issues the V
+//               tiles (a tile there is 32 two-kilobyte boxes), taking the items
+//               from the queue; warp 0 then issues Q and K only
 //  * Online softmax with lazy rescaling: O is rescaled (in TMEM) only when a
 //    row max grows by more than 2^8, so the correction is rare; the final
 //    normalisation uses the same running max, which keeps the result exact.
