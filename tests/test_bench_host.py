@@ -1,5 +1,6 @@
 """Host-side logic of bench.py on the CPU: multi-rank aggregation over gloo
-(world size 2), clock-sample parsing and the oracle reference arm."""
+(world size 2), clock-sample parsing, the oracle reference arm, the source-keyed
+traffic records and the L2 note."""
 import json
 import os
 import socket
@@ -96,3 +97,22 @@ def test_window_and_fp8_accounting():
     assert f.kv_bytes() * 2 == a.kv_bytes()
     wdw = W.make_decode("w", [100, 7000], 32, 8, 128, seed=2, window=4096)
     assert wdw.visible_tokens() == 100 + 4096
+
+
+def test_traffic_records_follow_their_sources(tmp_path, monkeypatch):
+    # a record applies only to the source it was measured on: any other hash reads null
+    name = "decode_partitions:llama8b_decode_b64_h32kv8_d128"
+    src = ("pa_decode_tc.cu", "pa_tcgen05.cuh", "pa_device.cuh")
+    rec = bench.TRAFFIC[name]
+    monkeypatch.setitem(bench.TRAFFIC, name, dict(rec, src=bench.source_hash(*src)))
+    assert bench.traffic_for(name, src) == rec["bytes_per_launch"]
+    monkeypatch.setitem(bench.TRAFFIC, name, dict(rec, src="0" * 16))
+    assert bench.traffic_for(name, src) is None
+    assert bench.traffic_for("no_such_kernel:no_such_workload", src) is None
+
+
+def test_l2_note_names_flush_or_size():
+    small = bench.l2_note(100e6)
+    large = bench.l2_note(600e6)
+    assert "flushed" in small and "read back" in small
+    assert "no flush" in large and "600 MB" in large
