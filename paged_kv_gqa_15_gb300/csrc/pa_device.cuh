@@ -11,6 +11,7 @@ namespace pa {
 
 constexpr int kBlockSize = 16;     // tokens per KV page
 constexpr int kPartition = 512;    // tokens per split-KV partition
+constexpr int kStatusUnsupported = 1 << 2;   // bit of PA_ERR_UNSUPPORTED (2)
 constexpr int kStatusTimeout = 1 << 5;   // bit of PA_ERR_TIMEOUT (5)
 constexpr int kStatusBounds = 1 << 6;    // bit of PA_ERR_DEVICE_BOUNDS (6)
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait

@@ -175,7 +175,8 @@ struct PrefillCfg {
     static constexpr uint32_t KV_BYTES = QCH * KV_CHUNK;
     // K ring stages.  With two, stage j % 2 is S buffer j % 2 and K_j is free once S_j
     // is done (s_full); head_dim 256 runs one CTA per SM, where a third stage (freed
-    // by a softmax-side arrival on k_empty) hides more of the TMA latency.
+    // by a softmax-side arrival on k_empty) hides more of the TMA latency.  (A third
+    // stage at head_dim 128, with two CTAs per SM, measured no faster.)
     static constexpr int KS = HD == 256 ? 3 : 2;
     static constexpr int VS = 2;                              // V ring stages
 
@@ -191,10 +192,12 @@ struct PrefillCfg {
     // Two CTAs share an SM when both fit in its 512 TMEM columns (and in shared
     // memory): their MMA and softmax phases then interleave on the tensor core.
     // A CTA that needs all 512 columns asks for enough shared memory to be alone.
-    // 1024 bytes of slack realign the base for the 128-byte-swizzled tiles.
+    // 1024 bytes of slack realign the base for the 128-byte-swizzled tiles (the kernel
+    // checks that the realigned tiles fit before touching shared memory).
     static constexpr int CTAS_PER_SM = TMEM_COLS <= 256 ? 2 : 1;
+    static constexpr uint32_t SLACK = 1024;
     static constexpr uint32_t SMEM_MIN = CTAS_PER_SM == 2 ? 0 : 118 * 1024;
-    static constexpr uint32_t SMEM = (SMEM_USED + 1024 > SMEM_MIN) ? SMEM_USED + 1024 : SMEM_MIN;
+    static constexpr uint32_t SMEM = (SMEM_USED + SLACK > SMEM_MIN) ? SMEM_USED + SLACK : SMEM_MIN;
     static_assert(HD % 64 == 0 && BN % 16 == 0 && BN <= 128, "tile shape");
     static_assert(KS >= 2 && KS <= 4 && VS >= 2 && VS <= 4, "ring stages");
     static_assert(TMEM_COLS <= 512, "TMEM budget");
@@ -346,9 +349,17 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
     using C = PrefillCfg<HD, BN>;
     constexpr bool SPLIT = ProducerSplit<HD, PAGED>::value;
     const int window = WINDOW ? p.window : 0;
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    {   // the realigned tiles must fit the dynamic shared memory this launch has
+        uint32_t dyn;
+        asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+        if (static_cast<uint32_t>(smem - smem_raw) + C::SMEM_USED > dyn) {
+            if (threadIdx.x == 0) atomicOr(p.status, kStatusUnsupported);
+            return;   // uniform over the CTA, before any barrier or TMEM is set up
+        }
+    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     // A tcgen05.commit costs the single MMA thread far more than an MMA, so each key
     // tile g (counted over all items of the CTA) has exactly two: s_full[g % 2] when
@@ -360,6 +371,7 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
     // wait on it, or the in-order completion of S_g after P_{g-2} V, saw the phase
     // before) nor one ahead (the next phase needs work the waiter has not released).
     uint64_t *q_full = bars + 0;
+    uint64_t *q_empty = bars + 1;   // split producer only: an item's last S is done
     uint64_t *k_full = bars + 2;    // [KS]
     uint64_t *k_empty = bars + 6;   // [KS] (KS != 2): one softmax thread arrives once S_g is done
     uint64_t *v_full = bars + 10;   // [VS]
@@ -388,6 +400,7 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < C::KS; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -462,6 +475,9 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
             const int slot = k & 3;
             if (lane == 0 && !mbar_wait(&item_full[slot], (k >> 2) & 1, p.status, abort_flag))
                 stop = 1;
+            // The shuffle carries the flag but orders no memory: the warp barrier makes
+            // lane 0's acquire on item_full cover the other lanes' reads of the slot.
+            __syncwarp();
             stop = __shfl_sync(kFullMask, stop, 0);
             if (stop) return end_item();
             const PrefillItem it = item_q[slot];
@@ -497,13 +513,27 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
             const int kh = w.h / group;
 
             if (!v_only && lane == 0) {
-                // Q is reused once the previous item's last S (tile kv_it - 1) is done
-                if (kv_it > 0 && !mbar_wait(&s_full[(kv_it - 1) & 1], ((kv_it - 1) >> 1) & 1,
-                                            p.status, abort_flag)) {
-                    stop = 1;
+                // Q is reused once the previous item's last S (tile kv_it - 1) is done.
+                // Without a split, this warp's own V loads keep it close behind the MMA:
+                // it issued V_{kv_it-1} after P_{kv_it-3} V was done, which in issue order
+                // means S_{kv_it-2} was done too, so s_full[(kv_it - 1) & 1] is at most one
+                // phase from the awaited one and its parity wait is exact.  A split
+                // producer is throttled only by its K ring (up to three tiles ahead at
+                // head_dim 256), where that barrier may still be two phases back and the
+                // parity wait would pass early; it waits instead on q_empty, which the
+                // MMA thread commits once per item after the item's last S.
+                bool ok_q = true;
+                if constexpr (SPLIT) {
+                    if (n_q > 0) ok_q = mbar_wait(q_empty, (n_q - 1) & 1u, p.status, abort_flag);
                 } else {
-                    mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+                    if (kv_it > 0)
+                        ok_q = mbar_wait(&s_full[(kv_it - 1) & 1], ((kv_it - 1) >> 1) & 1,
+                                         p.status, abort_flag);
                 }
+                if (!ok_q)
+                    stop = 1;
+                else
+                    mbar_arrive_expect_tx(q_full, C::Q_BYTES);
             }
             stop = __shfl_sync(kFullMask, stop, 0);
             if (stop) break;
@@ -697,6 +727,7 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
                                     kd + ((c * C::KV_CHUNK + inner) >> 4), idesc_s, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(&s_full[b]);
+                    if (SPLIT && j == w.n_kv - 1) tc_commit(q_empty);   // the item's Q is free
                     if (j >= 1) issue_pv(g - 1, j - 1, kv_rel, head);
                 }
                 issue_pv(base + w.n_kv - 1, w.n_kv - 1, kv_rel, head);
