@@ -65,7 +65,10 @@
  *    the pool is never dereferenced: the affected tokens contribute nothing and
  *    a device status word records PA_ERR_DEVICE_BOUNDS.  Every pipeline wait
  *    is bounded; a wait that runs out records PA_ERR_TIMEOUT and the kernel
- *    returns.  Read (and clear) that word with pa_get_device_status().
+ *    returns.  A kernel that finds its launch unusable on the device (its
+ *    realigned shared-memory tiles not fitting the launch's shared memory) does
+ *    no work and records PA_ERR_UNSUPPORTED.  Read (and clear) that word with
+ *    pa_get_device_status().
  */
 #ifndef PA_H
 #define PA_H
@@ -212,9 +215,15 @@ int pa_decode_merge(void *out, const int32_t *seq_lens, int num_seqs, int num_q_
  * Arguments and result are those of pa_decode_split without the workspace.
  *  - The first call on a device (with that device current) looks up the
  *    array's device address with cudaGetSymbolAddress; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is cached per device together
+ *    with the id of the CUDA context it was looked up in; after a
+ *    cudaDeviceReset the next call looks it up again (so, after a reset, that
+ *    call too must come before any capture).
  *  - A batch whose pa_decode_split_workspace_size() exceeds
- *    PA_STATIC_SCRATCH_BYTES is rejected with PA_ERR_WORKSPACE.
+ *    PA_STATIC_SCRATCH_BYTES is rejected with PA_ERR_WORKSPACE.  The 16 MiB
+ *    fit a 64-sequence, 32-head, head_dim-128 batch with seq_lens up to 4096
+ *    (about 8.1 MiB of partials); 8 such sequences of up to 131072 tokens need
+ *    about 32.5 MiB and must use pa_decode_split with a workspace.
  *  - All calls on a device share the array, which keeps the last call's
  *    partials; nothing in it needs clearing (each call writes every partition
  *    it later merges).  Calls that overlap on the GPU (e.g. on two streams of
@@ -281,9 +290,10 @@ int pa_ragged_prefill(void *o, const void *q, const void *k, const void *v,
  *   host_table   [num_rows][row_len] int32, the table the caller wants on the
  *                device (any host memory);
  *   snapshot     [num_rows][row_len] int32 PINNED host memory owned by the
- *                caller, holding what was last uploaded (fill it with a value
- *                no row has, e.g. -1, or call once with rows_uploaded == NULL
- *                semantics in mind, before the first sync);
+ *                caller, holding what was last uploaded.  Before the first
+ *                call, fill it with -1 (a value no row holds), so that the
+ *                first call finds every row changed and uploads the whole
+ *                table;
  *   device_table [num_rows][row_len] int32 device memory.
  * Rows of host_table that differ from the snapshot are copied into it, and
  * each run of consecutive changed rows is enqueued on `stream` as one async

@@ -4,6 +4,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+
+#include <cuda.h>
 
 #include "../../include/pa.h"
 #include "pa_device.cuh"
@@ -44,20 +47,27 @@ namespace {
 __device__ int g_status_word;
 
 constexpr int kMaxDevices = 64;
-int *g_status_ptr[kMaxDevices] = {nullptr};
+struct CachedStatus {
+    unsigned long long ctx;   // context the address belongs to (0: do not reuse)
+    int *ptr;
+};
+CachedStatus g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mutex;
 
 int status_ptr(int **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device %d", dev);
-    if (!g_status_ptr[dev]) {
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    const unsigned long long ctx = pa::current_context_id();
+    if (ctx == 0 || g_status_ptr[dev].ctx != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_status_word);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
-        g_status_ptr[dev] = static_cast<int *>(p);
+        g_status_ptr[dev] = {pa::current_context_id(), static_cast<int *>(p)};
     }
-    *out = g_status_ptr[dev];
+    *out = g_status_ptr[dev].ptr;
     return PA_OK;
 }
 
@@ -160,6 +170,33 @@ int decode_common(pa::DecodeParams &p, void *out, const void *q, const void *k_c
 int pa::set_error(int code, const char *msg) { return fail(code, "%s", msg); }
 
 int pa::api_status_ptr(int **out) { return status_ptr(out); }
+
+unsigned long long pa::current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault,
+                                             &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+                cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<GetCurrentFn>(a);
+            get_id = reinterpret_cast<GetIdFn>(b);
+        }
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 extern "C" {
 

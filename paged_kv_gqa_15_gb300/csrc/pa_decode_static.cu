@@ -12,8 +12,15 @@
 // array of PA_STATIC_SCRATCH_BYTES.  Host code cannot pass the array's name to
 // a kernel (on the host it only names a stand-in), so the first call on each
 // device, with that device current, asks the runtime for the array's device
-// address with cudaGetSymbolAddress and caches it; every call then runs the
-// regular pa_decode_split with that address as its workspace.
+// address with cudaGetSymbolAddress and caches it with the id of the CUDA
+// context it belongs to (a later context, after cudaDeviceReset, looks it up
+// again); every call then runs the regular pa_decode_split with that address
+// as its workspace.
+//
+// Size: the 16 MiB hold the split partials of the 64-sequence Llama-3-8B decode
+// batch (seq_lens up to 4096: about 8.1 MiB) and of the 4-sequence tiny batch;
+// the 8-sequence long-context batch (seq_lens up to 131072, about 32.5 MiB of
+// partials) does not fit and must use pa_decode_split with a workspace.
 #include <mutex>
 
 #include "../../include/pa.h"
@@ -25,10 +32,16 @@ namespace {
 static __device__ __align__(256) unsigned char g_split_scratch[PA_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {nullptr};
+struct CachedScratch {
+    unsigned long long ctx;   // context the address belongs to (0: do not reuse)
+    void *ptr;
+};
+CachedScratch g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 
-// Device address of g_split_scratch on the current device (looked up once per device).
+// Device address of g_split_scratch on the current device, looked up once per device
+// and context: after cudaDeviceReset the next context may place the array elsewhere,
+// so an address cached under an earlier context is looked up again.
 int scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -36,15 +49,16 @@ int scratch_address(void **out) {
     if (dev < 0 || dev >= kMaxDevices)
         return pa::set_error(PA_ERR_UNSUPPORTED, "device ordinal out of range");
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    const unsigned long long ctx = pa::current_context_id();
+    if (ctx == 0 || g_scratch_addr[dev].ctx != ctx) {
         void *ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_split_scratch);
         if (e != cudaSuccess || ptr == nullptr)
             return pa::set_error(PA_ERR_CUDA,
                                  "cudaGetSymbolAddress of the static split scratch failed");
-        g_scratch_addr[dev] = ptr;
+        g_scratch_addr[dev] = {pa::current_context_id(), ptr};
     }
-    *out = g_scratch_addr[dev];
+    *out = g_scratch_addr[dev].ptr;
     return PA_OK;
 }
 

@@ -106,5 +106,9 @@ cudaError_t launch_prefill(PrefillParams &p, const PrefillLaunch &L, cudaStream_
 int set_error(int code, const char *msg);
 // Device address of the current device's status word (PA_OK or an error status).
 int api_status_ptr(int **out);
+// Unique id of the CUDA context current on this thread, or 0 if there is none or the
+// driver cannot say.  A device address cached under one id is stale under another
+// (cudaDeviceReset tears the context down; the next one may load the module elsewhere).
+unsigned long long current_context_id();
 
 }  // namespace pa
