@@ -6,10 +6,20 @@ on the Llama-3-8B-shaped decode workload (64 sequences, 32 q / 8 kv heads,
 head_dim 128, 16-token pages, seq_lens U[512, 4096], shuffled block tables).
 The metric is decode KV-bytes GB/s (K and V of every visible token per step).
 The other workloads (long-context split decode, tiny decode, ragged prefill,
-chunked paged prefill) are measured in the same run and reported under
-"workloads", each with its own roofline.
+chunked paged prefill, and the legs of the sliding window, the FP8 cache, the
+single pass, the ungrouped split and the page copies) are measured in the same
+run.  Each is then checked on its whole output against the fp64 CPU oracle,
+which is timed on the host cores doing so (outside every GPU-timed region).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Output: one JSON line on stdout.  Its last key, "configs", summarises the five
+named workloads (step throughput, kernel time, roofline fractions of the
+measured and the nominal peak, median / min step time over 30 individually
+timed steps, the oracle's throughput on all host cores and on one, and the
+max / mean absolute error of the whole output against the oracle); "next", just
+before it, does the same for the other legs.  The full per-workload records go
+to stderr as one JSON line.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (no
 data-path collective); the step time is the max over ranks and `value` is the
@@ -38,6 +48,19 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode KV HBM GB/s & ragged prefill TFLOP/s, as fraction of GB300 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal peaks of one GB300, the denominators the decode and prefill targets are stated
+# against: HBM3e at 8 TB/s, and dense BF16 tensor throughput of 2.25 PFLOP/s (NVIDIA's
+# HGX B300 specification gives 36 PFLOPS FP16/BF16 per 8 GPUs with 2:4 sparsity, i.e.
+# 4.5 sparse = 2.25 dense per GPU).
+NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
+# The targets: decode at >= 70 % of nominal HBM on the long-context workload, ragged
+# prefill at >= 50 % of the nominal dense BF16 peak.
+TARGETS = {"long_context_decode": 0.70, "ragged_prefill": 0.50}
+# The five named workloads, by their index in the workload list.
+CONFIGS = {"tiny_decode": 1, "llama8b_decode": 2, "long_context_decode": 3,
+           "ragged_prefill": 4, "chunked_paged_prefill": 5}
+STAT_REPS = 30          # individually timed steps behind the median / min figures
+PARITY_MAX_ABS, PARITY_MEAN_ABS = 2e-2, 2e-3
 
 # DRAM bytes (read + write) per launch from ncu captures, keyed by kernel, valid only
 # for the source file hash they were measured on (otherwise reported as null).
@@ -121,7 +144,10 @@ def aggregate_throughput(units_per_step_local: float, ms_per_step_local: float, 
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons with nvidia-smi while running.  Samples
+    are time-stamped; `phase()` brackets a GPU-timed interval, and `summary_of_phases()`
+    keeps only the samples taken inside such intervals (host-only work in between, such
+    as the oracle legs, would otherwise add idle clocks)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -131,7 +157,8 @@ class ClockSampler:
         self.gpu_id = gpu_id
         self.interval_ms = interval_ms
         self.proc = None
-        self.lines = []
+        self.lines = []           # (monotonic time, csv line)
+        self.phases = []          # (start, end) of GPU-timed intervals
 
     def start(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -149,11 +176,26 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
-    def stop(self):
+    class _Phase:
+        def __init__(self, owner):
+            self.owner = owner
+
+        def __enter__(self):
+            self.t0 = time.monotonic()
+            return self
+
+        def __exit__(self, *exc):
+            self.owner.phases.append((self.t0, time.monotonic()))
+            return False
+
+    def phase(self):
+        return ClockSampler._Phase(self)
+
+    def _stop_proc(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return False
         time.sleep(self.interval_ms / 1000.0 * 2)
         self.proc.terminate()
         try:
@@ -161,7 +203,24 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        return self.summary(self.lines)
+        return True
+
+    def stop(self):
+        if not self._stop_proc():
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        return self.summary([ln for _, ln in self.lines])
+
+    def phase_lines(self):
+        """The samples taken inside a GPU-timed phase (with one sampling interval of
+        slack on either side)."""
+        slack = self.interval_ms / 1000.0
+        return [ln for t, ln in self.lines
+                if any(a - slack <= t <= b + slack for a, b in self.phases)]
+
+    def summary_of_phases(self):
+        if not self._stop_proc():
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        return self.summary(self.phase_lines())
 
     @staticmethod
     def summary(lines):
@@ -268,14 +327,23 @@ def flush_l2(stream, device):
         buf.sum(dtype=torch.int64)
 
 
-def time_steps(step, steps, warmup, stream, device, labels, flush=False):
+def step_stats(ms_list):
+    """Median, min, max and mean of individually timed steps (ms)."""
+    return {"reps": len(ms_list), "median_ms": round(statistics.median(ms_list), 5),
+            "min_ms": round(min(ms_list), 5), "max_ms": round(max(ms_list), 5),
+            "mean_ms": round(sum(ms_list) / len(ms_list), 5)}
+
+
+def time_steps(step, steps, warmup, stream, device, labels, flush=False, reps=STAT_REPS):
     """Warm up, then time exactly `steps` steps with CUDA events on `stream`.
     Without flush the step time comes from one pass with events only around the whole
     loop; with flush, L2 is flushed before every step, outside the timed intervals, and
     each step is timed on its own between two events.  Either way no event sits between
-    a step's kernels, so the dependent launches overlap as in use.  A second pass of
-    `steps` steps with an event after every kernel gives the per-kernel times.
-    Returns (ms per step, {label: avg ms}, launches per timed pass)."""
+    a step's kernels, so the dependent launches overlap as in use.  A second pass times
+    `reps` steps one by one (flushed the same way) for the median / min figures, and a
+    third pass of `steps` steps with an event after every kernel gives the per-kernel
+    times.  Returns {"ms": ms per step, "per": {label: avg ms}, "launches": launches of
+    the timed pass, "stats": step_stats of the second pass}."""
     import torch.distributed as dist
     for _ in range(warmup):
         if flush:
@@ -285,10 +353,11 @@ def time_steps(step, steps, warmup, stream, device, labels, flush=False):
     if dist.is_available() and dist.is_initialized():
         dist.barrier()
     torch.cuda.synchronize()
+    launches = 0
     if not flush:
         start = _ev(stream)
         for _ in range(steps):
-            step(None)
+            launches += step(None)
         end = _ev(stream)
         torch.cuda.synchronize()
         ms_whole = start.elapsed_time(end) / steps
@@ -297,17 +366,27 @@ def time_steps(step, steps, warmup, stream, device, labels, flush=False):
         for _ in range(steps):
             flush_l2(stream, device)
             a = _ev(stream)
-            step(None)
+            launches += step(None)
             spans.append((a, _ev(stream)))
         torch.cuda.synchronize()
         ms_whole = sum(a.elapsed_time(b) for a, b in spans) / steps
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+    spans = []
+    for _ in range(reps):
+        if flush:
+            flush_l2(stream, device)
+        a = _ev(stream)
+        step(None)
+        spans.append((a, _ev(stream)))
+    torch.cuda.synchronize()
+    stats = step_stats([a.elapsed_time(b) for a, b in spans])
     all_evs = []
-    launches = 0
     for _ in range(steps):
         if flush:
             flush_l2(stream, device)
         evs = []
-        launches += step(evs)
+        step(evs)
         all_evs.append(evs)
     torch.cuda.synchronize()
     if dist.is_available() and dist.is_initialized():
@@ -317,7 +396,7 @@ def time_steps(step, steps, warmup, stream, device, labels, flush=False):
         for i, l in enumerate(labels):
             per[l] += evs[i].elapsed_time(evs[i + 1])
     per = {l: v / steps for l, v in per.items()}
-    return ms_whole, per, launches
+    return {"ms": ms_whole, "per": per, "launches": launches, "stats": stats}
 
 
 def decode_footprint(w):
@@ -331,8 +410,25 @@ def prefill_footprint(w):
     return qo + 2 * w.total_kv * w.num_kv_heads * w.head_dim * 2
 
 
-def bench_decode(w, steps, warmup, dev, stream, peaks, peak_kind):
+def nominal_frac(achieved, bound):
+    peak = NOMINAL["hbm_gbs"] if bound == "hbm" else NOMINAL["bf16_tflops"]
+    return round(achieved / peak, 4)
+
+
+def decode_kernel_sources(w):
+    if not w.split:
+        return ("pa_decode_kernel.cuh", "pa_device.cuh")
+    if w.head_dim == 128 and w.num_q_heads // w.num_kv_heads in (4, 8):
+        return (("pa_decode_tc_fp8.cu" if w.kv_fp8 else "pa_decode_tc.cu"), "pa_tcgen05.cuh",
+                "pa_device.cuh")
+    return ("pa_decode_kernel.cuh", "pa_device.cuh")
+
+
+def bench_decode(w, steps, warmup, dev, stream, peaks, peak_kind, snapshot=False):
+    """Times the decode step of workload w.  With snapshot, the step's inputs are copied
+    to the host first (for the oracle leg) and the step's output after the timing."""
     s = decode_setup(w, dev)
+    snap = decode_snapshot(w, s) if snapshot else None
     flush = decode_footprint(w) < L2_FLUSH_BYTES
     labels = (["write_cache"] if w.new_token_write else []) + (
         ["decode_partitions", "decode_merge"] if w.split else ["decode"])
@@ -340,22 +436,40 @@ def bench_decode(w, steps, warmup, dev, stream, peaks, peak_kind):
     def step(evs):
         return decode_step(w, s, stream, evs)
 
-    ms, per, launches = time_steps(step, steps, warmup, stream, dev, labels, flush)
+    tm = time_steps(step, steps, warmup, stream, dev, labels, flush)
     kv = w.kv_bytes()
-    value, ms_max = aggregate_throughput(kv, ms, dev)
-    kern_ms = per["decode_partitions" if w.split else "decode"]
-    src = (("pa_decode_tc_fp8.cu" if w.kv_fp8 else "pa_decode_tc.cu"), "pa_tcgen05.cuh",
-           "pa_device.cuh") if w.split else ("pa_decode_kernel.cuh", "pa_device.cuh")
+    value, ms_max = aggregate_throughput(kv, tm["ms"], dev)
+    kern_ms = tm["per"]["decode_partitions" if w.split else "decode"]
+    achieved = kv / (kern_ms / 1e3) / 1e9
     res = {
         "value": value / 1e9, "unit": "GB/s", "ms_per_step": ms_max,
-        "kv_bytes_per_step": kv, "launches": launches,
-        "kernels_ms": {k: round(v, 5) for k, v in per.items()},
-        "roofline": roofline("hbm", kv / (kern_ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s",
-                             traffic_for("decode_partitions:" + w.name, src), peak_kind),
-        "roofline_nominal_frac": round(kv / (kern_ms / 1e3) / 1e9 / 8000.0, 4),
+        "kv_bytes_per_step": kv, "launches": tm["launches"], "step_stats": tm["stats"],
+        "kernels_ms": {k: round(v, 5) for k, v in tm["per"].items()},
+        "roofline": roofline("hbm", achieved, peaks["hbm_gbs"], "GB/s",
+                             traffic_for("decode_partitions:" + w.name,
+                                         decode_kernel_sources(w)), peak_kind),
+        "roofline_nominal_frac": nominal_frac(achieved, "hbm"),
     }
+    if snap is not None:
+        snap["out"] = W_bits(s["out"])
     res["graph"] = bench_decode_graph(w, s, steps, warmup, dev, stream, flush)
-    return res, s
+    return res, s, snap
+
+
+def W_bits(t):
+    from paged_kv_gqa_15_gb300 import workloads as W
+    return W.to_bits(t)
+
+
+def decode_snapshot(w, s):
+    """Host copies of a decode step's inputs, before any step ran: q and the new rows
+    as bf16 bits, the pools as bf16 bits or E4M3 codes."""
+    t = s["t"]
+    snap = {"q": W_bits(t["q"]), "k_cache": host_pool(w, t["k_cache"]),
+            "v_cache": host_pool(w, t["v_cache"])}
+    if w.new_token_write:
+        snap["k_new"], snap["v_new"] = W_bits(t["k_new"]), W_bits(t["v_new"])
+    return snap
 
 
 def bench_decode_graph(w, s, steps, warmup, dev, stream, flush):
@@ -378,11 +492,11 @@ def bench_decode_graph(w, s, steps, warmup, dev, stream, flush):
             evs.append(_ev(stream))
         return n
 
-    ms, _, _ = time_steps(replay, steps, warmup, stream, dev, ["step"], flush)
-    value, ms_max = aggregate_throughput(w.kv_bytes(), ms, dev)
+    tm = time_steps(replay, steps, warmup, stream, dev, ["step"], flush)
+    value, ms_max = aggregate_throughput(w.kv_bytes(), tm["ms"], dev)
     del graph
     return {"value": round(value / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms_max, 5),
-            "kernels_per_replay": n}
+            "kernels_per_replay": n, "median_ms": tm["stats"]["median_ms"]}
 
 
 def bench_decode_e2e(w, s, steps, warmup, dev, stream):
@@ -482,50 +596,73 @@ def bench_decode_e2e(w, s, steps, warmup, dev, stream):
                           "overlap the previous step's kernels"}
 
 
-def bench_prefill(w, steps, warmup, dev, stream, peaks, peak_kind):
+def prefill_setup(w, dev):
     import paged_kv_gqa_15_gb300 as pa
     t = w.tensors(dev)
-    qo_d = torch.from_numpy(w.qo_indptr).to(dev)
-    kv_d = torch.from_numpy(w.kv_indptr).to(dev)
-    o = torch.empty_like(t["q"])
-    ws = pa.alloc_workspace(pa.ragged_prefill_workspace_size(w.batch, w.total_qo, w.num_q_heads,
-                                                             w.head_dim), dev)
-    bt = torch.from_numpy(w.block_tables).to(dev) if w.paged else None
-    slots = torch.from_numpy(w.chunk_slot_mapping).to(dev) if w.chunk_write else None
+    return {"t": t,
+            "qo_d": torch.from_numpy(w.qo_indptr).to(dev),
+            "kv_d": torch.from_numpy(w.kv_indptr).to(dev),
+            "out": torch.empty_like(t["q"]),
+            "ws": pa.alloc_workspace(pa.ragged_prefill_workspace_size(
+                w.batch, w.total_qo, w.num_q_heads, w.head_dim), dev),
+            "bt": torch.from_numpy(w.block_tables).to(dev) if w.paged else None,
+            "slots": torch.from_numpy(w.chunk_slot_mapping).to(dev) if w.chunk_write else None}
+
+
+def prefill_step(w, s, stream, evs=None):
+    """One prefill step: the chunk's cache write (paged chunked prefill), then the ragged
+    prefill; records an event after each kernel when evs is a list."""
+    import paged_kv_gqa_15_gb300 as pa
+    t = s["t"]
+    n = 0
+    if evs is not None:
+        evs.append(_ev(stream))
+    if w.chunk_write:
+        pa.pa_write_cache(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], s["slots"],
+                          stream=stream)
+        n += 1
+        if evs is not None:
+            evs.append(_ev(stream))
+    k = t["k_cache"] if w.paged else t["k"]
+    v = t["v_cache"] if w.paged else t["v"]
+    pa.pa_ragged_prefill(s["out"], t["q"], k, v, w.qo_indptr, w.kv_indptr, s["qo_d"],
+                         s["kv_d"], w.scale, causal=w.causal, block_tables=s["bt"],
+                         workspace=s["ws"], stream=stream, sliding_window=w.window)
+    if evs is not None:
+        evs.append(_ev(stream))
+    return n + 1
+
+
+def bench_prefill(w, steps, warmup, dev, stream, peaks, peak_kind, snapshot=False):
+    """Times the prefill step of workload w (with its chunk's cache write if it has one).
+    With snapshot, the inputs go to the host first and the output after the timing."""
+    s = prefill_setup(w, dev)
+    snap = prefill_snapshot(w, s["t"]) if snapshot else None
     labels = (["write_cache"] if w.chunk_write else []) + ["ragged_prefill"]
 
     def step(evs):
-        n = 0
-        if evs is not None:
-            evs.append(_ev(stream))
-        if w.chunk_write:
-            pa.pa_write_cache(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], slots,
-                              stream=stream)
-            n += 1
-            if evs is not None:
-                evs.append(_ev(stream))
-        k = t["k_cache"] if w.paged else t["k"]
-        v = t["v_cache"] if w.paged else t["v"]
-        pa.pa_ragged_prefill(o, t["q"], k, v, w.qo_indptr, w.kv_indptr, qo_d, kv_d, w.scale,
-                             causal=w.causal, block_tables=bt, workspace=ws, stream=stream,
-                             sliding_window=w.window)
-        if evs is not None:
-            evs.append(_ev(stream))
-        return n + 1
+        return prefill_step(w, s, stream, evs)
 
-    ms, per, launches = time_steps(step, steps, warmup, stream, dev, labels,
-                                   prefill_footprint(w) < L2_FLUSH_BYTES)
+    tm = time_steps(step, steps, warmup, stream, dev, labels,
+                    prefill_footprint(w) < L2_FLUSH_BYTES)
     flops = w.flops()
-    value, ms_max = aggregate_throughput(flops, ms, dev)
-    kern_ms = per["ragged_prefill"]
+    value, ms_max = aggregate_throughput(flops, tm["ms"], dev)
+    kern_ms = tm["per"]["ragged_prefill"]
     achieved = flops / (kern_ms / 1e3) / 1e12
+    if snap is not None:
+        snap["out"] = W_bits(s["out"])
     return {"value": value / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_max,
-            "flops_per_step": flops, "launches": launches,
-            "kernels_ms": {k: round(v, 5) for k, v in per.items()},
+            "flops_per_step": flops, "launches": tm["launches"], "step_stats": tm["stats"],
+            "kernels_ms": {k: round(v, 5) for k, v in tm["per"].items()},
             "roofline": roofline("tensor", achieved, peaks["bf16_tflops"], "TFLOP/s",
                                  traffic_for("ragged_prefill:" + w.name,
                                              ("pa_prefill.cu", "pa_device.cuh")), peak_kind),
-            "roofline_nominal_frac": round(achieved / 2250.0, 4)}
+            "roofline_nominal_frac": nominal_frac(achieved, "tensor")}, snap
+
+
+def prefill_snapshot(w, t):
+    """Host copies of a prefill step's inputs (bf16 bits), before any step ran."""
+    return {n: W_bits(v) for n, v in t.items()}
 
 
 # Page-copy legs: a Llama-3-8B-shaped cache (32 layers x K and V pools of 1024
@@ -557,6 +694,7 @@ def bench_blocks(name, steps, warmup, dev, stream, peaks, peak_kind):
                          device=dev).normal_() for _ in range(2 * BLOCK_LAYERS)]
     page_bytes = int(np.prod(BLOCK_PAGE)) * 2
     moved = BLOCK_PAIRS * len(pools) * page_bytes          # bytes of pages per call
+    stats = {}
 
     def timed(call, label):
         def step(evs):
@@ -566,8 +704,9 @@ def bench_blocks(name, steps, warmup, dev, stream, peaks, peak_kind):
             if evs is not None:
                 evs.append(_ev(stream))
             return 1
-        ms, _, n = time_steps(step, steps, warmup, stream, dev, [label])
-        return ms, n
+        tm = time_steps(step, steps, warmup, stream, dev, [label])
+        stats[label] = tm["stats"]
+        return tm["ms"], tm["launches"]
 
     if name == "copy_blocks_fork":
         pairs = np.stack([perm[:BLOCK_PAIRS], perm[BLOCK_PAIRS:2 * BLOCK_PAIRS]], 1)
@@ -575,11 +714,14 @@ def bench_blocks(name, steps, warmup, dev, stream, peaks, peak_kind):
         ms, n = timed(lambda: pa.pa_copy_blocks(pools[0::2], pools[1::2], m, stream=stream),
                       "copy_blocks")
         hbm = 2 * moved / (ms / 1e3) / 1e9                  # read + write
+        st = stats["copy_blocks"]
         return {"value": round(hbm, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
-                "bytes_per_step": 2 * moved, "launches": n,
+                "bytes_per_step": 2 * moved, "launches": n, "step_stats": st,
+                "median_GB/s": round(2 * moved / (st["median_ms"] / 1e3) / 1e9, 2),
+                "max_GB/s": round(2 * moved / (st["min_ms"] / 1e3) / 1e9, 2),
                 "kernels_ms": {"copy_blocks": round(ms, 5)},
                 "roofline": roofline("hbm", hbm, peaks["hbm_gbs"], "GB/s", None, peak_kind),
-                "roofline_nominal_frac": round(hbm / 8000.0, 4),
+                "roofline_nominal_frac": nominal_frac(hbm, "hbm"),
                 "config": blocks_config(name)}
 
     host = [torch.empty((BLOCK_PAIRS,) + BLOCK_PAGE, dtype=torch.bfloat16).pin_memory()
@@ -612,6 +754,7 @@ def bench_blocks(name, steps, warmup, dev, stream, peaks, peak_kind):
             "kernels_ms": {"swap_out": round(ms_out, 5), "swap_in": round(ms_in, 5)},
             "out": {"GB/s": round(gbs(ms_out), 2), "copy_engine_GB/s": round(gbs(ce_out), 2)},
             "in": {"GB/s": round(gbs(ms_in), 2), "copy_engine_GB/s": round(gbs(ce_in), 2)},
+            "step_stats": {"swap_out": stats["swap_out"], "swap_in": stats["swap_in"]},
             "roofline": rl, "config": blocks_config(name)}
 
 
@@ -650,6 +793,71 @@ def oracle_decode_sample(w, t_host, target_s=12.0, nthreads=None):
         d, b = oracle_decode_time(w, t_host, np.arange(n), nthreads)
         dt, kv, passes = dt + d, kv + b, passes + 1
     return kv / dt / 1e9, dt, n, passes, nthreads
+
+
+def _parity(got_bits, ref):
+    """Max / mean absolute error of a bf16 output (bits) against the fp64 oracle, over
+    every element; ok when both are inside the bounds the tests use."""
+    from paged_kv_gqa_15_gb300 import workloads as W
+    got = W.bits_to_float(got_bits).astype(np.float64)
+    finite = bool(np.isfinite(got).all())
+    err = np.abs(got - ref)
+    mx, mean = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
+    return {"max_abs": round(mx, 6), "mean_abs": round(mean, 7), "elements": int(err.size),
+            "ok": finite and mx <= PARITY_MAX_ABS and mean <= PARITY_MEAN_ABS}
+
+
+def oracle_leg(w, snap, one_thread=False, target_1t_s=3.0):
+    """The fp64 oracle run once over the whole workload on all host cores, on the host
+    copies of the step's inputs: the step's cache write (if any), then the attention.
+    That run is timed (the oracle's throughput in the workload's unit) and its result is
+    compared with the GPU step's output on every element.  With one_thread, the oracle
+    is also timed on one thread over a bounded sample (whole sequences, about
+    target_1t_s seconds)."""
+    import oracle
+    from paged_kv_gqa_15_gb300 import workloads as W
+    th = oracle.default_threads()
+    scales = dict(k_scale=FP8_SCALE, v_scale=FP8_SCALE)
+    if isinstance(w, W.DecodeWorkload):
+        kc, vc = snap["k_cache"], snap["v_cache"]
+        t0 = time.perf_counter()
+        if w.new_token_write:
+            oracle.write_cache(snap["k_new"], snap["v_new"], kc, vc, w.slot_mapping,
+                               w.block_size, kv_fp8=w.kv_fp8, **scales)
+        ref = oracle.decode(snap["q"], kc, vc, w.block_tables, w.seq_lens, w.num_kv_heads,
+                            w.block_size, w.scale, nthreads=th, window=w.window,
+                            kv_fp8=w.kv_fp8, **scales)
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(w.kv_bytes() / dt / 1e9, 4), "unit": "GB/s", "cores": th,
+               "kind": "oracle", "seconds": round(dt, 3),
+               "sample": "the whole workload once (cache write + decode of every sequence "
+                         "and head)"}
+        if one_thread:
+            n, dt1, kv1 = 0, 0.0, 0
+            while n < w.batch and dt1 < target_1t_s:
+                d, b = oracle_decode_time(w, (snap["q"], kc, vc), [n], 1)
+                dt1, kv1, n = dt1 + d, kv1 + b, n + 1
+            cpu["one_thread"] = {"value": round(kv1 / dt1 / 1e9, 4), "unit": "GB/s",
+                                 "sample": f"{n} of {w.batch} sequences, {dt1:.1f} s"}
+    else:
+        q = snap["q"]
+        t0 = time.perf_counter()
+        if w.paged:
+            k, v = snap["k_cache"], snap["v_cache"]
+            if w.chunk_write:
+                oracle.write_cache(snap["k_new"], snap["v_new"], k, v, w.chunk_slot_mapping,
+                                   w.block_size)
+        else:
+            k, v = snap["k"], snap["v"]
+        ref = oracle.prefill(q, k, v, w.qo_indptr, w.kv_indptr, w.num_kv_heads, w.scale,
+                             causal=w.causal, block_tables=w.block_tables if w.paged else None,
+                             block_size=w.block_size, nthreads=th, window=w.window)
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(w.flops() / dt / 1e12, 5), "unit": "TFLOP/s", "cores": th,
+               "kind": "oracle", "seconds": round(dt, 3),
+               "sample": "the whole workload once (every query row and head" +
+                         (", after the chunk's cache write)" if w.chunk_write else ")")}
+    return cpu, _parity(snap["out"], ref)
 
 
 def host_pool(w, pool):
@@ -740,6 +948,39 @@ def workload_config(w):
 
 # ---------------------------------------------------------------------------------------
 
+def compact(name, r):
+    """A short summary of one workload's record, for the tail of the printed line."""
+    if "unavailable" in r:
+        return {"unavailable": r["unavailable"]}
+    e = {r["unit"]: round(r["value"], 2)}
+    rl = r.get("roofline") or {}
+    km = r.get("kernels_ms") or {}
+    main_k = next((k for k in ("decode_partitions", "decode", "ragged_prefill", "copy_blocks")
+                   if k in km), None)
+    if main_k:
+        e["kernel_ms"] = km[main_k]
+    if rl.get("frac") is not None:
+        e["frac"] = rl["frac"]
+    if "roofline_nominal_frac" in r:
+        e["frac_nominal"] = r["roofline_nominal_frac"]
+    st = r.get("step_stats") or {}
+    if "median_ms" in st:
+        e["median_ms"], e["min_ms"] = st["median_ms"], st["min_ms"]
+    if name in TARGETS:
+        e["target_nominal"] = TARGETS[name]
+        e["met"] = r.get("roofline_nominal_frac", 0) >= TARGETS[name]
+    cpu = r.get("cpu")
+    if cpu:
+        e["oracle"] = cpu["value"]
+        e["oracle_cores"] = cpu["cores"]
+        if "one_thread" in cpu:
+            e["oracle_1t"] = cpu["one_thread"]["value"]
+    par = r.get("parity")
+    if par:
+        e["max_abs"], e["mean_abs"], e["parity_ok"] = par["max_abs"], par["mean_abs"], par["ok"]
+    return e
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -747,12 +988,14 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_decode")
-    ap.add_argument("--extra", default="long_context_decode,tiny_decode,ragged_prefill,"
+    ap.add_argument("--extra", default="tiny_decode,long_context_decode,ragged_prefill,"
                                        "chunked_paged_prefill,window_decode,window_prefill,"
                                        "llama8b_decode_fp8,long_context_decode_fp8,"
+                                       "llama8b_decode_single,mha_decode,"
                                        "copy_blocks_fork,swap_blocks",
                     help="other workloads measured in the same run (N=1 only); 'none' for none")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle legs (timing and whole-output parity)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
@@ -786,49 +1029,68 @@ def main(argv=None):
         uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
     except Exception:
         uuid = None
+    oracle_on = rank == 0 and world == 1 and not args.no_cpu_baseline
 
     clocks = ClockSampler(uuid)
     clocks.start()
     is_decode = isinstance(w, W.DecodeWorkload)
     if is_decode:
-        res, state = bench_decode(w, args.steps, args.warmup, dev, stream, peaks, peak_kind)
+        res, state, snap = bench_decode(w, args.steps, args.warmup, dev, stream, peaks,
+                                        peak_kind, snapshot=oracle_on)
     else:
-        res, state = bench_prefill(w, args.steps, args.warmup, dev, stream, peaks,
-                                   peak_kind), None
+        (res, snap), state = bench_prefill(w, args.steps, args.warmup, dev, stream, peaks,
+                                           peak_kind, snapshot=oracle_on), None
     clk_main = clocks.stop()
     e2e = bench_decode_e2e(w, state, args.steps, args.warmup, dev, stream) if is_decode else None
     status = pa.device_status(stream)
+    if snap is not None:
+        res["cpu"], res["parity"] = oracle_leg(w, snap, one_thread=args.workload in
+                                               ("tiny_decode", "llama8b_decode",
+                                                "long_context_decode"))
+        del snap
+    records = {args.workload: res}
+
     clocks_all = ClockSampler(uuid)
     clocks_all.start()
-
-    extra = {}
     if world == 1 and args.extra:
         for name in [x for x in args.extra.split(",") if x and x not in ("none", args.workload)]:
             if name in BLOCK_LEGS:
-                extra[name] = bench_blocks(name, max(3, min(args.steps, 50)), args.warmup, dev,
-                                           stream, peaks, peak_kind)
+                with clocks_all.phase():
+                    records[name] = bench_blocks(name, max(STAT_REPS, min(args.steps, 50)),
+                                                 args.warmup, dev, stream, peaks, peak_kind)
                 torch.cuda.empty_cache()
                 continue
             wx = W.WORKLOADS[name]()
+            snap = None
             try:
-                if isinstance(wx, W.DecodeWorkload):
-                    steps = max(3, min(args.steps, 50)) if wx.kv_bytes() > 1e9 else args.steps
-                    r, _ = bench_decode(wx, steps, args.warmup, dev, stream, peaks, peak_kind)
-                else:
-                    r = bench_prefill(wx, max(3, min(args.steps, 50)), args.warmup, dev, stream,
-                                      peaks, peak_kind)
+                with clocks_all.phase():
+                    if isinstance(wx, W.DecodeWorkload):
+                        steps = max(3, min(args.steps, 50)) if wx.kv_bytes() > 1e9 \
+                            else args.steps
+                        r, _, snap = bench_decode(wx, steps, args.warmup, dev, stream, peaks,
+                                                  peak_kind, snapshot=oracle_on)
+                    else:
+                        r, snap = bench_prefill(wx, max(3, min(args.steps, 50)), args.warmup,
+                                                dev, stream, peaks, peak_kind,
+                                                snapshot=oracle_on)
                 r["config"] = workload_config(wx)
-                extra[name] = r
+                records[name] = r
             except pa.PaError as e:
-                extra[name] = {"unavailable": str(e)}
+                records[name] = {"unavailable": str(e)}
             torch.cuda.empty_cache()
+            if snap is not None:     # host-only work, outside the clock phases
+                records[name]["cpu"], records[name]["parity"] = oracle_leg(
+                    wx, snap, one_thread=CONFIGS.get(name, 0) in (1, 2, 3))
+                del snap
         status |= pa.device_status(stream)
-    clk_all = clocks_all.stop()
+    clk_all = clocks_all.summary_of_phases()
     clk = dict(clk_main)
     clk["extra_workloads"] = clk_all
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and is_decode:
+    if oracle_on and is_decode:
+        # the contract's CPU baseline: the oracle on the headline workload, whole passes
+        # repeated for about 12 s (the single pass above is too short to time alone)
         t = state["t"]
         host = host_decode_inputs(w, t)
         gbs, dt, n, passes, th = oracle_decode_sample(w, host)
@@ -837,6 +1099,11 @@ def main(argv=None):
                          f"pass(es) (all {w.num_q_heads} heads, {dt:.1f} s)"}
 
     if rank == 0:
+        configs = {f"c{CONFIGS[n]}_{n}": compact(n, r)
+                   for n, r in sorted(records.items(), key=lambda kv: CONFIGS.get(kv[0], 0))
+                   if n in CONFIGS}
+        nxt = {n: compact(n, r) for n, r in records.items() if n not in CONFIGS}
+        parity_ok = all(r.get("parity", {}).get("ok", True) for r in records.values())
         line = {
             "metric": METRIC, "value": round(res["value"], 3), "unit": res["unit"],
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -844,11 +1111,17 @@ def main(argv=None):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
             "data": "synthetic", "config": workload_config(w),
             "roofline": res["roofline"], "roofline_nominal_frac": res["roofline_nominal_frac"],
-            "kernels_ms": res["kernels_ms"], "cpu_baseline": cpu, "e2e": e2e,
+            "kernels_ms": res["kernels_ms"], "step_stats": res["step_stats"],
+            "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": res["launches"], "clocks": clk, "device_status": status,
             "graph": res.get("graph"),
-            "workloads": extra,
+            "parity_all_ok": parity_ok if oracle_on else None,
+            "nominal_peaks": NOMINAL,
+            "next": nxt,
+            "configs": configs,
         }
+        sys.stderr.write("bench records: " + json.dumps(records, default=float) + "\n")
+        sys.stderr.flush()
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -346,6 +346,24 @@ def window_prefill():
                         seed=1006, window=1024)
 
 
+def llama8b_decode_single():
+    """llama8b_decode (the same sequences, pages and new token) through the single-pass
+    pa_decode: one pass over each whole sequence per (sequence, kv head), no split."""
+    rng = np.random.default_rng(1001)
+    lens = rng.integers(512, 4096, size=64, endpoint=True)
+    return make_decode("llama8b_decode_single_b64_h32kv8_d128", lens, 32, 8, 128, seed=1001,
+                       new_token_write=True, split=False)
+
+
+def mha_decode():
+    """Split-KV decode without grouping, shaped like Llama-2-7B (32 q / 32 kv heads,
+    hd 128): batch 32, seq_lens U[512, 4096]."""
+    rng = np.random.default_rng(1007)
+    lens = rng.integers(512, 4096, size=32, endpoint=True)
+    return make_decode("mha_decode_b32_h32kv32_d128", lens, 32, 32, 128, seed=1007,
+                       split=True)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama8b_decode": llama8b_decode,
@@ -356,4 +374,6 @@ WORKLOADS = {
     "llama8b_decode_fp8": llama8b_decode_fp8,
     "long_context_decode_fp8": long_context_decode_fp8,
     "window_prefill": window_prefill,
+    "llama8b_decode_single": llama8b_decode_single,
+    "mha_decode": mha_decode,
 }

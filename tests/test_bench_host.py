@@ -116,3 +116,43 @@ def test_l2_note_names_flush_or_size():
     large = bench.l2_note(600e6)
     assert "flushed" in small and "read back" in small
     assert "no flush" in large and "600 MB" in large
+
+
+def test_clock_phases_keep_only_gpu_timed_samples():
+    c = bench.ClockSampler(interval_ms=50)
+    busy = "2070, 2070, 900, 0x0, Not Active, Not Active, Not Active, Not Active"
+    idle = "345, 2070, 120, 0x1, Not Active, Not Active, Not Active, Not Active"
+    c.lines = [(0.0, idle), (1.0, busy), (1.5, busy), (3.0, idle), (5.02, busy)]
+    c.phases = [(0.9, 1.6), (4.0, 5.0)]
+    kept = c.phase_lines()
+    assert kept == [busy, busy, busy]          # 5.02 is within one interval of slack
+    assert bench.ClockSampler.summary(kept)["sm_mhz"] == 2070
+
+
+def test_step_stats_and_compact_summary():
+    st = bench.step_stats([0.3, 0.1, 0.2, 0.4])
+    assert st["median_ms"] == 0.25 and st["min_ms"] == 0.1 and st["reps"] == 4
+    rec = {"value": 1000.0, "unit": "TFLOP/s", "kernels_ms": {"ragged_prefill": 0.18},
+           "roofline": {"frac": 0.55}, "roofline_nominal_frac": 0.49, "step_stats": st,
+           "cpu": {"value": 0.01, "cores": 16}, "parity": {"max_abs": 0.004,
+                                                           "mean_abs": 1e-4, "ok": True}}
+    e = bench.compact("ragged_prefill", rec)
+    assert e["TFLOP/s"] == 1000.0 and e["kernel_ms"] == 0.18 and e["frac"] == 0.55
+    assert e["target_nominal"] == 0.50 and e["met"] is False      # 0.49 of nominal
+    assert e["median_ms"] == 0.25 and e["oracle"] == 0.01 and e["parity_ok"] is True
+    assert "target_nominal" not in bench.compact("chunked_paged_prefill", rec)
+
+
+def test_parity_record_counts_every_element():
+    import numpy as np
+    from paged_kv_gqa_15_gb300 import workloads as W
+    ref = np.linspace(-2, 2, 24).reshape(2, 3, 4)
+    bits = W.float_to_bits(ref.astype(np.float32))          # bf16 of the reference
+    p = bench._parity(bits, ref)
+    assert p["ok"] and p["elements"] == 24 and p["max_abs"] <= 2 ** -8 * 2
+    bad = bits.copy()
+    bad[1, 2, 3] = W.float_to_bits(np.float32(5.0))
+    assert not bench._parity(bad, ref)["ok"]
+    nan = bits.copy()
+    nan[0, 0, 0] = np.uint16(0x7FC0)
+    assert not bench._parity(nan, ref)["ok"]

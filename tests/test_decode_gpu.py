@@ -272,27 +272,3 @@ def test_llama8b_config_write_then_split_decode_full_parity():
     touched = np.unique(w.slot_mapping // 16)
     np.testing.assert_array_equal(W.to_bits(t["k_cache"][torch.from_numpy(touched).to(DEV)]),
                                   kc_h[touched])
-
-
-def test_long_context_config_sampled_parity():
-    """8 sequences of 32k-128k tokens; split decode in the launch configuration the
-    benchmark times; two sequences (all 32 heads) are checked against the oracle."""
-    w = W.long_context_decode()
-    t = w.tensors(DEV)
-    bt = torch.from_numpy(w.block_tables).to(DEV)
-    sl = torch.from_numpy(w.seq_lens).to(DEV)
-    out = torch.empty_like(t["q"])
-    ws = pa.alloc_workspace(pa.decode_split_workspace_size(w.batch, 32, 128, w.max_seq_len), DEV)
-    pa.pa_decode_split(out, t["q"], t["k_cache"], t["v_cache"], bt, sl, w.scale, w.max_seq_len,
-                       ws)
-    torch.cuda.synchronize()
-    q = W.to_bits(t["q"])
-    for b in (int(np.argmax(w.seq_lens)), int(np.argmin(w.seq_lens))):
-        L = int(w.seq_lens[b])
-        pages = w.block_tables[b, :(L + 15) // 16]
-        idx = torch.from_numpy(pages.astype(np.int64)).to(DEV)
-        kc = W.to_bits(t["k_cache"][idx])
-        vc = W.to_bits(t["v_cache"][idx])
-        bt_local = np.arange(len(pages), dtype=np.int32)[None, :]
-        ref = oracle.decode(q[b:b + 1], kc, vc, bt_local, np.array([L], np.int32), 8, 16, w.scale)
-        assert_close_bf16(bf16_out(out[b:b + 1]), ref, what=f"long seq {b} (L={L})")

@@ -223,63 +223,6 @@ def test_paged_bad_block_id_is_flagged():
     assert torch.isfinite(o.float()).all()
 
 
-# ---- full-size workloads, sampled rows --------------------------------------------------------
-
-
-def _sample_rows(w, per_request=6, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = []
-    for r in range(w.batch):
-        a, b = int(w.qo_indptr[r]), int(w.qo_indptr[r + 1])
-        if b <= a:
-            continue
-        pick = {a, b - 1, min(a + 127, b - 1), min(a + 128, b - 1)}
-        pick.update(rng.integers(a, b, size=per_request).tolist())
-        rows.extend(sorted(pick))
-    return np.array(rows, np.int64)
-
-
-def test_ragged_prefill_config_sampled():
-    """16 requests, qo = kv ~ U[128, 2048], 32 q / 8 kv heads, hd 128, causal, one launch
-    in the configuration the benchmark times; sampled rows (all heads) vs the oracle."""
-    w = W.ragged_prefill()
-    t = w.tensors(DEV)
-    o = torch.empty_like(t["q"])
-    pa.pa_ragged_prefill(o, t["q"], t["k"], t["v"], w.qo_indptr, w.kv_indptr,
-                         torch.from_numpy(w.qo_indptr).to(DEV),
-                         torch.from_numpy(w.kv_indptr).to(DEV), w.scale, causal=True)
-    torch.cuda.synchronize()
-    rows = _sample_rows(w)
-    q, k, v = (W.to_bits(t[n]) for n in ("q", "k", "v"))
-    ref = oracle.prefill(q, k, v, w.qo_indptr, w.kv_indptr, 8, w.scale, causal=True, rows=rows)
-    assert_close_bf16(bf16_out(o)[rows], ref[rows], what="config ragged prefill")
-    assert pa.device_status() == 0
-
-
-def test_chunked_paged_prefill_config_sampled():
-    """8 requests, prefix U[1024, 8192] in a shuffled paged cache + a 512-token chunk
-    written by pa_write_cache, 16 q / 8 kv heads, hd 256; sampled rows vs the oracle."""
-    w = W.chunked_paged_prefill()
-    t = w.tensors(DEV)
-    kc_h, vc_h = W.to_bits(t["k_cache"]), W.to_bits(t["v_cache"])
-    pa.pa_write_cache(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"],
-                      torch.from_numpy(w.chunk_slot_mapping).to(DEV))
-    oracle.write_cache(W.to_bits(t["k_new"]), W.to_bits(t["v_new"]), kc_h, vc_h,
-                       w.chunk_slot_mapping, 16)
-    o = torch.empty_like(t["q"])
-    pa.pa_ragged_prefill(o, t["q"], t["k_cache"], t["v_cache"], w.qo_indptr, w.kv_indptr,
-                         torch.from_numpy(w.qo_indptr).to(DEV),
-                         torch.from_numpy(w.kv_indptr).to(DEV), w.scale, causal=True,
-                         block_tables=torch.from_numpy(w.block_tables).to(DEV))
-    torch.cuda.synchronize()
-    rows = _sample_rows(w, per_request=4)
-    q = W.to_bits(t["q"])
-    ref = oracle.prefill(q, kc_h, vc_h, w.qo_indptr, w.kv_indptr, 8, w.scale, causal=True,
-                         block_tables=w.block_tables, block_size=16, rows=rows)
-    assert_close_bf16(bf16_out(o)[rows], ref[rows], what="config chunked paged prefill")
-    assert pa.device_status() == 0
-
-
 def test_paged_stale_nan_rows_do_not_leak():
     """Rows of a request's last page past its kv length may hold anything (here NaN):
     they are masked out and must not reach the output."""
