@@ -161,10 +161,19 @@ __device__ __forceinline__ void tile_exp(const uint32_t (&sr)[BN], float scale, 
 // producer warp (warp 6) issues the V tiles.  Contiguous K/V move as 8 KB boxes and
 // do not need it (a split measured 7 % slower there); at head_dim <= 128 two CTAs
 // share an SM and their registers leave no room for a seventh warp.
+// At head_dim 256 (one CTA per SM) two threads issue the MMAs: warp 1 the scores
+// S_j = Q K_j^T, warp 6 the P_j V_j (tcgen05.commit tracks each thread's own MMAs), so
+// the scores of tile j + 1 never queue behind the issue of P_j V_j in one thread's
+// program order, nor P_j V_j behind a K tile the score issuer waits for: chunked paged
+// prefill 0.246 -> 0.221 ms.  At head_dim <= 128 two CTAs share an SM, and the seventh
+// warp's registers (128 per thread, with spills) made it 5 % slower there.
 template <int HD, bool PAGED>
 struct ProducerSplit {
     static constexpr bool value = HD == 256 && PAGED;
-    static constexpr int threads = value ? 224 : 192;
+    static constexpr bool two_issuers = HD == 256;
+    static constexpr int PV_WARP = two_issuers ? 6 : -1;
+    static constexpr int V_WARP = two_issuers ? 7 : 6;   // the V producer (split only)
+    static constexpr int threads = 32 * (6 + (two_issuers ? 1 : 0) + (value ? 1 : 0));
 };
 
 template <int HD, int BN>
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
     // wait on it, or the in-order completion of S_g after P_{g-2} V, saw the phase
     // before) nor one ahead (the next phase needs work the waiter has not released).
     uint64_t *q_full = bars + 0;
-    uint64_t *q_empty = bars + 1;   // split producer only: an item's last S is done
+    uint64_t *q_empty = bars + 1;   // head_dim 256: an item's last S is done (score issuer)
     uint64_t *k_full = bars + 2;    // [KS]
     uint64_t *k_empty = bars + 6;   // [KS] (KS != 2): one softmax thread arrives once S_g is done
     uint64_t *v_full = bars + 10;   // [VS]
@@ -382,7 +391,7 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
     // serialised and sat on the softmax -> MMA critical path.
     uint64_t *p_full = bars + 20;   // [2]: P_j is in TMEM
     uint64_t *o_free = bars + 24;   // the epilogue has read O
-    uint64_t *drain = bars + 25;
+    uint64_t *drain = bars + 25;     // [S issuer], and bars + 23 for the P.V issuer
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 26);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 27);
     // Work items are claimed dynamically (atomicAdd on a global counter) by the
@@ -415,9 +424,11 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
         }
         mbar_init(o_free, 4);
         mbar_init(drain, 1);
+        mbar_init(bars + 23, 1);
         for (int k = 0; k < 4; ++k) {
             mbar_init(&item_full[k], 1);
-            mbar_init(&item_empty[k], SPLIT ? 6 : 5);
+            mbar_init(&item_empty[k], 5 + (ProducerSplit<HD, PAGED>::two_issuers ? 1 : 0) +
+                                          (SPLIT ? 1 : 0));
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -431,11 +442,11 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 || (SPLIT && warp == 6)) {
+    if (warp == 0 || (SPLIT && warp == ProducerSplit<HD, PAGED>::V_WARP)) {
         // ------------------------------- TMA producers -------------------------------
         // Warp 0 claims the items and loads Q, K (and, unless split, V); with a split
         // producer warp 6 loads V, taking the items from the queue like the consumers.
-        const bool v_only = SPLIT && warp == 6;
+        const bool v_only = SPLIT && warp == ProducerSplit<HD, PAGED>::V_WARP;
         const bool loads_v = !SPLIT || v_only;
         if (lane == 0) {
             prefetch_tensormap(&p.tm_q);
@@ -514,16 +525,17 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
 
             if (!v_only && lane == 0) {
                 // Q is reused once the previous item's last S (tile kv_it - 1) is done.
-                // Without a split, this warp's own V loads keep it close behind the MMA:
-                // it issued V_{kv_it-1} after P_{kv_it-3} V was done, which in issue order
-                // means S_{kv_it-2} was done too, so s_full[(kv_it - 1) & 1] is at most one
-                // phase from the awaited one and its parity wait is exact.  A split
-                // producer is throttled only by its K ring (up to three tiles ahead at
-                // head_dim 256), where that barrier may still be two phases back and the
-                // parity wait would pass early; it waits instead on q_empty, which the
-                // MMA thread commits once per item after the item's last S.
+                // With one MMA issuer and no split, this warp's own V loads keep it close
+                // behind the MMA: it issued V_{kv_it-1} after P_{kv_it-3} V was done, which
+                // in that thread's issue order means S_{kv_it-2} was done too, so
+                // s_full[(kv_it - 1) & 1] is at most one phase from the awaited one and its
+                // parity wait is exact.  At head_dim 256 neither holds (a split producer is
+                // throttled only by its 3-stage K ring; two issuers have no common order),
+                // so the wait is on q_empty, which the score issuer commits once per item
+                // after the item's last S.
+                constexpr bool Q_EMPTY = ProducerSplit<HD, PAGED>::two_issuers;
                 bool ok_q = true;
-                if constexpr (SPLIT) {
+                if constexpr (Q_EMPTY) {
                     if (n_q > 0) ok_q = mbar_wait(q_empty, (n_q - 1) & 1u, p.status, abort_flag);
                 } else {
                     if (kv_it > 0)
@@ -633,8 +645,10 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
                 p.item_counter[1] = 0;
             }
         }
-    } else if (warp == 1) {
-        // -------------------------------- MMA issuer --------------------------------
+    } else if (warp == 1 || warp == ProducerSplit<HD, PAGED>::PV_WARP) {
+        // ------------------ MMA issuers: warp 1 the scores, warp 6 the P.V ------------------
+        constexpr bool TWO = ProducerSplit<HD, PAGED>::two_issuers;
+        const bool s_role = warp == 1;
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, HD, false, true);
@@ -705,18 +719,29 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
                 mbar_arrive(&item_empty[slot]);
                 if (w.n_kv < 0) break;
                 if (w.n_kv == 0) continue;
-                ok = mbar_wait(q_full, q_it & 1, p.status, abort_flag);
-                if (!ok) break;
-                tc_fence_after_sync();
                 const uint32_t base = kv_it;
                 // keys from the item's first tile on, and its first row in the window
                 const int kv_rel = WINDOW ? w.kv_len - w.j0 * BN : w.kv_len;
                 const int head = WINDOW ? w.kv_lo - w.j0 * BN : 0;
+                if (TWO && !s_role) {
+                    for (int j = 0; j < w.n_kv && ok; ++j) issue_pv(base + j, j, kv_rel, head);
+                    kv_it += w.n_kv;
+                    ++o_items;
+                    continue;
+                }
+                ok = mbar_wait(q_full, q_it & 1, p.status, abort_flag);
+                if (!ok) break;
+                tc_fence_after_sync();
                 for (int j = 0; j < w.n_kv && ok; ++j) {
                     const uint32_t g = base + j;
                     const int s = g % C::KS;      // K stage
                     const int b = g & 1;          // S / P buffer
                     ok = mbar_wait(&k_full[s], (g / C::KS) & 1, p.status, abort_flag);
+                    // S buffer b held P_{g-2}: with two issuers its P.V (the other thread's)
+                    // must be done; one issuer's MMAs run in issue order
+                    if (TWO && ok && g >= 2)
+                        ok = mbar_wait(&v_empty[(g - 2) % C::VS], ((g - 2) / C::VS) & 1, p.status,
+                                       abort_flag);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint64_t kd = k_desc + ((s * C::KV_BYTES) >> 4);
@@ -727,18 +752,19 @@ __global__ void __launch_bounds__(ProducerSplit<HD, PAGED>::threads, PrefillCfg<
                                     kd + ((c * C::KV_CHUNK + inner) >> 4), idesc_s, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(&s_full[b]);
-                    if (SPLIT && j == w.n_kv - 1) tc_commit(q_empty);   // the item's Q is free
-                    if (j >= 1) issue_pv(g - 1, j - 1, kv_rel, head);
+                    if (TWO && j == w.n_kv - 1) tc_commit(q_empty);   // the item's Q is free
+                    if (!TWO && j >= 1) issue_pv(g - 1, j - 1, kv_rel, head);
                 }
-                issue_pv(base + w.n_kv - 1, w.n_kv - 1, kv_rel, head);
+                if (!TWO) issue_pv(base + w.n_kv - 1, w.n_kv - 1, kv_rel, head);
                 kv_it += w.n_kv;
                 ++q_it;
-                ++o_items;
+                if (!TWO) ++o_items;
             }
             // never release TMEM / smem with tensor-core work still in flight
-            tc_commit(drain);
+            uint64_t *my_drain = s_role ? drain : bars + 23;
+            tc_commit(my_drain);
             const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(drain, 0)) {
+            while (!mbar_try_wait(my_drain, 0)) {
                 if (global_timer_ns() - t0 > kWaitLimitNs) {
                     atomicOr(p.status, kStatusTimeout);
                     break;
