@@ -137,6 +137,27 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 }
 
 // Named barrier over `nthreads` threads (a multiple of 32) with id `id` (1..15).
+// Cluster-wide barrier: every thread of every CTA of the cluster arrives (release) and
+// waits (acquire); called by all threads of each warp together.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// The shared::cluster address of this CTA's shared-memory address `addr` in CTA `rank`
+// of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -50,12 +50,14 @@ def _run_decode(w, split, layout="HND", stale=True, q_zero=False):
         ws = pa.alloc_workspace(pa.decode_split_workspace_size(w.batch, w.num_q_heads,
                                                                w.head_dim, L), DEV)
         ws.fill_(0xFF)  # NaN pattern: partitions that are never written must never be read
-        pa.pa_decode_split(out, q_d, kc_d, vc_d, bt, sl, w.scale, L, ws, layout=layout)
+        pa.pa_decode_split(out, q_d, kc_d, vc_d, bt, sl, w.scale, L, ws, layout=layout,
+                           sliding_window=w.window)
     else:
-        pa.pa_decode(out, q_d, kc_d, vc_d, bt, sl, w.scale, layout=layout)
+        pa.pa_decode(out, q_d, kc_d, vc_d, bt, sl, w.scale, layout=layout,
+                     sliding_window=w.window)
     torch.cuda.synchronize()
     ref = oracle.decode(q, kc, vc, w.block_tables, w.seq_lens, w.num_kv_heads, w.block_size,
-                        w.scale, strides=strides)
+                        w.scale, strides=strides, window=w.window)
     return out, ref, ws, (q, kc, vc)
 
 
@@ -115,6 +117,19 @@ def test_write_cache_empty_is_a_no_op():
 def test_tiny_config_single_pass():
     out, ref, _, _ = _run_decode(W.tiny_decode(), split=False)
     assert_close_bf16(out, ref, what="tiny decode")
+
+
+@pytest.mark.parametrize("window", [0, 5000])
+@pytest.mark.parametrize("hd,nq,nkv", [(128, 32, 8), (64, 8, 8), (256, 16, 2)])
+def test_single_pass_cluster_split_of_long_sequences(hd, nq, nkv, window):
+    """Few (sequence, kv head) items with long sequences: the single pass spreads each
+    over a 4-CTA cluster that merges its partial results in distributed shared memory.
+    Lengths cover page counts not divisible by 4, fewer pages than ranks, and 0."""
+    lens = [70001, 4099, 3, 0, 1025]
+    w = W.make_decode("cluster", lens, nq, nkv, hd, seed=hd + window, window=window)
+    out, ref, _, _ = _run_decode(w, split=False)
+    assert_close_bf16(out, ref, what=f"cluster single pass hd{hd} window {window}")
+    assert pa.device_status() == 0
 
 
 def test_tiny_config_split():
