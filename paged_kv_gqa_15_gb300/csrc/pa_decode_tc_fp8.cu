@@ -14,19 +14,25 @@
 //    pair holds q to about 2^-8 relative, close to its bf16 input, so K needs no
 //    conversion.  The MMA's N = 16 columns hold the G hi rows and the G lo rows; the
 //    softmax adds each pair and divides by s.
-//  * O^T = V^T P takes V as an MN-major operand, so four converter warps turn each V
-//    tile into f16 (exact for every E4M3 value) in the 128-byte-swizzled layout of a
-//    TMA-loaded 16-bit tile, writing zeros for rows outside the partition's tokens; P
-//    is f16 and the MMA is kind::f16.  k_scale scales the scores, v_scale the outputs.
+//  * O^T = V^T P also runs on the 8-bit tensor cores, straight from the TMA tile: V^T
+//    is read as an MN-major E4M3 operand (a tile's 128-byte rows are tokens, its bytes
+//    dims), and P is carried like Q, as two E4M3 rows per head, hi = e4m3(256 p) and
+//    lo = e4m3(256 p - hi), which hold p to 2^-8 relative (R17); the epilogue adds each
+//    head's hi and lo columns and divides by 256.  Rows outside the partition's tokens
+//    in a loaded page are zeroed in the tile before the MMA (0 x NaN would poison O).
+//    An earlier design converted every V tile to f16 with four converter warps into a
+//    2-stage f16 ring, and that convert -> P.V chain set the pace; dropping it frees
+//    the ring's 64 KB for a 6-stage fp8 V ring.  k_scale scales the scores, v_scale
+//    the outputs.
 //  * Warps: 0 K producer, 1 score-MMA issuer, 2-5 softmax, Q rows and epilogue, 6 V
-//    producer, 7-10 V converters, 11 P.V-MMA issuer.  With two issuing threads the
-//    score MMAs of later items never queue behind the P.V of an item whose softmax is
-//    still running (tcgen05.commit tracks each thread's own MMAs).  P is double
-//    buffered and each item's epilogue waits until the next item's P is written, so
-//    one item's P.V overlaps the next item's softmax.  The softmax warps also split q
-//    into the Q rows, two items ahead, so the K producer does nothing but stream
-//    tiles: with the split on the producer, that warp's serial work per item set the
-//    whole kernel's pace.  Every wait is bounded.
+//    producer, 7 P.V-MMA issuer.  With two issuing threads the score MMAs of later
+//    items never queue behind the P.V of an item whose softmax is still running
+//    (tcgen05.commit tracks each thread's own MMAs).  P is double buffered and each
+//    item's epilogue waits until the next item's P is written, so one item's P.V
+//    overlaps the next item's softmax.  The softmax warps also split q into the Q rows,
+//    two items ahead, so the K producer does nothing but stream tiles: with the split
+//    on the producer, that warp's serial work per item set the whole kernel's pace.
+//    Every wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -42,22 +48,18 @@ constexpr int kHD = 128;
 constexpr int kTok = 128;                      // tokens per tile (MMA M of S^T)
 constexpr int kTiles = kPartition / kTok;      // tiles per partition
 constexpr int kPagesPerTile = kTok / kBlockSize;
-constexpr int kN = 16;                         // MMA N: G hi and G lo rows of Q, padded
-constexpr int kThreads = 384;                  // 12 warps
+constexpr int kN = 16;                         // MMA N: G hi and G lo rows (Q or P), padded
+constexpr int kThreads = 256;                  // 8 warps
 constexpr int kKStages = 4;                    // fp8 K tile ring
-constexpr int kV8Stages = 3;                   // fp8 V tile ring
-constexpr int kV16Stages = 2;                  // converted f16 V tile ring
+constexpr int kV8Stages = 6;                   // fp8 V tile ring
 constexpr uint32_t kTile8Bytes = kTok * 128;   // 128 tokens x 128 one-byte dims
-constexpr uint32_t kTile16Chunk = kTok * 128;  // one 64-dim chunk of a 16-bit tile
-constexpr uint32_t kTile16Bytes = 2 * kTile16Chunk;
 constexpr uint32_t kQBytes = kN * 128;         // Q rows: 16 x 128 bytes
-constexpr uint32_t kSmallChunk = kN * 128;     // one 64-column chunk of P (16 rows)
-constexpr uint32_t kPTile = 2 * kSmallChunk;   // P of one tile
+constexpr uint32_t kPTile = kN * 128;          // P rows of one tile: 16 x 128 tokens, bytes
 constexpr uint32_t kPBytes = kTiles * kPTile;
+constexpr float kPScale = 256.f;               // P is carried as E4M3 codes of 256 p
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV8 = kOffK + kKStages * kTile8Bytes;
-constexpr uint32_t kOffV16 = kOffV8 + kV8Stages * kTile8Bytes;
-constexpr uint32_t kOffQ = kOffV16 + kV16Stages * kTile16Bytes;   // two Q buffers
+constexpr uint32_t kOffQ = kOffV8 + kV8Stages * kTile8Bytes;     // two Q buffers
 constexpr uint32_t kOffP = kOffQ + 2 * kQBytes;                  // two P buffers
 constexpr uint32_t kOffRed = kOffP + 2 * kPBytes;                // float [2][4 warps][16]
 constexpr uint32_t kOffQinv = kOffRed + 2 * 4 * kN * 4;          // float [2][16]
@@ -68,7 +70,7 @@ constexpr uint32_t kSmem = kOffBar + 512 + 1024;                 // + realignmen
 constexpr uint32_t kTmemCols = 256;            // S: 2 x 4 tiles x 16; O: 2 x 16
 constexpr uint32_t kTmS = 0, kTmO = 128;
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-static_assert((2 * (kKStages + kV8Stages + kV16Stages) + 16) * 8 <= 512, "barriers fit");
+static_assert((2 * (kKStages + kV8Stages) + 16) * 8 <= 512, "barriers fit");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms on 1 KB boundaries");
 
 struct DecodeTc8Params {
@@ -205,10 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *k_full = bars;                       // fp8 K tile landed (TMA)
     uint64_t *k_empty = k_full + kKStages;         // its score MMAs are done (commit)
     uint64_t *v8_full = k_empty + kKStages;        // fp8 V tile landed (TMA)
-    uint64_t *v8_empty = v8_full + kV8Stages;      // the converters have read it (4 arrivals)
-    uint64_t *v16_full = v8_empty + kV8Stages;     // f16 V tile written (4 arrivals)
-    uint64_t *v16_empty = v16_full + kV16Stages;   // its P.V MMAs are done (commit)
-    uint64_t *q_full = v16_empty + kV16Stages;     // [2] Q rows written (4 arrivals)
+    uint64_t *v8_empty = v8_full + kV8Stages;      // its P.V MMAs are done (commit)
+    uint64_t *q_full = v8_empty + kV8Stages;       // [2] Q rows written (4 arrivals)
     uint64_t *s_full = q_full + 2;                 // [2] S^T of all the item's tiles (commit)
     uint64_t *s_free = s_full + 2;                 // [2] softmax has read S^T (4 arrivals)
     uint64_t *p_full = s_free + 2;                 // [2] P written (4 arrivals)
@@ -234,11 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kV8Stages; ++s) {
             mbar_init(&v8_full[s], 1);
-            mbar_init(&v8_empty[s], 4);
-        }
-        for (int s = 0; s < kV16Stages; ++s) {
-            mbar_init(&v16_full[s], 4);
-            mbar_init(&v16_empty[s], 1);
+            mbar_init(&v8_empty[s], 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&q_full[x], 4);
@@ -341,62 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (global_timer_ns() - t0 > kWaitLimitNs) break;
             }
         }
-    } else if (warp >= 7 && warp <= 10) {
-        // ------------------- V converters: E4M3 tile -> f16 tile, one row each -------------------
-        const int t = threadIdx.x - 7 * 32;       // token row of the tile
-        uint32_t it8 = 0, it16 = 0;
-        bool ok = true;
-        int b, kh, part;
-        for (int e = 0; ok && item8(p, pref, total, e, b, kh, part); ++e) {
-            const Span8 sp = span8(p, b, part);
-            for (int i = sp.i_lo; ok && i < sp.n_tiles; ++i, ++it8, ++it16) {
-                const int s8 = it8 % kV8Stages, s16 = it16 % kV16Stages;
-                ok = mbar_wait(&v8_full[s8], (it8 / kV8Stages) & 1, p.status, abort_flag) &&
-                     mbar_wait(&v16_empty[s16], ((it16 / kV16Stages) & 1) ^ 1u, p.status,
-                               abort_flag);
-                if (__any_sync(kMask, !ok)) {
-                    ok = false;
-                    break;
-                }
-                // rows outside [t_lo, n_tok) become zeros, whatever the pool held there
-                const int tok = i * kTok + t;
-                const bool valid = tok >= sp.t_lo && tok < sp.n_tok;
-                const uint8_t *src = smem + kOffV8 + s8 * kTile8Bytes + t * 128;
-                uint8_t *dst = smem + kOffV16 + s16 * kTile16Bytes + t * 128;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {             // dims 16u .. 16u + 15
-                    const uint4 raw = valid ? *reinterpret_cast<const uint4 *>(src + ((u ^ (t & 7)) << 4))
-                                            : make_uint4(0u, 0u, 0u, 0u);
-                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                    uint32_t h[8];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * j])
-                            : "h"(static_cast<unsigned short>(w[j] & 0xffffu)));
-                        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * j + 1])
-                            : "h"(static_cast<unsigned short>(w[j] >> 16)));
-                    }
-                    const int chunk = u >> 2, unit = (u & 3) * 2;   // 8 f16 dims per 16-byte unit
-                    uint8_t *row = dst + chunk * kTile16Chunk;
-                    *reinterpret_cast<uint4 *>(row + ((unit ^ (t & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-                    *reinterpret_cast<uint4 *>(row + (((unit + 1) ^ (t & 7)) << 4)) =
-                        make_uint4(h[4], h[5], h[6], h[7]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&v8_empty[s8]);
-                    mbar_arrive(&v16_full[s16]);
-                }
-            }
-        }
-    } else if (warp == 1 || warp == 11) {
-        // ------------- MMA issuers: warp 1 the scores, warp 11 the P.V -------------
+    } else if (warp == 1 || warp == 7) {
+        // ------------- MMA issuers: warp 1 the scores, warp 7 the P.V -------------
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f32(kTok, kN, 0, 0, false, false);   // E4M3 x E4M3
-            constexpr uint32_t idesc_o = idesc_f32(kHD, kN, 0, 0, true, false);     // f16 x f16
+            // E4M3 V^T, MN-major: a tile's 128 dims of one token are one 128-byte row
+            constexpr uint32_t idesc_o = idesc_f32(kHD, kN, 0, 0, true, false);
             const uint64_t ring_k = smem_desc_sw128(smem_addr(smem + kOffK), 16, 1024);
-            const uint64_t ring_v = smem_desc_sw128(smem_addr(smem + kOffV16), kTile16Chunk, 1024);
+            const uint64_t ring_v = smem_desc_sw128(smem_addr(smem + kOffV8), kTile8Bytes, 1024);
             const uint64_t q_desc = smem_desc_sw128(smem_addr(smem + kOffQ), 16, 1024);
             const uint64_t p_desc = smem_desc_sw128(smem_addr(smem + kOffP), 16, 1024);
             uint32_t kit = 0, vit = 0;
@@ -434,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) return;
                 tc_commit(&s_full[x]);
             };
-            // O^T = V^T P over the converted tiles of item e
+            // O^T = V^T P over the fp8 V tiles of item e, with P's E4M3 hi / lo rows
             auto issue_pv = [&](int e, const Span8 &sp) {
                 const int x = e & 1;
                 const uint32_t use = e >> 1;
@@ -443,18 +391,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) return;
                 tc_fence_after_sync();
                 for (int i = sp.i_lo; i < sp.n_tiles && ok; ++i, ++vit) {
-                    const int s = vit % kV16Stages;
-                    ok = mbar_wait(&v16_full[s], (vit / kV16Stages) & 1, p.status, abort_flag);
+                    const int s = vit % kV8Stages;
+                    ok = mbar_wait(&v8_full[s], (vit / kV8Stages) & 1, p.status, abort_flag);
                     if (!ok) return;
                     tc_fence_after_sync();
-                    const uint64_t vd = ring_v + ((s * kTile16Bytes) >> 4);
+                    // rows outside [t_lo, n_tok) in a page that was loaded hold whatever
+                    // the pool held (whole pages outside read as zeros); P is 0 there,
+                    // but 0 x NaN would poison O, so zero those V rows: past the sequence
+                    // in its last page, and before the window in its first page
+                    const int stale = sp.n_tok - i * kTok;   // first row past the tokens
+                    const int head = sp.t_lo - i * kTok;     // first row in the window
+                    if (stale < kTok || (head > 0 && head < kTok)) {
+                        uint8_t *vt = smem + kOffV8 + s * kTile8Bytes;
+                        const int tail_end = min(kTok, (stale + kBlockSize - 1) / kBlockSize * kBlockSize);
+                        const int head_begin = max(0, head / kBlockSize * kBlockSize);
+                        for (int r = stale; r < tail_end; ++r) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(vt + r * 128);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        for (int r = head_begin; r < head && r < kTok; ++r) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(vt + r * 128);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    const uint64_t vd = ring_v + ((s * kTile8Bytes) >> 4);
                     const uint64_t pd = p_desc + ((x * kPBytes + i * kPTile) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kTok / 16; ++kk)
-                        mma_bf16_ss(tmem + kTmO + x * kN, vd + ((kk * 16 * 128) >> 4),
-                                    pd + (((kk / 4) * kSmallChunk + (kk % 4) * 32) >> 4), idesc_o,
-                                    (i > sp.i_lo || kk > 0) ? 1u : 0u);
-                    tc_commit(&v16_empty[s]);
+                    for (int kk = 0; kk < kTok / 32; ++kk)   // 32 one-byte tokens per MMA
+                        mma_f8_ss(tmem + kTmO + x * kN, vd + ((kk * 32 * 128) >> 4),
+                                  pd + ((kk * 32) >> 4), idesc_o, (i > sp.i_lo || kk > 0) ? 1u : 0u);
+                    tc_commit(&v8_empty[s]);
                 }
                 if (!ok) return;
                 tc_commit(&o_full[x]);
@@ -528,10 +497,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto epilogue = [&]() -> bool {
             bool done = prev_got && mbar_wait(&o_full[prev_x], prev_use & 1, p.status, abort_flag);
             done = !__any_sync(kMask, !done);
-            uint32_t o[8];
+            uint32_t o[16];   // column g: head g's hi part, column G + g its lo part
             if (done) {
                 tc_fence_after_sync();
-                tmem_load_8(tmem + t_lane + kTmO + prev_x * kN, o);
+                if constexpr (G == 8) {
+                    tmem_load_16(tmem + t_lane + kTmO + prev_x * kN, o);
+                } else {
+                    tmem_load_8(tmem + t_lane + kTmO + prev_x * kN,
+                                *reinterpret_cast<uint32_t (*)[8]>(o));
+                }
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -541,7 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int g = 0; g < G; ++g) {
                     const int64_t r =
                         (static_cast<int64_t>(prev_b) * nq + prev_kh * G + g) * p.max_parts + prev_part;
-                    p.part_o[r * kHD + row] = __uint_as_float(o[g]) / prev_sm[g] * p.v_scale;
+                    const float og = (__uint_as_float(o[g]) + __uint_as_float(o[G + g])) *
+                                     (1.f / kPScale);
+                    p.part_o[r * kHD + row] = og / prev_sm[g] * p.v_scale;
                     if (row == 0) {
                         p.part_m[r] = prev_mx[g] * kLn2;
                         p.part_l[r] = prev_sm[g];
@@ -620,17 +596,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int g = 0; g < G; ++g) rl[g] = sm[g];
             }
-            // P (f16) into buffer e % 2, K-major by head, as the bf16 decode lays it out;
-            // the P.V of item e - 2 that read this buffer finished before that item's
-            // epilogue, which ran in the previous iteration
-            uint8_t *pb = smem + kOffP + x * kPBytes + (row / 64) * kSmallChunk + (row % 8) * 2;
+            // P into buffer e % 2 as E4M3 rows, K-major (a row's bytes are the tile's
+            // tokens, swizzled in 16-byte units by row % 8): row g holds hi = e4m3(256 p)
+            // of head g, row G + g its lo = e4m3(256 p - hi) (R17).  The P.V of item e - 2
+            // that read this buffer finished before that item's epilogue, which ran in the
+            // previous iteration.
+            uint8_t *pb = smem + kOffP + x * kPBytes + (row & 15);
 #pragma unroll
-            for (int i = 0; i < kTiles; ++i)
+            for (int i = 0; i < kTiles; ++i) {
 #pragma unroll
-                for (int g = 0; g < G; ++g)
-                    *reinterpret_cast<__half *>(pb + i * kPTile + g * 128 +
-                                                ((((row % 64) / 8) ^ g) << 4)) =
-                        __float2half_rn(pv[i][g]);
+                for (int g = 0; g < G; g += 2) {
+                    const float a0 = pv[i][g] * kPScale, a1 = pv[i][g + 1] * kPScale;
+                    const uint16_t hi = e4m3x2(a1, a0);
+                    const float2 back = e4m3x2_to_float2(hi);
+                    const uint16_t lo = e4m3x2(a1 - back.y, a0 - back.x);
+                    uint8_t *t = pb + i * kPTile;
+                    const int u = row >> 4;   // 16-byte unit of this token within a row
+                    t[g * 128 + ((u ^ (g & 7)) << 4)] = static_cast<uint8_t>(hi & 0xffu);
+                    t[(g + 1) * 128 + ((u ^ ((g + 1) & 7)) << 4)] = static_cast<uint8_t>(hi >> 8);
+                    t[(G + g) * 128 + ((u ^ ((G + g) & 7)) << 4)] = static_cast<uint8_t>(lo & 0xffu);
+                    t[(G + g + 1) * 128 + ((u ^ ((G + g + 1) & 7)) << 4)] =
+                        static_cast<uint8_t>(lo >> 8);
+                }
+            }
             fence_proxy_async_smem();
             named_barrier(1, 128);   // also publishes the sums
 #pragma unroll
