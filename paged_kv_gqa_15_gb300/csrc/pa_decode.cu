@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(const __grid_constant__
 
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
-    if (split && decode_tc_supported(p, head_dim)) return launch_decode_tc(p, stream);
+    if (decode_tc_supported(p, head_dim))
+        return split ? launch_decode_tc(p, stream) : launch_decode_tc_single(p, stream);
     if (split && decode_tc8_supported(p, head_dim)) return launch_decode_tc8(p, stream);
     if (p.kv_fp8) return launch_decode_fp8(p, head_dim, split, stream);
     return launch_decode_cache<false>(p, head_dim, split, stream);

@@ -34,6 +34,15 @@
 //    that reach into the window; in the one holding L - window, tiles wholly before
 //    it are skipped, pages before it inside its first tile are read as zero boxes
 //    (their table entries are never looked up), and its earlier rows are masked.
+//  * The same kernel runs the single pass (pa_decode, "paged_attn.py" V1 branch),
+//    which has no workspace for partials: there a CTA owns whole (sequence, kv head)
+//    pairs and walks their partitions in order, and the epilogue merges each
+//    partition's (max, sum, output) into running registers (the log-sum-exp rule of
+//    the split's merge) and writes the bf16 output after the pair's last partition.
+//    Pairs go to CTAs in a snake over the sequences sorted by partition count
+//    (heaviest first: CTA c takes ranks c, 2C - 1 - c, 2C + c, ...), so the loads
+//    even out without a work counter; every CTA sorts the same way (a stable counting
+//    sort in shared memory), so they agree on the assignment.
 #include <cuda.h>
 
 #include "pa_device.cuh"
@@ -67,6 +76,8 @@ constexpr uint32_t kOffP = kOffQ + 2 * kQBytes;
 constexpr uint32_t kOffRed = kOffP + kPBytes;                // float [2][4 warps][16]
 constexpr uint32_t kOffPref = kOffRed + 2 * 4 * kN * 4;      // int [MAXB + 1]
 constexpr int kMaxSeqsTc = 2048;
+constexpr int kSortKeys = 1024;                // single pass: partition-count buckets
+static_assert(kSortKeys * 4 <= kPBytes, "the sort's histogram fits in the P buffer");
 constexpr uint32_t kOffBar = kOffPref + (kMaxSeqsTc + 8) * 4;
 constexpr uint32_t kSmemTc = kOffBar + 256 + 1024;           // + realignment slack
 constexpr uint32_t kTmemCols = 256;            // S: 2 x 4 tiles x 16; O: 2 x 16
@@ -101,6 +112,57 @@ __device__ __forceinline__ bool tc_item(const DecodeParams &p, const int *pref, 
     return true;
 }
 
+// Active partitions of a sequence of L tokens (those reaching into the window).
+__device__ __forceinline__ int tc_parts(int L, int window) {
+    return (L + kPartition - 1) / kPartition - window_start(L, window) / kPartition;
+}
+
+// The single pass's walk over this CTA's (sequence, kv head) pairs, one partition per
+// step: order[] lists the sequences by partition count, heaviest first; pair rank r of
+// this CTA is snake position r * C + c (r even) or r * C + C - 1 - c (r odd), and pair
+// position q is sequence order[q / nkv], kv head q % nkv.  Each role keeps its own walk
+// and asks for its steps e = 0, 1, 2, ... in order.
+struct TcWalk {
+    int r = -1;       // rank of the current pair within this CTA (-1: none yet)
+    int base = 0;     // step of the current pair's first partition
+    int np = 0;       // its active partitions
+    int b = 0, kh = 0, first_part = 0;
+
+    __device__ __forceinline__ bool at(const DecodeParams &p, const int *order, int e, int &ob,
+                                       int &okh, int &opart) {
+        const int C = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+        const long long n_pairs = static_cast<long long>(p.num_seqs) * p.num_kv_heads;
+        while (r < 0 || e >= base + np) {
+            if (r >= 0) base += np;
+            ++r;
+            const long long q = static_cast<long long>(r) * C + ((r & 1) ? C - 1 - c : c);
+            if (q >= n_pairs) return false;
+            b = order[q / p.num_kv_heads];
+            kh = static_cast<int>(q % p.num_kv_heads);
+            const int L = tc_seq_len(p, b, false);
+            np = tc_parts(L, p.window);
+            first_part = window_start(L, p.window) / kPartition;
+            if (np == 0) return false;   // sorted heaviest first: the rest are empty too
+        }
+        ob = b;
+        okh = kh;
+        opart = first_part + (e - base);
+        return true;
+    }
+};
+
+// The k-th item of this CTA in either mode.
+template <bool SINGLE>
+struct TcItems {
+    const int *pref;  // split: prefix of partition counts; single: sequences by weight
+    long long total;
+    TcWalk walk;
+    __device__ __forceinline__ bool at(const DecodeParams &p, int e, int &b, int &kh, int &part) {
+        if constexpr (SINGLE) return walk.at(p, pref, e, b, kh, part);
+        else return tc_item(p, pref, total, e, b, kh, part);
+    }
+};
+
 // The part of item (b, part) inside the sequence and its window: tokens
 // [t0 + t_lo, t0 + n_tok) of the partition starting at t0, in tiles i_lo .. n_tiles-1.
 struct TcSpan {
@@ -130,7 +192,7 @@ __device__ __forceinline__ int tc_seq_len(const DecodeParams &p, int b, bool fla
     return L;
 }
 
-template <int G>
+template <int G, bool SINGLE>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcParams prm) {
     const DecodeParams &p = prm.d;
@@ -206,6 +268,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    if constexpr (!SINGLE) {
     // prefix over sequences of their partition counts (the compact item list)
     for (int b = threadIdx.x; b < p.num_seqs; b += kThreadsTc) {
         const int L = tc_seq_len(p, b, blockIdx.x == 0);
@@ -227,11 +290,69 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             carry += __shfl_sync(kFullMaskTc, v, 31);
         }
     }
+    } else {
+        // the sequences by partition count, heaviest first, into pref[]: a stable
+        // counting sort (key 1023 - min(partitions, 1023)) with its histogram in the P
+        // buffer, which is zeroed again afterwards; and zeros for the outputs of
+        // sequences with no visible token, which no pair's epilogue writes
+        int *hist = reinterpret_cast<int *>(smem + kOffP);
+        for (int k = threadIdx.x; k < kSortKeys; k += kThreadsTc) hist[k] = 0;
+        __syncthreads();
+        auto key_of = [&](int b) {
+            return kSortKeys - 1 - min(tc_parts(tc_seq_len(p, b, false), p.window), kSortKeys - 1);
+        };
+        for (int b = threadIdx.x; b < p.num_seqs; b += kThreadsTc) {
+            const int L = tc_seq_len(p, b, blockIdx.x == 0);
+            atomicAdd(&hist[key_of(b)], 1);
+            if (tc_parts(L, p.window) == 0 && b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
+                __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) +
+                                   static_cast<int64_t>(b) * p.num_q_heads * kHD;
+                for (int i = 0; i < p.num_q_heads * kHD; ++i) o[i] = __float2bfloat16_rn(0.f);
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {   // exclusive prefix of the histogram, then the stable scatter
+            constexpr int PER = kSortKeys / 32;
+            int loc = 0;
+            for (int i = 0; i < PER; ++i) loc += hist[lane * PER + i];
+            int incl = loc;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(kFullMaskTc, incl, off);
+                if (lane >= off) incl += u;
+            }
+            int run = incl - loc;
+            for (int i = 0; i < PER; ++i) {
+                const int cnt = hist[lane * PER + i];
+                hist[lane * PER + i] = run;
+                run += cnt;
+            }
+            __syncwarp();
+            for (int base = 0; base < p.num_seqs; base += 32) {
+                const int b = base + lane;
+                const bool v = b < p.num_seqs;
+                const int key = v ? key_of(b) : -1 - lane;   // invalid lanes match no one
+                const unsigned same = __match_any_sync(kFullMaskTc, key);
+                const int leader = __ffs(same) - 1;
+                int start = 0;
+                if (v && lane == leader) {
+                    start = hist[key];
+                    hist[key] = start + __popc(same);
+                }
+                start = __shfl_sync(kFullMaskTc, start, leader);
+                if (v) pref[start + __popc(same & ((1u << lane) - 1u))] = b;
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+        for (int k = threadIdx.x; k < kSortKeys; k += kThreadsTc) hist[k] = 0;   // P padding
+        fence_proxy_async_smem();
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const long long total = static_cast<long long>(pref[p.num_seqs]) * p.num_kv_heads;
+    const long long total = SINGLE ? 0 : static_cast<long long>(pref[p.num_seqs]) * p.num_kv_heads;
 
     if (warp == 0 || warp == 6) {
         // --------------------- TMA producers: warp 0 Q and K, warp 6 V ---------------------
@@ -245,7 +366,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         uint32_t it = 0;   // ring uses
         int stop = 0;
         int b, kh, part;
-        for (int e = 0; !stop && tc_item(p, pref, total, e, b, kh, part); ++e) {
+        TcItems<SINGLE> items{pref, total};
+        for (int e = 0; !stop && items.at(p, e, b, kh, part); ++e) {
             const TcSpan sp = tc_span(p, b, part);
             const int t0 = sp.t0;
             const int n_tiles = sp.n_tiles;
@@ -314,9 +436,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             uint32_t kit = 0, vit = 0;   // K / V ring uses
             bool ok = true;
             // The token span of item e; n_tiles = -1 when there is none.
+            TcItems<SINGLE> items{pref, total};
             auto item_span = [&](int e) -> TcSpan {
                 int b, kh, part;
-                if (!tc_item(p, pref, total, e, b, kh, part)) {
+                if (!items.at(p, e, b, kh, part)) {
                     TcSpan none = {};
                     none.n_tiles = -1;
                     return none;
@@ -436,7 +559,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int nq = p.num_q_heads;
         bool ok = true;
         int b, kh, part;
-        for (int e = 0; tc_item(p, pref, total, e, b, kh, part); ++e) {
+        TcItems<SINGLE> items{pref, total};
+        // single pass: the pair's running max (log2 units), sum and unnormalised output
+        // (this thread's dim) over the partitions merged so far
+        float run_m[G], run_l[G], run_o[G];
+        for (int e = 0; items.at(p, e, b, kh, part); ++e) {
             const TcSpan sp = tc_span(p, b, part);
             const int n_tok = sp.n_tok;
             const int x = e & 1;
@@ -530,7 +657,37 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&o_free[x]);
-            if (done) {
+            if constexpr (SINGLE) {
+                if (e == items.walk.base) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        run_m[g] = -INFINITY;
+                        run_l[g] = 0.f;
+                        run_o[g] = 0.f;
+                    }
+                }
+                if (done) {
+                    // log-sum-exp merge of this partition into the running state
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float M = fmaxf(run_m[g], mx[g]);
+                        if (M != -INFINITY) {
+                            const float fa = run_m[g] == -INFINITY ? 0.f : exp2f(run_m[g] - M);
+                            const float fb = mx[g] == -INFINITY ? 0.f : exp2f(mx[g] - M);
+                            run_o[g] = run_o[g] * fa + __uint_as_float(o[g]) * fb;
+                            run_l[g] = run_l[g] * fa + sm[g] * fb;
+                            run_m[g] = M;
+                        }
+                    }
+                    if (e == items.walk.base + items.walk.np - 1) {   // the pair's last partition
+#pragma unroll
+                        for (int g = 0; g < G; ++g)
+                            static_cast<__nv_bfloat16 *>(p.out)[(static_cast<int64_t>(b) * nq +
+                                                                 kh * G + g) * kHD + row] =
+                                __float2bfloat16_rn(run_l[g] > 0.f ? run_o[g] / run_l[g] : 0.f);
+                    }
+                }
+            } else if (done) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const int64_t r =
@@ -555,7 +712,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
 }
 
-template <int G>
+template <int G, bool SINGLE>
 cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
     DecodeTcParams prm;
     prm.d = p;
@@ -578,7 +735,7 @@ cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
             !encode_tensor_map_bf16(&prm.tm_v, p.v_cache, 4, dims, str, box))
             return cudaErrorInvalidValue;
     }
-    auto kern = decode_tc_kernel<G>;
+    auto kern = decode_tc_kernel<G, SINGLE>;
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -591,8 +748,9 @@ cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
     static int sms = 0;
     if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 152;
+    // split: one CTA per item at most; single pass: one per (sequence, kv head) pair
     const long long slots = static_cast<long long>(p.num_seqs) * p.num_kv_heads *
-                            active_partitions_cap(p.max_parts, p.window);
+                            (SINGLE ? 1 : active_partitions_cap(p.max_parts, p.window));
     long long n = sms;
     if (slots < n) n = slots;
     cudaLaunchConfig_t cfg = {};
@@ -624,8 +782,17 @@ bool decode_tc_supported(const DecodeParams &p, int head_dim) {
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
     switch (p.num_q_heads / p.num_kv_heads) {
-        case 4: return launch_tc<4>(p, stream);
-        case 8: return launch_tc<8>(p, stream);
+        case 4: return launch_tc<4, false>(p, stream);
+        case 8: return launch_tc<8, false>(p, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+cudaError_t launch_decode_tc_single(const DecodeParams &p, cudaStream_t stream) {
+    if (p.num_seqs == 0) return cudaSuccess;
+    switch (p.num_q_heads / p.num_kv_heads) {
+        case 4: return launch_tc<4, true>(p, stream);
+        case 8: return launch_tc<8, true>(p, stream);
         default: return cudaErrorNotSupported;
     }
 }

@@ -132,6 +132,22 @@ def test_single_pass_cluster_split_of_long_sequences(hd, nq, nkv, window):
     assert pa.device_status() == 0
 
 
+@pytest.mark.parametrize("window", [0, 700])
+@pytest.mark.parametrize("nq,nkv", [(32, 8), (64, 8)])
+def test_tensor_core_single_pass(nq, nkv, window):
+    """The single pass at head_dim 128 with GQA 4 or 8 runs on the tensor cores: each CTA
+    owns whole (sequence, kv head) pairs (snake order over the sequences sorted by their
+    partitions) and merges the partitions in registers.  Lengths include 0, 1, partition
+    edges, ties and long sequences."""
+    rng = np.random.default_rng(nq + window)
+    lens = np.concatenate([[0, 1, 511, 512, 513, 4096, 4096, 9000, 0],
+                           rng.integers(1, 3000, size=40)])
+    w = W.make_decode("tc_single", lens, nq, nkv, 128, seed=nq * 3 + window, window=window)
+    out, ref, _, _ = _run_decode(w, split=False)
+    assert_close_bf16(out, ref, what=f"tensor-core single pass nq{nq} window {window}")
+    assert pa.device_status() == 0
+
+
 def test_tiny_config_split():
     out, ref, _, _ = _run_decode(W.tiny_decode(), split=True)
     assert_close_bf16(out, ref, what="tiny split decode")
