@@ -711,8 +711,32 @@ def bench_blocks(name, steps, warmup, dev, stream, peaks, peak_kind):
     if name == "copy_blocks_fork":
         pairs = np.stack([perm[:BLOCK_PAIRS], perm[BLOCK_PAIRS:2 * BLOCK_PAIRS]], 1)
         m = torch.from_numpy(pairs.astype(np.int64)).to(dev)
-        ms, n = timed(lambda: pa.pa_copy_blocks(pools[0::2], pools[1::2], m, stream=stream),
-                      "copy_blocks")
+        keys, vals = pools[0::2], pools[1::2]
+        call = lambda: pa.pa_copy_blocks(keys, vals, m, stream=stream)
+        # A direct call costs the host about as long as the kernel runs (the binding
+        # gathers 64 pool pointers), so timed call by call the device can idle between
+        # kernels and the figure follows the host's speed.  The call is captured once in
+        # a CUDA graph and replayed, so the timing is the device's; the host's cost per
+        # direct call is reported beside it.
+        with torch.cuda.stream(stream):
+            call()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+        torch.cuda.synchronize()
+
+        def replay():
+            with torch.cuda.stream(stream):
+                graph.replay()
+        ms, n = timed(replay, "copy_blocks")
+        t0 = time.perf_counter()
+        for _ in range(20):
+            call()
+        host_us = (time.perf_counter() - t0) / 20 * 1e6
+        torch.cuda.synchronize()
+        ms_direct, _ = timed(call, "copy_blocks_direct")
+        del graph
         hbm = 2 * moved / (ms / 1e3) / 1e9                  # read + write
         st = stats["copy_blocks"]
         return {"value": round(hbm, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
@@ -720,6 +744,9 @@ def bench_blocks(name, steps, warmup, dev, stream, peaks, peak_kind):
                 "median_GB/s": round(2 * moved / (st["median_ms"] / 1e3) / 1e9, 2),
                 "max_GB/s": round(2 * moved / (st["min_ms"] / 1e3) / 1e9, 2),
                 "kernels_ms": {"copy_blocks": round(ms, 5)},
+                "timing": "CUDA graph replays of one captured pa_copy_blocks call",
+                "direct_calls": {"GB/s": round(2 * moved / (ms_direct / 1e3) / 1e9, 2),
+                                 "host_us_per_call": round(host_us, 1)},
                 "roofline": roofline("hbm", hbm, peaks["hbm_gbs"], "GB/s", None, peak_kind),
                 "roofline_nominal_frac": nominal_frac(hbm, "hbm"),
                 "config": blocks_config(name)}
