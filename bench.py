@@ -70,14 +70,17 @@ TRAFFIC = {
     "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
         "src": "23c62bb4aa65e8f7", "bytes_per_launch": 573813760},
     # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
-    # causal prefill: dram__bytes_read.sum 294.99 MB + dram__bytes_write.sum 108.21 MB
-    # (captured on source 024cc71c5a1bbe51; re-keyed after a comment-only edit)
+    # causal prefill: dram__bytes_read.sum 299.76 MB + dram__bytes_write.sum 108.24 MB
     "ragged_prefill:ragged_prefill_r16_h32kv8_d128": {
-        "src": "3ff2430e17fafd35", "bytes_per_launch": 403205632},
+        "src": "b5cbd151fc7c0059", "bytes_per_launch": 407998208},
+    # ncu capture of one prefill_kernel<256,64,paged> launch on the chunked paged prefill:
+    # dram__bytes_read.sum 377.21 MB + dram__bytes_write.sum 22.65 MB
+    "ragged_prefill:chunked_paged_prefill_r8_h16kv8_d256": {
+        "src": "b5cbd151fc7c0059", "bytes_per_launch": 399863040},
     # ncu capture of one decode_tc8_kernel<4> launch on the Llama-8B decode workload over
-    # an FP8 cache: dram__bytes_read.sum 284.47 MB + dram__bytes_write.sum 4.72 MB
+    # an FP8 cache: dram__bytes_read.sum 284.45 MB + dram__bytes_write.sum 4.31 MB
     "decode_partitions:llama8b_decode_fp8_b64_h32kv8_d128": {
-        "src": "a9c251812034d7df", "bytes_per_launch": 289189888},
+        "src": "805c9dde768d1484", "bytes_per_launch": 288761600},
 }
 
 

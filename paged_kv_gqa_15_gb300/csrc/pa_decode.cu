@@ -150,7 +150,8 @@ cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaS
     if (p.num_seqs == 0) return cudaSuccess;
     if (decode_tc_supported(p, head_dim))
         return split ? launch_decode_tc(p, stream) : launch_decode_tc_single(p, stream);
-    if (split && decode_tc8_supported(p, head_dim)) return launch_decode_tc8(p, stream);
+    if (decode_tc8_supported(p, head_dim))
+        return split ? launch_decode_tc8(p, stream) : launch_decode_tc8_single(p, stream);
     if (p.kv_fp8) return launch_decode_fp8(p, head_dim, split, stream);
     return launch_decode_cache<false>(p, head_dim, split, stream);
 }

@@ -45,6 +45,7 @@
 //    sort in shared memory), so they agree on the assignment.
 #include <cuda.h>
 
+#include "pa_decode_pairs.cuh"
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_tcgen05.cuh"
@@ -76,8 +77,7 @@ constexpr uint32_t kOffP = kOffQ + 2 * kQBytes;
 constexpr uint32_t kOffRed = kOffP + kPBytes;                // float [2][4 warps][16]
 constexpr uint32_t kOffPref = kOffRed + 2 * 4 * kN * 4;      // int [MAXB + 1]
 constexpr int kMaxSeqsTc = 2048;
-constexpr int kSortKeys = 1024;                // single pass: partition-count buckets
-static_assert(kSortKeys * 4 <= kPBytes, "the sort's histogram fits in the P buffer");
+static_assert(kPairSortKeys * 4 <= kPBytes, "the single pass's sort histogram fits in P");
 constexpr uint32_t kOffBar = kOffPref + (kMaxSeqsTc + 8) * 4;
 constexpr uint32_t kSmemTc = kOffBar + 256 + 1024;           // + realignment slack
 constexpr uint32_t kTmemCols = 256;            // S: 2 x 4 tiles x 16; O: 2 x 16
@@ -112,51 +112,12 @@ __device__ __forceinline__ bool tc_item(const DecodeParams &p, const int *pref, 
     return true;
 }
 
-// Active partitions of a sequence of L tokens (those reaching into the window).
-__device__ __forceinline__ int tc_parts(int L, int window) {
-    return (L + kPartition - 1) / kPartition - window_start(L, window) / kPartition;
-}
-
-// The single pass's walk over this CTA's (sequence, kv head) pairs, one partition per
-// step: order[] lists the sequences by partition count, heaviest first; pair rank r of
-// this CTA is snake position r * C + c (r even) or r * C + C - 1 - c (r odd), and pair
-// position q is sequence order[q / nkv], kv head q % nkv.  Each role keeps its own walk
-// and asks for its steps e = 0, 1, 2, ... in order.
-struct TcWalk {
-    int r = -1;       // rank of the current pair within this CTA (-1: none yet)
-    int base = 0;     // step of the current pair's first partition
-    int np = 0;       // its active partitions
-    int b = 0, kh = 0, first_part = 0;
-
-    __device__ __forceinline__ bool at(const DecodeParams &p, const int *order, int e, int &ob,
-                                       int &okh, int &opart) {
-        const int C = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-        const long long n_pairs = static_cast<long long>(p.num_seqs) * p.num_kv_heads;
-        while (r < 0 || e >= base + np) {
-            if (r >= 0) base += np;
-            ++r;
-            const long long q = static_cast<long long>(r) * C + ((r & 1) ? C - 1 - c : c);
-            if (q >= n_pairs) return false;
-            b = order[q / p.num_kv_heads];
-            kh = static_cast<int>(q % p.num_kv_heads);
-            const int L = tc_seq_len(p, b, false);
-            np = tc_parts(L, p.window);
-            first_part = window_start(L, p.window) / kPartition;
-            if (np == 0) return false;   // sorted heaviest first: the rest are empty too
-        }
-        ob = b;
-        okh = kh;
-        opart = first_part + (e - base);
-        return true;
-    }
-};
-
 // The k-th item of this CTA in either mode.
 template <bool SINGLE>
 struct TcItems {
     const int *pref;  // split: prefix of partition counts; single: sequences by weight
     long long total;
-    TcWalk walk;
+    PairWalk walk;
     __device__ __forceinline__ bool at(const DecodeParams &p, int e, int &b, int &kh, int &part) {
         if constexpr (SINGLE) return walk.at(p, pref, e, b, kh, part);
         else return tc_item(p, pref, total, e, b, kh, part);
@@ -181,15 +142,7 @@ __device__ __forceinline__ TcSpan tc_span(const DecodeParams &p, int b, int part
 }
 
 __device__ __forceinline__ int tc_seq_len(const DecodeParams &p, int b, bool flag) {
-    int L = p.seq_lens[b];
-    if (L < 0) L = 0;
-    int cap = p.max_blocks * kBlockSize;
-    if (p.max_seq_len < cap) cap = p.max_seq_len;
-    if (L > cap) {
-        if (flag) atomicOr(p.status, kStatusBounds);
-        L = cap;
-    }
-    return L;
+    return pair_seq_len(p, b, flag);
 }
 
 template <int G, bool SINGLE>
@@ -291,61 +244,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
     }
     } else {
-        // the sequences by partition count, heaviest first, into pref[]: a stable
-        // counting sort (key 1023 - min(partitions, 1023)) with its histogram in the P
-        // buffer, which is zeroed again afterwards; and zeros for the outputs of
-        // sequences with no visible token, which no pair's epilogue writes
-        int *hist = reinterpret_cast<int *>(smem + kOffP);
-        for (int k = threadIdx.x; k < kSortKeys; k += kThreadsTc) hist[k] = 0;
-        __syncthreads();
-        auto key_of = [&](int b) {
-            return kSortKeys - 1 - min(tc_parts(tc_seq_len(p, b, false), p.window), kSortKeys - 1);
-        };
-        for (int b = threadIdx.x; b < p.num_seqs; b += kThreadsTc) {
-            const int L = tc_seq_len(p, b, blockIdx.x == 0);
-            atomicAdd(&hist[key_of(b)], 1);
-            if (tc_parts(L, p.window) == 0 && b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
-                __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) +
-                                   static_cast<int64_t>(b) * p.num_q_heads * kHD;
-                for (int i = 0; i < p.num_q_heads * kHD; ++i) o[i] = __float2bfloat16_rn(0.f);
-            }
-        }
-        __syncthreads();
-        if (warp == 0) {   // exclusive prefix of the histogram, then the stable scatter
-            constexpr int PER = kSortKeys / 32;
-            int loc = 0;
-            for (int i = 0; i < PER; ++i) loc += hist[lane * PER + i];
-            int incl = loc;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int u = __shfl_up_sync(kFullMaskTc, incl, off);
-                if (lane >= off) incl += u;
-            }
-            int run = incl - loc;
-            for (int i = 0; i < PER; ++i) {
-                const int cnt = hist[lane * PER + i];
-                hist[lane * PER + i] = run;
-                run += cnt;
-            }
-            __syncwarp();
-            for (int base = 0; base < p.num_seqs; base += 32) {
-                const int b = base + lane;
-                const bool v = b < p.num_seqs;
-                const int key = v ? key_of(b) : -1 - lane;   // invalid lanes match no one
-                const unsigned same = __match_any_sync(kFullMaskTc, key);
-                const int leader = __ffs(same) - 1;
-                int start = 0;
-                if (v && lane == leader) {
-                    start = hist[key];
-                    hist[key] = start + __popc(same);
-                }
-                start = __shfl_sync(kFullMaskTc, start, leader);
-                if (v) pref[start + __popc(same & ((1u << lane) - 1u))] = b;
-                __syncwarp();
-            }
-        }
-        __syncthreads();
-        for (int k = threadIdx.x; k < kSortKeys; k += kThreadsTc) hist[k] = 0;   // P padding
+        // the sequences by partition count, heaviest first, into pref[] (the sort's
+        // histogram lives in the P buffer, whose zero padding it restores)
+        pair_sort<kThreadsTc>(p, pref, reinterpret_cast<int *>(smem + kOffP), kHD);
         fence_proxy_async_smem();
     }
     tc_fence_before_sync();
@@ -658,7 +559,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&o_free[x]);
             if constexpr (SINGLE) {
-                if (e == items.walk.base) {
+                if (items.walk.first(e)) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         run_m[g] = -INFINITY;
@@ -679,7 +580,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                             run_m[g] = M;
                         }
                     }
-                    if (e == items.walk.base + items.walk.np - 1) {   // the pair's last partition
+                    if (items.walk.last(e)) {   // the pair's last partition
 #pragma unroll
                         for (int g = 0; g < G; ++g)
                             static_cast<__nv_bfloat16 *>(p.out)[(static_cast<int64_t>(b) * nq +

@@ -33,9 +33,13 @@
 //    two items ahead, so the K producer does nothing but stream tiles: with the split
 //    on the producer, that warp's serial work per item set the whole kernel's pace.
 //    Every wait is bounded.
+//  * The same kernel runs the single pass (pa_decode) as the bf16 one does: a CTA owns
+//    whole (sequence, kv head) pairs (pa_decode_pairs.cuh) and its epilogue merges the
+//    pair's partitions in registers, writing the bf16 output after the last one.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include "pa_decode_pairs.cuh"
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_tcgen05.cuh"
@@ -72,6 +76,7 @@ constexpr uint32_t kTmS = 0, kTmO = 128;
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 static_assert((2 * (kKStages + kV8Stages) + 16) * 8 <= 512, "barriers fit");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms on 1 KB boundaries");
+static_assert(kPairSortKeys * 4 <= kPBytes, "the single pass's sort histogram fits in P");
 
 struct DecodeTc8Params {
     CUtensorMap tm_k;   // pool bytes as (hd, 16 rows, nkv, blocks), box {128, 16, 1, 1}
@@ -80,15 +85,7 @@ struct DecodeTc8Params {
 };
 
 __device__ __forceinline__ int seq_len8(const DecodeParams &p, int b, bool flag) {
-    int L = p.seq_lens[b];
-    if (L < 0) L = 0;
-    int cap = p.max_blocks * kBlockSize;
-    if (p.max_seq_len < cap) cap = p.max_seq_len;
-    if (L > cap) {
-        if (flag) atomicOr(p.status, kStatusBounds);
-        L = cap;
-    }
-    return L;
+    return pair_seq_len(p, b, flag);
 }
 
 // The k-th item of this CTA: (b, kh, partition); false when there is none.
@@ -109,6 +106,19 @@ __device__ __forceinline__ bool item8(const DecodeParams &p, const int *pref, lo
         part += window_start(seq_len8(p, b, false), p.window) / kPartition;
     return true;
 }
+
+// The k-th item of this CTA in either mode (split: the compact partition list; single
+// pass: the walk over this CTA's pairs).
+template <bool SINGLE>
+struct Items8 {
+    const int *pref;  // split: prefix of partition counts; single: sequences by weight
+    long long total;
+    PairWalk walk;
+    __device__ __forceinline__ bool at(const DecodeParams &p, int e, int &b, int &kh, int &part) {
+        if constexpr (SINGLE) return walk.at(p, pref, e, b, kh, part);
+        else return item8(p, pref, total, e, b, kh, part);
+    }
+};
 
 // Tokens [t0 + t_lo, t0 + n_tok) of the partition at t0, in tiles i_lo .. n_tiles - 1.
 struct Span8 {
@@ -192,7 +202,7 @@ __device__ __forceinline__ void store_q_split(uint8_t *qb, int c, const uint4 &r
         make_uint2(lw[0], lw[1]);
 }
 
-template <int G>
+template <int G, bool SINGLE>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc8_kernel(const __grid_constant__ DecodeTc8Params prm) {
     const DecodeParams &p = prm.d;
@@ -224,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tensor maps, which are launch parameters) runs before the wait; as a programmatic
     // dependent of the cache write it then overlaps that kernel.  Everything that reads
     // global memory (sequence lengths, block tables, q, the pools) comes after it.
-    // Q rows 2G .. 15 and P rows G .. 15 stay zero (padding of the MMA's N)
+    // Q and P rows 2G .. 15 stay zero (padding of the MMA's N)
     for (uint32_t i = threadIdx.x; i < (2 * kQBytes + 2 * kPBytes) / 16; i += kThreads)
         reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (threadIdx.x == 0) {
@@ -260,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    if constexpr (!SINGLE) {
     for (int b = threadIdx.x; b < p.num_seqs; b += kThreads) {
         const int L = seq_len8(p, b, blockIdx.x == 0);
         pref[b + 1] = (L + kPartition - 1) / kPartition - window_start(L, p.window) / kPartition;
@@ -280,11 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             carry += __shfl_sync(kMask, v, 31);
         }
     }
+    } else {
+        // the sequences by partition count, heaviest first, into pref[] (the sort's
+        // histogram lives in the P buffer, whose zero padding it restores)
+        pair_sort<kThreads>(p, pref, reinterpret_cast<int *>(smem + kOffP), kHD);
+        fence_proxy_async_smem();
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const long long total = static_cast<long long>(pref[p.num_seqs]) * p.num_kv_heads;
+    const long long total = SINGLE ? 0 : static_cast<long long>(pref[p.num_seqs]) * p.num_kv_heads;
     const int nq = p.num_q_heads;
 
     if (warp == 0 || warp == 6) {
@@ -299,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t it = 0;
         int stop = 0;
         int b, kh, part;
-        for (int e = 0; !stop && item8(p, pref, total, e, b, kh, part); ++e) {
+        Items8<SINGLE> items{pref, total};
+        for (int e = 0; !stop && items.at(p, e, b, kh, part); ++e) {
             const Span8 sp = span8(p, b, part);
             // page ids of the partition, one per lane (past the sequence, before the window
             // or bad: an out-of-range box that reads zeros); the V producer flags nothing
@@ -349,9 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t p_desc = smem_desc_sw128(smem_addr(smem + kOffP), 16, 1024);
             uint32_t kit = 0, vit = 0;
             bool ok = true;
+            Items8<SINGLE> items{pref, total};
             auto item_span = [&](int e) -> Span8 {
                 int b, kh, part;
-                if (!item8(p, pref, total, e, b, kh, part)) {
+                if (!items.at(p, e, b, kh, part)) {
                     Span8 none = {};
                     none.n_tiles = -1;
                     return none;
@@ -464,16 +483,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // does nothing but stream K tiles.  Thread sid < 16 G holds one 16-byte chunk of
         // q, loaded an item before it is split so that the load's latency stays off
         // this chain.
+        // each of q_chunk, q_write and the item loop walks the items in its own order
+        Items8<SINGLE> items_qc{pref, total}, items_qw{pref, total}, items{pref, total};
         auto q_chunk = [&](int e) -> uint4 {
             int bb, kk, pp;
-            if (sid >= 16 * G || !item8(p, pref, total, e, bb, kk, pp)) return make_uint4(0u, 0u, 0u, 0u);
+            if (sid >= 16 * G || !items_qc.at(p, e, bb, kk, pp)) return make_uint4(0u, 0u, 0u, 0u);
             const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q) +
                                       (static_cast<int64_t>(bb) * nq + kk * G) * kHD;
             return __ldg(reinterpret_cast<const uint4 *>(qg) + sid);
         };
         auto q_write = [&](int e, const uint4 &raw) {
             int bb, kk, pp;
-            if (!item8(p, pref, total, e, bb, kk, pp)) return;   // uniform over the CTA
+            if (!items_qw.at(p, e, bb, kk, pp)) return;   // uniform over the CTA
             if (sid < 16 * G) {                                  // warp-uniform
                 const float s = q_split_scale(head_max(raw));
                 if ((lane & 15) == 0) qinv[(e & 1) * kN + (sid >> 4)] = 1.f / s;  // exact
@@ -490,10 +511,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The epilogue of an item (O^T from TMEM, normalised, to the partials) is deferred
         // until the next item's P is written, so that the P.V of one item overlaps the
         // softmax of the next; its inputs wait in these registers.
-        bool have_prev = false, prev_got = false;
+        bool have_prev = false, prev_got = false, prev_first = false, prev_last = false;
         int prev_b = 0, prev_kh = 0, prev_part = 0, prev_x = 0;
         uint32_t prev_use = 0;
         float prev_sm[G], prev_mx[G];
+        // single pass: the pair's running max (log2 units), sum and unnormalised output
+        // (this thread's dim, v_scale not yet applied) over the partitions merged so far
+        float run_m[G], run_l[G], run_o[G];
         auto epilogue = [&]() -> bool {
             bool done = prev_got && mbar_wait(&o_full[prev_x], prev_use & 1, p.status, abort_flag);
             done = !__any_sync(kMask, !done);
@@ -510,7 +534,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&o_free[prev_x]);
-            if (done) {
+            if constexpr (SINGLE) {
+                if (prev_first) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        run_m[g] = -INFINITY;
+                        run_l[g] = 0.f;
+                        run_o[g] = 0.f;
+                    }
+                }
+                if (done) {
+                    // log-sum-exp merge of this partition into the running state
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float og = (__uint_as_float(o[g]) + __uint_as_float(o[G + g])) *
+                                         (1.f / kPScale);
+                        const float M = fmaxf(run_m[g], prev_mx[g]);
+                        if (M != -INFINITY) {
+                            const float fa = run_m[g] == -INFINITY ? 0.f : exp2f(run_m[g] - M);
+                            const float fb = prev_mx[g] == -INFINITY ? 0.f : exp2f(prev_mx[g] - M);
+                            run_o[g] = run_o[g] * fa + og * fb;
+                            run_l[g] = run_l[g] * fa + prev_sm[g] * fb;
+                            run_m[g] = M;
+                        }
+                    }
+                    if (prev_last) {   // the pair's last partition: its output
+#pragma unroll
+                        for (int g = 0; g < G; ++g)
+                            static_cast<__nv_bfloat16 *>(p.out)[(static_cast<int64_t>(prev_b) * nq +
+                                                                 prev_kh * G + g) * kHD + row] =
+                                __float2bfloat16_rn(
+                                    run_l[g] > 0.f ? run_o[g] / run_l[g] * p.v_scale : 0.f);
+                    }
+                }
+            } else if (done) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const int64_t r =
@@ -526,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return done;
         };
-        for (int e = 0; item8(p, pref, total, e, b, kh, part); ++e) {
+        for (int e = 0; items.at(p, e, b, kh, part); ++e) {
             const Span8 sp = span8(p, b, part);
             const int x = e & 1;
             const uint32_t use = e >> 1;
@@ -637,6 +694,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             prev_x = x;
             prev_use = use;
             prev_got = got;
+            prev_first = items.walk.first(e);
+            prev_last = items.walk.last(e);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 prev_sm[g] = sm[g];
@@ -655,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int G>
+template <int G, bool SINGLE>
 cudaError_t launch_tc8(const DecodeParams &p, cudaStream_t stream) {
     DecodeTc8Params prm;
     prm.d = p;
@@ -670,7 +729,7 @@ cudaError_t launch_tc8(const DecodeParams &p, cudaStream_t stream) {
             !encode_tensor_map_u8(&prm.tm_v, p.v_cache, 4, dims, str, box))
             return cudaErrorInvalidValue;
     }
-    auto kern = decode_tc8_kernel<G>;
+    auto kern = decode_tc8_kernel<G, SINGLE>;
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -683,8 +742,9 @@ cudaError_t launch_tc8(const DecodeParams &p, cudaStream_t stream) {
     static int sms = 0;
     if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 152;
+    // split: one CTA per item at most; single pass: one per (sequence, kv head) pair
     const long long slots = static_cast<long long>(p.num_seqs) * p.num_kv_heads *
-                            active_partitions_cap(p.max_parts, p.window);
+                            (SINGLE ? 1 : active_partitions_cap(p.max_parts, p.window));
     long long n = sms;
     if (slots < n) n = slots;
     cudaLaunchConfig_t cfg = {};
@@ -716,8 +776,17 @@ bool decode_tc8_supported(const DecodeParams &p, int head_dim) {
 cudaError_t launch_decode_tc8(const DecodeParams &p, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
     switch (p.num_q_heads / p.num_kv_heads) {
-        case 4: return launch_tc8<4>(p, stream);
-        case 8: return launch_tc8<8>(p, stream);
+        case 4: return launch_tc8<4, false>(p, stream);
+        case 8: return launch_tc8<8, false>(p, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+cudaError_t launch_decode_tc8_single(const DecodeParams &p, cudaStream_t stream) {
+    if (p.num_seqs == 0) return cudaSuccess;
+    switch (p.num_q_heads / p.num_kv_heads) {
+        case 4: return launch_tc8<4, true>(p, stream);
+        case 8: return launch_tc8<8, true>(p, stream);
         default: return cudaErrorNotSupported;
     }
 }

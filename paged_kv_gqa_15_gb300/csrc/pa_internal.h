@@ -95,6 +95,7 @@ cudaError_t launch_decode_tc_single(const DecodeParams &p, cudaStream_t stream);
 // The same over an FP8 E4M3 cache (pa_decode_tc_fp8.cu).
 bool decode_tc8_supported(const DecodeParams &p, int head_dim);
 cudaError_t launch_decode_tc8(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_decode_tc8_single(const DecodeParams &p, cudaStream_t stream);
 // Returns cudaErrorNotSupported for an unsupported (head_dim, group) pair.
 cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaStream_t stream);
 // The CUDA-core decode over FP8 E4M3 caches (pa_decode_fp8.cu).
