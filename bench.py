@@ -66,9 +66,9 @@ PARITY_MAX_ABS, PARITY_MEAN_ABS = 2e-2, 2e-3
 # for the source file hash they were measured on (otherwise reported as null).
 TRAFFIC = {
     # ncu capture of one decode_tc_kernel<4> launch on the Llama-8B decode workload:
-    # dram__bytes_read.sum 568.37 MB + dram__bytes_write.sum 4.92 MB
+    # dram__bytes_read.sum 568.31 MB + dram__bytes_write.sum 5.21 MB
     "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
-        "src": "cabba7bf355c890a", "bytes_per_launch": 573293056},
+        "src": "5b3756e870a8f35e", "bytes_per_launch": 573526784},
     # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
     # causal prefill: dram__bytes_read.sum 299.76 MB + dram__bytes_write.sum 108.24 MB
     "ragged_prefill:ragged_prefill_r16_h32kv8_d128": {

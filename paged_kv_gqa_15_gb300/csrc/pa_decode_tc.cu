@@ -60,8 +60,12 @@ constexpr int kTiles = kPartition / kTok;      // tiles per partition
 constexpr int kPagesPerTile = kTok / kBlockSize;
 constexpr int kN = 16;                         // MMA N: query heads, zero-padded
 constexpr int kThreadsTc = 256;                // K producer, MMA, 4 softmax, V producer, P.V MMA
-constexpr int kKStages = 2;                    // K tile ring
-constexpr int kVStages = 4;                    // V tile ring: a whole partition
+// Tile rings: 3 K and 3 V stages (a partition is 4 tiles).  Against 2 K / 4 V stages
+// this measured ~0.5 % faster on the Llama-8B batch, ~1 % on the 4096-key window and
+// ~1.2 % on the long-context batch: a partition's first three K tiles are in flight at
+// once, so its softmax starts a round trip earlier.
+constexpr int kKStages = 3;                    // K tile ring
+constexpr int kVStages = 3;                    // V tile ring
 constexpr uint32_t kTileChunk = kTok * 128;    // one 64-column chunk of a tile
 constexpr uint32_t kTileBytes = 2 * kTileChunk;
 constexpr uint32_t kSmallChunk = kN * 128;     // one 64-column chunk of Q^T or P
@@ -83,6 +87,7 @@ constexpr uint32_t kSmemTc = kOffBar + 256 + 1024;           // + realignment sl
 constexpr uint32_t kTmemCols = 256;            // S: 2 x 4 tiles x 16; O: 2 x 16
 constexpr uint32_t kTmS = 0, kTmO = 128;
 static_assert(kSmemTc <= 227 * 1024, "shared memory");
+static_assert(kKStages <= 3 && kVStages <= 3, "the barrier layout holds 3 stages per ring");
 
 struct DecodeTcParams {
     CUtensorMap tm_q;   // q as (hd, nq, B), box {64, g, 1}
@@ -162,10 +167,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     //   s_free[2]   softmax has read S^T (one arrival per softmax warp)
     //   p_full[2]   P written to shared memory (one arrival per softmax warp)
     //   o_full[2]   O^T done (commit);  o_free[2]: epilogue has read O^T
-    uint64_t *k_full = bars + 0;     // [2]
-    uint64_t *k_empty = bars + 2;    // [2]
-    uint64_t *v_full = bars + 4;     // [4]
-    uint64_t *v_empty = bars + 8;    // [4]
+    uint64_t *k_full = bars + 0;     // [kKStages <= 3]
+    uint64_t *k_empty = bars + 3;    // [kKStages]
+    uint64_t *v_full = bars + 6;     // [kVStages <= 3]
+    uint64_t *v_empty = bars + 9;    // [kVStages]
     uint64_t *q_full = bars + 12;
     uint64_t *q_empty = bars + 14;
     uint64_t *s_full = bars + 16;
