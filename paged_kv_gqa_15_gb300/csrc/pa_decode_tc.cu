@@ -224,6 +224,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         prefetch_tensormap(&prm.tm_v);
         prefetch_tensormap(&prm.tm_q);
     }
+    if (warp >= 2 && warp < 6)   // the softmax warps are idle until the first scores
+        prefetch_decode_inputs(p.seq_lens, p.block_tables, p.q, p.num_seqs, p.max_blocks,
+                               static_cast<size_t>(p.num_seqs) * p.num_q_heads * kHD * 2,
+                               threadIdx.x - 64, 128);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if constexpr (!SINGLE) {

@@ -268,6 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&prm.tm_k);
         prefetch_tensormap(&prm.tm_v);
     }
+    if (warp >= 2 && warp < 6)   // the softmax warps are idle until the first scores
+        prefetch_decode_inputs(p.seq_lens, p.block_tables, p.q, p.num_seqs, p.max_blocks,
+                               static_cast<size_t>(p.num_seqs) * p.num_q_heads * kHD * 2,
+                               threadIdx.x - 64, 128);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if constexpr (!SINGLE) {

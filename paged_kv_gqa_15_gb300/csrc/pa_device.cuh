@@ -50,6 +50,31 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Brings lines [idx * 128, bytes) of `base`, every stride-th 128-byte line, into L2.  A
+// dependent launch may issue it before griddepcontrol.wait even for data the kernel
+// before it writes: L2 is where writes become visible, so a later load sees them.
+__device__ __forceinline__ void prefetch_l2_lines(const void *base, size_t bytes, unsigned idx,
+                                                  unsigned stride) {
+    const char *p = static_cast<const char *>(base);
+    for (size_t off = static_cast<size_t>(idx) * 128; off < bytes;
+         off += static_cast<size_t>(stride) * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
+}
+
+// The decode kernels' first reads after the dependency wait -- sequence lengths, block
+// tables and q -- into L2 beforehand, spread over the grid (up to 4 MB of tables).
+__device__ __forceinline__ void prefetch_decode_inputs(const int32_t *seq_lens,
+                                                       const int32_t *block_tables,
+                                                       const void *q, int num_seqs,
+                                                       int max_blocks, size_t q_bytes,
+                                                       unsigned t, unsigned nt) {
+    const unsigned idx = blockIdx.x * nt + t, stride = gridDim.x * nt;
+    prefetch_l2_lines(seq_lens, static_cast<size_t>(num_seqs) * 4, idx, stride);
+    const size_t tb = static_cast<size_t>(num_seqs) * max_blocks * 4;
+    if (tb <= (4u << 20)) prefetch_l2_lines(block_tables, tb, idx, stride);
+    if (q_bytes <= (4u << 20)) prefetch_l2_lines(q, q_bytes, idx, stride);
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
