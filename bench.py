@@ -66,17 +66,17 @@ PARITY_MAX_ABS, PARITY_MEAN_ABS = 2e-2, 2e-3
 # for the source file hash they were measured on (otherwise reported as null).
 TRAFFIC = {
     # ncu capture of one decode_tc_kernel<4> launch on the Llama-8B decode workload:
-    # dram__bytes_read.sum 568.31 MB + dram__bytes_write.sum 5.21 MB
+    # dram__bytes_read.sum 568.34 MB + dram__bytes_write.sum 5.12 MB
     "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
-        "src": "5b3756e870a8f35e", "bytes_per_launch": 573526784},
+        "src": "925dfe2e4a8d4844", "bytes_per_launch": 573459200},
     # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
-    # causal prefill: dram__bytes_read.sum 299.76 MB + dram__bytes_write.sum 108.24 MB
+    # causal prefill: dram__bytes_read.sum 298.53 MB + dram__bytes_write.sum 108.54 MB
     "ragged_prefill:ragged_prefill_r16_h32kv8_d128": {
-        "src": "b5cbd151fc7c0059", "bytes_per_launch": 407998208},
+        "src": "fe29602adfbe4d3a", "bytes_per_launch": 407071488},
     # ncu capture of one prefill_kernel<256,64,paged> launch on the chunked paged prefill:
-    # dram__bytes_read.sum 377.21 MB + dram__bytes_write.sum 22.65 MB
+    # dram__bytes_read.sum 396.10 MB + dram__bytes_write.sum 23.06 MB
     "ragged_prefill:chunked_paged_prefill_r8_h16kv8_d256": {
-        "src": "b5cbd151fc7c0059", "bytes_per_launch": 399863040},
+        "src": "fe29602adfbe4d3a", "bytes_per_launch": 419157248},
     # ncu capture of one decode_tc8_kernel<4> launch on the Llama-8B decode workload over
     # an FP8 cache: dram__bytes_read.sum 284.45 MB + dram__bytes_write.sum 4.31 MB
     "decode_partitions:llama8b_decode_fp8_b64_h32kv8_d128": {
