@@ -78,9 +78,9 @@ TRAFFIC = {
     "ragged_prefill:chunked_paged_prefill_r8_h16kv8_d256": {
         "src": "fe29602adfbe4d3a", "bytes_per_launch": 419157248},
     # ncu capture of one decode_tc8_kernel<4> launch on the Llama-8B decode workload over
-    # an FP8 cache: dram__bytes_read.sum 284.45 MB + dram__bytes_write.sum 4.31 MB
+    # an FP8 cache: dram__bytes_read.sum 284.48 MB + dram__bytes_write.sum 4.04 MB
     "decode_partitions:llama8b_decode_fp8_b64_h32kv8_d128": {
-        "src": "43624b868bfe5f42", "bytes_per_launch": 288755200},
+        "src": "b0c4bd7d5d2d957b", "bytes_per_launch": 288514048},
 }
 
 
