@@ -1021,7 +1021,7 @@ def main(argv=None):
     ap.add_argument("--extra", default="tiny_decode,long_context_decode,ragged_prefill,"
                                        "chunked_paged_prefill,window_decode,window_prefill,"
                                        "llama8b_decode_fp8,long_context_decode_fp8,"
-                                       "llama8b_decode_single,mha_decode,"
+                                       "llama8b_decode_single,mha_decode,gqa7_decode,"
                                        "copy_blocks_fork,swap_blocks",
                     help="other workloads measured in the same run (N=1 only); 'none' for none")
     ap.add_argument("--no-cpu-baseline", action="store_true",

@@ -80,9 +80,6 @@ int check_heads(int head_dim, int num_q_heads, int num_kv_heads) {
     if (num_q_heads % num_kv_heads != 0)
         return fail(PA_ERR_INVALID, "num_q_heads %d is not a multiple of num_kv_heads %d",
                     num_q_heads, num_kv_heads);
-    const int g = num_q_heads / num_kv_heads;
-    if (g != 1 && g != 2 && g != 4 && g != 8)
-        return fail(PA_ERR_UNSUPPORTED, "GQA group size %d not in {1, 2, 4, 8}", g);
     if (head_dim != 64 && head_dim != 128 && head_dim != 256)
         return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", head_dim);
     return PA_OK;
@@ -154,6 +151,8 @@ int decode_common(pa::DecodeParams &p, void *out, const void *q, const void *k_c
     p.num_seqs = num_seqs;
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
+    p.kv_rep = 1;
+    p.pool_kv_heads = num_kv_heads;
     p.max_blocks = max_blocks_per_seq;
     p.scale_log2 = sm_scale * 1.4426950408889634f;
     p.rows_contiguous = (st == head_dim) ? 1 : 0;

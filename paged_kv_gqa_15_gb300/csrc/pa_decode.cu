@@ -1,6 +1,8 @@
 // pa_decode.cu -- bf16-cache instantiation of the paged GQA decode kernel
 // (pa_decode_kernel.cuh), the log-sum-exp merge of the split partitions, and the
 // decode / merge dispatch.
+#include <initializer_list>
+
 #include "pa_decode_kernel.cuh"
 
 namespace pa {
@@ -146,12 +148,47 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(const __grid_constant__
 }  // namespace
 
 
-cudaError_t launch_decode(const DecodeParams &p, int head_dim, bool split, cudaStream_t stream) {
-    if (p.num_seqs == 0) return cudaSuccess;
-    if (decode_tc_supported(p, head_dim))
-        return split ? launch_decode_tc(p, stream) : launch_decode_tc_single(p, stream);
-    if (decode_tc8_supported(p, head_dim))
-        return split ? launch_decode_tc8(p, stream) : launch_decode_tc8_single(p, stream);
+namespace {
+
+// The call's kv heads as kernel groups of g query heads: each pool kv head then serves
+// G / g groups (kv_rep), which read its pages through L2.
+DecodeParams regroup(const DecodeParams &p, int g) {
+    DecodeParams r = p;
+    const int G = p.num_q_heads / p.num_kv_heads;
+    r.num_kv_heads = p.num_q_heads / g;
+    r.kv_rep = G / g;
+    r.pool_kv_heads = p.num_kv_heads;
+    return r;
+}
+
+// The largest of cands (descending) that divides G, or 0.
+int largest_divisor(int G, std::initializer_list<int> cands) {
+    for (int c : cands)
+        if (G % c == 0) return c;
+    return 0;
+}
+
+}  // namespace
+
+// Any GQA group size G = nq / nkv ("paged_attn.py", forward_decode's num_queries_per_kv).
+// Kernels exist for some group sizes: the bf16 tensor-core decode (head_dim 128) for 3-8
+// query heads, the fp8 one for 4, 6 and 8, the CUDA-core decode for 1, 2, 4 and 8.  A
+// call runs on the first path with a kernel for G, else for the largest divisor of G it
+// has (G = 16 as two groups of 8 per kv head; a prime G > 8 on the CUDA cores as G groups
+// of one).  Groups 1 and 2 stay on the CUDA cores, which stream them at the copy peak.
+cudaError_t launch_decode(const DecodeParams &p0, int head_dim, bool split, cudaStream_t stream) {
+    if (p0.num_seqs == 0) return cudaSuccess;
+    const int G = p0.num_q_heads / p0.num_kv_heads;
+    const int g_tc = p0.kv_fp8 ? largest_divisor(G, {8, 6, 4})
+                               : (G <= 2 ? 0 : largest_divisor(G, {8, 7, 6, 5, 4, 3}));
+    if (g_tc) {
+        const DecodeParams p = regroup(p0, g_tc);
+        if (decode_tc_supported(p, head_dim))
+            return split ? launch_decode_tc(p, stream) : launch_decode_tc_single(p, stream);
+        if (decode_tc8_supported(p, head_dim))
+            return split ? launch_decode_tc8(p, stream) : launch_decode_tc8_single(p, stream);
+    }
+    const DecodeParams p = regroup(p0, largest_divisor(G, {8, 4, 2, 1}));
     if (p.kv_fp8) return launch_decode_fp8(p, head_dim, split, stream);
     return launch_decode_cache<false>(p, head_dim, split, stream);
 }

@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(DecodeCfg<HD, G, FP8>::NT, (HD == 256 || G == 
                         __syncwarp();
                         if (lane < C::SP && ok) {
                             const uint8_t *src = base + (static_cast<int64_t>(page) * p.s_block +
-                                                         static_cast<int64_t>(kh) * p.s_head) * C::ELEM;
+                                                         static_cast<int64_t>(kh / p.kv_rep) * p.s_head) * C::ELEM;
                             uint8_t *dst = ring + s * C::STAGE_BYTES + lane * C::PAGE_BYTES;
                             if (p.rows_contiguous) {
                                 bulk_copy_g2s_hint(dst, src, C::PAGE_BYTES, &full[s], policy);

@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             const TcSpan sp = tc_span(p, b, part);
             const int t0 = sp.t0;
             const int n_tiles = sp.n_tiles;
+            const int kvh = p.kv_rep == 1 ? kh : kh / p.kv_rep;   // the pool's kv head
             // page ids of the partition, one per lane (past the sequence, before the
             // window or bad: an out-of-range box that reads zeros); read before the Q load
             // is issued, so the read and that load overlap
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 if (lane < 2 * kPagesPerTile)   // K / V are read once: evict them first
                     tma_load_4d_hint(ring + s * kTileBytes + (lane & 1) * kTileChunk +
                                          (lane >> 1) * kBlockSize * 128,
-                                     tm, (lane & 1) * 64, 0, kh, pg, &full[s], policy);
+                                     tm, (lane & 1) * 64, 0, kvh, pg, &full[s], policy);
             }
         }
         // never leave the CTA with copies still landing in its shared memory
@@ -635,7 +636,7 @@ cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
             return cudaErrorInvalidValue;
     }
     {
-        const cuuint64_t dims[4] = {kHD, kBlockSize, static_cast<cuuint64_t>(p.num_kv_heads),
+        const cuuint64_t dims[4] = {kHD, kBlockSize, static_cast<cuuint64_t>(p.pool_kv_heads),
                                     static_cast<cuuint64_t>(p.num_blocks)};
         const cuuint64_t str[3] = {static_cast<cuuint64_t>(p.s_token) * 2,
                                    static_cast<cuuint64_t>(p.s_head) * 2,
@@ -682,7 +683,7 @@ cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
 
 bool decode_tc_supported(const DecodeParams &p, int head_dim) {
     const int g = p.num_kv_heads > 0 ? p.num_q_heads / p.num_kv_heads : 0;
-    return !p.kv_fp8 && head_dim == kHD && (g == 4 || g == 8) && p.num_seqs <= kMaxSeqsTc &&
+    return !p.kv_fp8 && head_dim == kHD && g >= 3 && g <= 8 && p.num_seqs <= kMaxSeqsTc &&
            (p.s_token * 2) % 16 == 0 && (p.s_head * 2) % 16 == 0 && (p.s_block * 2) % 16 == 0 &&
            (reinterpret_cast<uintptr_t>(p.k_cache) & 15) == 0 &&
            (reinterpret_cast<uintptr_t>(p.v_cache) & 15) == 0 &&
@@ -692,7 +693,11 @@ bool decode_tc_supported(const DecodeParams &p, int head_dim) {
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
     switch (p.num_q_heads / p.num_kv_heads) {
+        case 3: return launch_tc<3, false>(p, stream);
         case 4: return launch_tc<4, false>(p, stream);
+        case 5: return launch_tc<5, false>(p, stream);
+        case 6: return launch_tc<6, false>(p, stream);
+        case 7: return launch_tc<7, false>(p, stream);
         case 8: return launch_tc<8, false>(p, stream);
         default: return cudaErrorNotSupported;
     }
@@ -701,7 +706,11 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream) {
 cudaError_t launch_decode_tc_single(const DecodeParams &p, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
     switch (p.num_q_heads / p.num_kv_heads) {
+        case 3: return launch_tc<3, true>(p, stream);
         case 4: return launch_tc<4, true>(p, stream);
+        case 5: return launch_tc<5, true>(p, stream);
+        case 6: return launch_tc<6, true>(p, stream);
+        case 7: return launch_tc<7, true>(p, stream);
         case 8: return launch_tc<8, true>(p, stream);
         default: return cudaErrorNotSupported;
     }

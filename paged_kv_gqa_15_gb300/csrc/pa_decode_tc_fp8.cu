@@ -327,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Items8<SINGLE> items{pref, total};
         for (int e = 0; !stop && items.at(p, e, b, kh, part); ++e) {
             const Span8 sp = span8(p, b, part);
+            const int kvh = p.kv_rep == 1 ? kh : kh / p.kv_rep;   // the pool's kv head
             // page ids of the partition, one per lane (past the sequence, before the window
             // or bad: an out-of-range box that reads zeros); the V producer flags nothing
             const int np = (sp.n_tok + kBlockSize - 1) / kBlockSize;
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int pg = __shfl_sync(kMask, page, (i * kPagesPerTile + (lane & 7)) & 31);
                 if (lane < kPagesPerTile)   // K / V are read once: evict them first
                     tma_load_4d_hint(ring + s * kTile8Bytes + lane * kBlockSize * 128, tm, 0, 0,
-                                     kh, pg, &full[s], policy);
+                                     kvh, pg, &full[s], policy);
             }
         }
         // never leave the CTA with copies still landing in its shared memory
@@ -532,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[16];   // column g: head g's hi part, column G + g its lo part
             if (done) {
                 tc_fence_after_sync();
-                if constexpr (G == 8) {
+                if constexpr (2 * G > 8) {   // G hi and G lo columns
                     tmem_load_16(tmem + t_lane + kTmO + prev_x * kN, o);
                 } else {
                     tmem_load_8(tmem + t_lane + kTmO + prev_x * kN,
@@ -605,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool tile = got && i >= sp.i_lo && i * kTok < sp.n_tok;
                 uint32_t v[16];
                 if (tile) {
-                    if constexpr (G == 8) {
+                    if constexpr (2 * G > 8) {   // G hi and G lo columns
                         tmem_load_16(tmem + t_lane + kTmS + x * 64 + i * kN, v);
                     } else {
                         uint32_t (&v8)[8] = *reinterpret_cast<uint32_t (*)[8]>(v);
@@ -727,7 +728,7 @@ cudaError_t launch_tc8(const DecodeParams &p, cudaStream_t stream) {
     DecodeTc8Params prm;
     prm.d = p;
     {
-        const cuuint64_t dims[4] = {kHD, kBlockSize, static_cast<cuuint64_t>(p.num_kv_heads),
+        const cuuint64_t dims[4] = {kHD, kBlockSize, static_cast<cuuint64_t>(p.pool_kv_heads),
                                     static_cast<cuuint64_t>(p.num_blocks)};
         const cuuint64_t str[3] = {static_cast<cuuint64_t>(p.s_token),
                                    static_cast<cuuint64_t>(p.s_head),
@@ -774,7 +775,8 @@ cudaError_t launch_tc8(const DecodeParams &p, cudaStream_t stream) {
 
 bool decode_tc8_supported(const DecodeParams &p, int head_dim) {
     const int g = p.num_kv_heads > 0 ? p.num_q_heads / p.num_kv_heads : 0;
-    return p.kv_fp8 && head_dim == kHD && (g == 4 || g == 8) && p.num_seqs <= kMaxSeqs &&
+    // the P rows pair heads (g even); 2 g hi / lo rows fill the MMA's N of 16
+    return p.kv_fp8 && head_dim == kHD && (g == 4 || g == 6 || g == 8) && p.num_seqs <= kMaxSeqs &&
            p.s_token % 16 == 0 && p.s_head % 16 == 0 && p.s_block % 16 == 0 &&
            (reinterpret_cast<uintptr_t>(p.k_cache) & 15) == 0 &&
            (reinterpret_cast<uintptr_t>(p.v_cache) & 15) == 0 &&
@@ -785,6 +787,7 @@ cudaError_t launch_decode_tc8(const DecodeParams &p, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
     switch (p.num_q_heads / p.num_kv_heads) {
         case 4: return launch_tc8<4, false>(p, stream);
+        case 6: return launch_tc8<6, false>(p, stream);
         case 8: return launch_tc8<8, false>(p, stream);
         default: return cudaErrorNotSupported;
     }
@@ -794,6 +797,7 @@ cudaError_t launch_decode_tc8_single(const DecodeParams &p, cudaStream_t stream)
     if (p.num_seqs == 0) return cudaSuccess;
     switch (p.num_q_heads / p.num_kv_heads) {
         case 4: return launch_tc8<4, true>(p, stream);
+        case 6: return launch_tc8<6, true>(p, stream);
         case 8: return launch_tc8<8, true>(p, stream);
         default: return cudaErrorNotSupported;
     }

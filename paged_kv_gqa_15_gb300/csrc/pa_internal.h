@@ -31,6 +31,10 @@ struct DecodeParams {
     int64_t num_blocks;
     int64_t s_block, s_head, s_token;
     int num_seqs, num_q_heads, num_kv_heads, max_blocks;
+    // The kernels serve num_kv_heads groups of num_q_heads / num_kv_heads query heads;
+    // group kh reads pool kv head kh / kv_rep, of pool_kv_heads.  A call whose GQA group
+    // has no kernel of its own runs as kv_rep groups per pool kv head (launch_decode).
+    int kv_rep, pool_kv_heads;
     int max_parts;                // split: partitions per (b, h) in the workspace
     int max_seq_len;              // split: clamp for seq_lens
     float scale_log2;             // sm_scale * log2(e)

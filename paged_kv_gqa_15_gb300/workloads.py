@@ -364,6 +364,14 @@ def mha_decode():
                        split=True)
 
 
+def gqa7_decode():
+    """Split-KV decode with groups of 7 query heads, shaped like Qwen-2.5-7B (28 q / 4 kv
+    heads, hd 128): batch 64, seq_lens U[512, 4096]."""
+    rng = np.random.default_rng(1008)
+    lens = rng.integers(512, 4096, size=64, endpoint=True)
+    return make_decode("gqa7_decode_b64_h28kv4_d128", lens, 28, 4, 128, seed=1008, split=True)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "llama8b_decode": llama8b_decode,
@@ -376,4 +384,5 @@ WORKLOADS = {
     "window_prefill": window_prefill,
     "llama8b_decode_single": llama8b_decode_single,
     "mha_decode": mha_decode,
+    "gqa7_decode": gqa7_decode,
 }

@@ -52,7 +52,6 @@ def _decode(lib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(hd=96), pa.PA_ERR_UNSUPPORTED),
     (dict(nq=6, nkv=4), pa.PA_ERR_INVALID),
-    (dict(nq=12, nkv=2), pa.PA_ERR_UNSUPPORTED),     # group 6
     (dict(bs=32), pa.PA_ERR_UNSUPPORTED),
     (dict(nb=0), pa.PA_ERR_INVALID),
     (dict(mb=0), pa.PA_ERR_INVALID),

@@ -20,7 +20,7 @@ DEV = "cuda"
 
 DECODE = ["tiny_decode", "llama8b_decode", "long_context_decode", "window_decode",
           "llama8b_decode_fp8", "long_context_decode_fp8", "llama8b_decode_single",
-          "mha_decode"]
+          "mha_decode", "gqa7_decode"]
 PREFILL = ["ragged_prefill", "chunked_paged_prefill", "window_prefill"]
 
 
