@@ -487,12 +487,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
             for (int i = 0; i < kTiles; ++i) {
                 const bool tile = got && i >= sp.i_lo && i * kTok < n_tok;
-                uint32_t v[8];
+                constexpr int NL = G > 8 ? 16 : 8;   // S^T columns loaded: one per head
+                uint32_t v[NL];
                 if (tile) {
-                    tmem_load_8(tmem + t_lane + kTmS + x * 64 + i * kN, v);
+                    if constexpr (NL == 16) {
+                        tmem_load_16(tmem + t_lane + kTmS + x * 64 + i * kN, v);
+                    } else {
+                        tmem_load_8(tmem + t_lane + kTmS + x * 64 + i * kN, v);
+                    }
                 } else {
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) v[g] = 0u;
+                    for (int g = 0; g < NL; ++g) v[g] = 0u;
                 }
                 const bool valid = tile && i * kTok + row < n_tok && i * kTok + row >= sp.t_lo;
 #pragma unroll
@@ -540,15 +545,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 for (int g = 0; g < G; ++g) rl[g] = sm[g];
             }
             // P (bf16), K-major by head: tile i, chunk row / 64, head row g, 16-byte
-            // chunk (row % 64) / 8 swizzled by g, element row % 8.  The previous item's
-            // P.V has completed: this warp's epilogue of it waited for O^T.
+            // chunk (row % 64) / 8 swizzled by g % 8 (rows 8-15 are the second 8-row swizzle
+            // atom), element row % 8.  The previous item's P.V has completed: this warp's
+            // epilogue of it waited for O^T.
             uint8_t *pb = smem + kOffP + (row / 64) * kSmallChunk + (row % 8) * 2;
 #pragma unroll
             for (int i = 0; i < kTiles; ++i)
 #pragma unroll
                 for (int g = 0; g < G; ++g)
                     *reinterpret_cast<__nv_bfloat16 *>(pb + i * kPTile + g * 128 +
-                                                       ((((row % 64) / 8) ^ g) << 4)) =
+                                                       ((((row % 64) / 8) ^ (g & 7)) << 4)) =
                         __float2bfloat16_rn(pv[i][g]);
             fence_proxy_async_smem();
             named_barrier(1, 128);   // also publishes the sums
@@ -560,10 +566,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             // epilogue: O^T (lane = dim) -> partial output, normalised by the sum
             bool done = got && mbar_wait(&o_full[x], use & 1, p.status, abort_flag);
             done = !__any_sync(kFullMaskTc, !done);
-            uint32_t o[8];
+            uint32_t o[G > 8 ? 16 : 8];   // O^T columns: one per head
             if (done) {
                 tc_fence_after_sync();
-                tmem_load_8(tmem + t_lane + kTmO + x * kN, o);
+                if constexpr (G > 8) {
+                    tmem_load_16(tmem + t_lane + kTmO + x * kN, o);
+                } else {
+                    tmem_load_8(tmem + t_lane + kTmO + x * kN, o);
+                }
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -683,7 +693,7 @@ cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
 
 bool decode_tc_supported(const DecodeParams &p, int head_dim) {
     const int g = p.num_kv_heads > 0 ? p.num_q_heads / p.num_kv_heads : 0;
-    return !p.kv_fp8 && head_dim == kHD && g >= 3 && g <= 8 && p.num_seqs <= kMaxSeqsTc &&
+    return !p.kv_fp8 && head_dim == kHD && g >= 3 && g <= kN && p.num_seqs <= kMaxSeqsTc &&
            (p.s_token * 2) % 16 == 0 && (p.s_head * 2) % 16 == 0 && (p.s_block * 2) % 16 == 0 &&
            (reinterpret_cast<uintptr_t>(p.k_cache) & 15) == 0 &&
            (reinterpret_cast<uintptr_t>(p.v_cache) & 15) == 0 &&
@@ -699,6 +709,14 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream) {
         case 6: return launch_tc<6, false>(p, stream);
         case 7: return launch_tc<7, false>(p, stream);
         case 8: return launch_tc<8, false>(p, stream);
+        case 9: return launch_tc<9, false>(p, stream);
+        case 10: return launch_tc<10, false>(p, stream);
+        case 11: return launch_tc<11, false>(p, stream);
+        case 12: return launch_tc<12, false>(p, stream);
+        case 13: return launch_tc<13, false>(p, stream);
+        case 14: return launch_tc<14, false>(p, stream);
+        case 15: return launch_tc<15, false>(p, stream);
+        case 16: return launch_tc<16, false>(p, stream);
         default: return cudaErrorNotSupported;
     }
 }
@@ -712,6 +730,14 @@ cudaError_t launch_decode_tc_single(const DecodeParams &p, cudaStream_t stream) 
         case 6: return launch_tc<6, true>(p, stream);
         case 7: return launch_tc<7, true>(p, stream);
         case 8: return launch_tc<8, true>(p, stream);
+        case 9: return launch_tc<9, true>(p, stream);
+        case 10: return launch_tc<10, true>(p, stream);
+        case 11: return launch_tc<11, true>(p, stream);
+        case 12: return launch_tc<12, true>(p, stream);
+        case 13: return launch_tc<13, true>(p, stream);
+        case 14: return launch_tc<14, true>(p, stream);
+        case 15: return launch_tc<15, true>(p, stream);
+        case 16: return launch_tc<16, true>(p, stream);
         default: return cudaErrorNotSupported;
     }
 }
