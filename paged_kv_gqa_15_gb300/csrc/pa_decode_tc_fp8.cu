@@ -504,10 +504,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto q_write = [&](int e, const uint4 &raw) {
             int bb, kk, pp;
             if (!items_qw.at(p, e, bb, kk, pp)) return;   // uniform over the CTA
-            if (sid < 16 * G) {                                  // warp-uniform
+            // head_max shuffles over the whole warp, so every lane of a warp holding a head's
+            // chunk takes part (with an odd G the last such warp's upper half holds zeros)
+            if (sid < 32 * ((G + 1) / 2)) {
                 const float s = q_split_scale(head_max(raw));
-                if ((lane & 15) == 0) qinv[(e & 1) * kN + (sid >> 4)] = 1.f / s;  // exact
-                store_q_split<G>(smem + kOffQ + (e & 1) * kQBytes, sid, raw, s);
+                if (sid < 16 * G) {
+                    if ((lane & 15) == 0) qinv[(e & 1) * kN + (sid >> 4)] = 1.f / s;  // exact
+                    store_q_split<G>(smem + kOffQ + (e & 1) * kQBytes, sid, raw, s);
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -671,18 +675,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kTiles; ++i) {
 #pragma unroll
-                for (int g = 0; g < G; g += 2) {
-                    const float a0 = pv[i][g] * kPScale, a1 = pv[i][g + 1] * kPScale;
+                for (int g = 0; g < G; g += 2) {   // heads in pairs; an odd G's last alone
+                    const bool pair = g + 1 < G;
+                    const float a0 = pv[i][g] * kPScale;
+                    const float a1 = pair ? pv[i][pair ? g + 1 : g] * kPScale : 0.f;
                     const uint16_t hi = e4m3x2(a1, a0);
                     const float2 back = e4m3x2_to_float2(hi);
                     const uint16_t lo = e4m3x2(a1 - back.y, a0 - back.x);
                     uint8_t *t = pb + i * kPTile;
                     const int u = row >> 4;   // 16-byte unit of this token within a row
                     t[g * 128 + ((u ^ (g & 7)) << 4)] = static_cast<uint8_t>(hi & 0xffu);
-                    t[(g + 1) * 128 + ((u ^ ((g + 1) & 7)) << 4)] = static_cast<uint8_t>(hi >> 8);
                     t[(G + g) * 128 + ((u ^ ((G + g) & 7)) << 4)] = static_cast<uint8_t>(lo & 0xffu);
-                    t[(G + g + 1) * 128 + ((u ^ ((G + g + 1) & 7)) << 4)] =
-                        static_cast<uint8_t>(lo >> 8);
+                    if (pair) {
+                        t[(g + 1) * 128 + ((u ^ ((g + 1) & 7)) << 4)] = static_cast<uint8_t>(hi >> 8);
+                        t[(G + g + 1) * 128 + ((u ^ ((G + g + 1) & 7)) << 4)] =
+                            static_cast<uint8_t>(lo >> 8);
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -775,8 +783,8 @@ cudaError_t launch_tc8(const DecodeParams &p, cudaStream_t stream) {
 
 bool decode_tc8_supported(const DecodeParams &p, int head_dim) {
     const int g = p.num_kv_heads > 0 ? p.num_q_heads / p.num_kv_heads : 0;
-    // the P rows pair heads (g even); 2 g hi / lo rows fill the MMA's N of 16
-    return p.kv_fp8 && head_dim == kHD && (g == 4 || g == 6 || g == 8) && p.num_seqs <= kMaxSeqs &&
+    // 2 g hi / lo rows fill the MMA's N of 16
+    return p.kv_fp8 && head_dim == kHD && g >= 3 && g <= kN / 2 && p.num_seqs <= kMaxSeqs &&
            p.s_token % 16 == 0 && p.s_head % 16 == 0 && p.s_block % 16 == 0 &&
            (reinterpret_cast<uintptr_t>(p.k_cache) & 15) == 0 &&
            (reinterpret_cast<uintptr_t>(p.v_cache) & 15) == 0 &&
@@ -786,8 +794,11 @@ bool decode_tc8_supported(const DecodeParams &p, int head_dim) {
 cudaError_t launch_decode_tc8(const DecodeParams &p, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
     switch (p.num_q_heads / p.num_kv_heads) {
+        case 3: return launch_tc8<3, false>(p, stream);
         case 4: return launch_tc8<4, false>(p, stream);
+        case 5: return launch_tc8<5, false>(p, stream);
         case 6: return launch_tc8<6, false>(p, stream);
+        case 7: return launch_tc8<7, false>(p, stream);
         case 8: return launch_tc8<8, false>(p, stream);
         default: return cudaErrorNotSupported;
     }
@@ -796,8 +807,11 @@ cudaError_t launch_decode_tc8(const DecodeParams &p, cudaStream_t stream) {
 cudaError_t launch_decode_tc8_single(const DecodeParams &p, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
     switch (p.num_q_heads / p.num_kv_heads) {
+        case 3: return launch_tc8<3, true>(p, stream);
         case 4: return launch_tc8<4, true>(p, stream);
+        case 5: return launch_tc8<5, true>(p, stream);
         case 6: return launch_tc8<6, true>(p, stream);
+        case 7: return launch_tc8<7, true>(p, stream);
         case 8: return launch_tc8<8, true>(p, stream);
         default: return cudaErrorNotSupported;
     }
