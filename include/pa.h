@@ -51,8 +51,9 @@
  *  - Supported shapes: head_dim in {64, 128, 256}; block_size == 16;
  *    num_q_heads % num_kv_heads == 0, with any group size g = num_q_heads /
  *    num_kv_heads ("paged_attn.py", num_queries_per_kv).  Query head h reads kv
- *    head h / g.  The decode kernels serve some group sizes directly (head_dim
- *    128 on the tensor cores: bf16 3-16, fp8 3-8; the CUDA-core kernel
+ *    head h / g.  The decode kernels serve some group sizes directly (on the
+ *    tensor cores bf16 3-16 at head_dim 128 and 3-8 at head_dim 64, fp8 3-8 at
+ *    head_dim 128; the CUDA-core kernel
  *    1, 2, 4 and 8); any other g runs as several groups of a divisor of g per kv
  *    head, each reading that kv head's pages (through L2).
  *    Pointers must be 16-byte aligned.

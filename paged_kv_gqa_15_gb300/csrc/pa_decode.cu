@@ -171,9 +171,9 @@ int largest_divisor(int G, std::initializer_list<int> cands) {
 }  // namespace
 
 // Any GQA group size G = nq / nkv ("paged_attn.py", forward_decode's num_queries_per_kv).
-// Kernels exist for some group sizes: the bf16 tensor-core decode (head_dim 128) for 3-16
-// query heads (its MMA's N), the fp8 one for 3-8 (hi and lo rows fill N), the CUDA-core
-// decode for 1, 2, 4 and 8.  A call runs on the first path with a kernel for G, else for
+// Kernels exist for some group sizes: the bf16 tensor-core decode for 3-16 query heads at
+// head_dim 128 (its MMA's N) and 3-8 at head_dim 64, the fp8 one for 3-8 at head_dim 128
+// (hi and lo rows fill N), the CUDA-core decode for 1, 2, 4 and 8.  A call runs on the first path with a kernel for G, else for
 // the largest divisor of G it has: bf16 G = 32 as two groups of 16 per kv head, fp8
 // G = 12 as two of 6, and a prime G above 16 (above 8 with fp8) on the CUDA cores as G
 // groups of one.  Groups of 1 and 2 stay on the CUDA cores, which stream them at the
@@ -181,13 +181,15 @@ int largest_divisor(int G, std::initializer_list<int> cands) {
 cudaError_t launch_decode(const DecodeParams &p0, int head_dim, bool split, cudaStream_t stream) {
     if (p0.num_seqs == 0) return cudaSuccess;
     const int G = p0.num_q_heads / p0.num_kv_heads;
-    const int g_tc = p0.kv_fp8 ? (G <= 2 ? 0 : largest_divisor(G, {8, 7, 6, 5, 4, 3}))
-                               : (G <= 2 ? 0 : largest_divisor(G, {16, 15, 14, 13, 12, 11, 10, 9,
-                                                                     8, 7, 6, 5, 4, 3}));
+    const int g_max = p0.kv_fp8 ? 8 : decode_tc_max_group(head_dim);
+    int g_tc = 0;
+    for (int c = g_max; G > 2 && c >= 3 && !g_tc; --c)
+        if (G % c == 0) g_tc = c;
     if (g_tc) {
         const DecodeParams p = regroup(p0, g_tc);
         if (decode_tc_supported(p, head_dim))
-            return split ? launch_decode_tc(p, stream) : launch_decode_tc_single(p, stream);
+            return split ? launch_decode_tc(p, head_dim, stream)
+                         : launch_decode_tc_single(p, head_dim, stream);
         if (decode_tc8_supported(p, head_dim))
             return split ? launch_decode_tc8(p, stream) : launch_decode_tc8_single(p, stream);
     }

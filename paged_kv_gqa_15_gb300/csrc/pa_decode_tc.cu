@@ -150,9 +150,14 @@ __device__ __forceinline__ int tc_seq_len(const DecodeParams &p, int b, bool fla
     return pair_seq_len(p, b, flag);
 }
 
-template <int G, bool SINGLE>
+template <int HD, int G, bool SINGLE>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     decode_tc_kernel(const __grid_constant__ DecodeTcParams prm) {
+    // head_dim 64 runs the head_dim-128 pipeline on the first 64-column chunk of every
+    // row: the score MMAs cover only that chunk, and O^T = V^T P keeps M = 128 over V
+    // tiles whose second chunk stays zero (its output rows 64-127 are zero and unread)
+    static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
+    constexpr int kCh = HD / 64;   // 64-column chunks of a row that carry data
     const DecodeParams &p = prm.d;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -191,6 +196,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // rows g .. 15 of the Q^T and P buffers stay zero (padding of the MMA's N)
     for (uint32_t i = threadIdx.x; i < (2 * kQBytes + kPBytes) / 16; i += kThreadsTc)
         reinterpret_cast<uint4 *>(smem + kOffQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (kCh == 1)   // the V tiles' unused second chunk reads zero
+        for (uint32_t i = threadIdx.x; i < kVStages * (kTileChunk / 16); i += kThreadsTc)
+            reinterpret_cast<uint4 *>(smem + kOffV + (i / (kTileChunk / 16)) * kTileBytes +
+                                      kTileChunk)[i % (kTileChunk / 16)] = make_uint4(0u, 0u, 0u, 0u);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&k_full[s], 1);
@@ -226,7 +235,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     if (warp >= 2 && warp < 6)   // the softmax warps are idle until the first scores
         prefetch_decode_inputs(p.seq_lens, p.block_tables, p.q, p.num_seqs, p.max_blocks,
-                               static_cast<size_t>(p.num_seqs) * p.num_q_heads * kHD * 2,
+                               static_cast<size_t>(p.num_seqs) * p.num_q_heads * HD * 2,
                                threadIdx.x - 64, 128);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -255,7 +264,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     } else {
         // the sequences by partition count, heaviest first, into pref[] (the sort's
         // histogram lives in the P buffer, whose zero padding it restores)
-        pair_sort<kThreadsTc>(p, pref, reinterpret_cast<int *>(smem + kOffP), kHD);
+        pair_sort<kThreadsTc>(p, pref, reinterpret_cast<int *>(smem + kOffP), HD);
         fence_proxy_async_smem();
     }
     tc_fence_before_sync();
@@ -297,11 +306,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     if (!mbar_wait(&q_empty[qb], ((e >> 1) & 1) ^ 1u, p.status, abort_flag))
                         stop = 1;
                     else
-                        mbar_arrive_expect_tx(&q_full[qb], 2 * G * 128);
+                        mbar_arrive_expect_tx(&q_full[qb], kCh * G * 128);
                 }
                 stop = __shfl_sync(kFullMaskTc, stop, 0);
                 if (stop) break;
-                if (lane < 2)   // Q rows of the group: one 64-column chunk per lane
+                if (lane < kCh)   // Q rows of the group: one 64-column chunk per lane
                     tma_load_3d(smem + kOffQ + qb * kQBytes + lane * kSmallChunk, &prm.tm_q,
                                 lane * 64, kh * G, b, &q_full[qb]);
             }
@@ -315,16 +324,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     if (!mbar_wait(&empty[s], ((it / NS) & 1) ^ 1u, p.status, abort_flag))
                         stop = 1;
                     else
-                        mbar_arrive_expect_tx(&full[s], kTileBytes);
+                        mbar_arrive_expect_tx(&full[s], kCh * kTileChunk);
                 }
                 stop = __shfl_sync(kFullMaskTc, stop, 0);
                 if (stop) break;
-                // lane l: page l / 2 of the tile, 64-column chunk l % 2
-                const int pg = __shfl_sync(kFullMaskTc, page, (i * kPagesPerTile + lane / 2) & 31);
-                if (lane < 2 * kPagesPerTile)   // K / V are read once: evict them first
-                    tma_load_4d_hint(ring + s * kTileBytes + (lane & 1) * kTileChunk +
-                                         (lane >> 1) * kBlockSize * 128,
-                                     tm, (lane & 1) * 64, 0, kvh, pg, &full[s], policy);
+                // lane l: page l / kCh of the tile, 64-column chunk l % kCh
+                const int pg = __shfl_sync(kFullMaskTc, page, (i * kPagesPerTile + lane / kCh) & 31);
+                if (lane < kCh * kPagesPerTile)   // K / V are read once: evict them first
+                    tma_load_4d_hint(ring + s * kTileBytes + (lane % kCh) * kTileChunk +
+                                         (lane / kCh) * kBlockSize * 128,
+                                     tm, (lane % kCh) * 64, 0, kvh, pg, &full[s], policy);
             }
         }
         // never leave the CTA with copies still landing in its shared memory
@@ -375,7 +384,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     tc_fence_after_sync();
                     const uint64_t kd = ring_k + ((s * kTileBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kHD / 16; ++kk) {
+                    for (int kk = 0; kk < HD / 16; ++kk) {
                         const uint32_t off = (kk % 4) * 32;
                         mma_bf16_ss(tmem + kTmS + x * 64 + i * kN,
                                     kd + (((kk / 4) * kTileChunk + off) >> 4),
@@ -413,7 +422,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                         uint8_t *vt = smem + kOffV + s * kTileBytes;
                         const int tail_end = min(kTok, (stale + kBlockSize - 1) / kBlockSize * kBlockSize);
                         const int head_begin = max(0, head / kBlockSize * kBlockSize);
-                        for (int c = 0; c < 2; ++c) {
+                        for (int c = 0; c < kCh; ++c) {
                             for (int row = stale; row < tail_end; ++row) {
                                 uint4 *dst = reinterpret_cast<uint4 *>(vt + c * kTileChunk + row * 128);
 #pragma unroll
@@ -600,11 +609,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                             run_m[g] = M;
                         }
                     }
-                    if (items.walk.last(e)) {   // the pair's last partition
+                    if (items.walk.last(e) && row < HD) {   // the pair's last partition
 #pragma unroll
                         for (int g = 0; g < G; ++g)
                             static_cast<__nv_bfloat16 *>(p.out)[(static_cast<int64_t>(b) * nq +
-                                                                 kh * G + g) * kHD + row] =
+                                                                 kh * G + g) * HD + row] =
                                 __float2bfloat16_rn(run_l[g] > 0.f ? run_o[g] / run_l[g] : 0.f);
                     }
                 }
@@ -613,7 +622,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 for (int g = 0; g < G; ++g) {
                     const int64_t r =
                         (static_cast<int64_t>(b) * nq + kh * G + g) * p.max_parts + part;
-                    p.part_o[r * kHD + row] = __uint_as_float(o[g]) / sm[g];
+                    if (row < HD) p.part_o[r * HD + row] = __uint_as_float(o[g]) / sm[g];
                     if (row == 0) {
                         p.part_m[r] = mx[g] * kLn2;
                         p.part_l[r] = sm[g];
@@ -633,20 +642,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
 }
 
-template <int G, bool SINGLE>
+template <int HD, int G, bool SINGLE>
 cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
     DecodeTcParams prm;
     prm.d = p;
     {
-        const cuuint64_t dims[3] = {kHD, static_cast<cuuint64_t>(p.num_q_heads),
+        const cuuint64_t dims[3] = {HD, static_cast<cuuint64_t>(p.num_q_heads),
                                     static_cast<cuuint64_t>(p.num_seqs)};
-        const cuuint64_t str[2] = {kHD * 2, static_cast<cuuint64_t>(p.num_q_heads) * kHD * 2};
+        const cuuint64_t str[2] = {HD * 2, static_cast<cuuint64_t>(p.num_q_heads) * HD * 2};
         const cuuint32_t box[3] = {64, G, 1};
         if (!encode_tensor_map_bf16(&prm.tm_q, p.q, 3, dims, str, box))
             return cudaErrorInvalidValue;
     }
     {
-        const cuuint64_t dims[4] = {kHD, kBlockSize, static_cast<cuuint64_t>(p.pool_kv_heads),
+        const cuuint64_t dims[4] = {HD, kBlockSize, static_cast<cuuint64_t>(p.pool_kv_heads),
                                     static_cast<cuuint64_t>(p.num_blocks)};
         const cuuint64_t str[3] = {static_cast<cuuint64_t>(p.s_token) * 2,
                                    static_cast<cuuint64_t>(p.s_head) * 2,
@@ -656,7 +665,7 @@ cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
             !encode_tensor_map_bf16(&prm.tm_v, p.v_cache, 4, dims, str, box))
             return cudaErrorInvalidValue;
     }
-    auto kern = decode_tc_kernel<G, SINGLE>;
+    auto kern = decode_tc_kernel<HD, G, SINGLE>;
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -691,55 +700,63 @@ cudaError_t launch_tc(const DecodeParams &p, cudaStream_t stream) {
 
 }  // namespace
 
+// The largest group size with a kernel at this head_dim.
+int decode_tc_max_group(int head_dim) { return head_dim == kHD ? kN : (head_dim == 64 ? 8 : 0); }
+
 bool decode_tc_supported(const DecodeParams &p, int head_dim) {
     const int g = p.num_kv_heads > 0 ? p.num_q_heads / p.num_kv_heads : 0;
-    return !p.kv_fp8 && head_dim == kHD && g >= 3 && g <= kN && p.num_seqs <= kMaxSeqsTc &&
+    return !p.kv_fp8 && g >= 3 && g <= decode_tc_max_group(head_dim) &&
+           p.num_seqs <= kMaxSeqsTc &&
            (p.s_token * 2) % 16 == 0 && (p.s_head * 2) % 16 == 0 && (p.s_block * 2) % 16 == 0 &&
            (reinterpret_cast<uintptr_t>(p.k_cache) & 15) == 0 &&
            (reinterpret_cast<uintptr_t>(p.v_cache) & 15) == 0 &&
            (reinterpret_cast<uintptr_t>(p.q) & 15) == 0;
 }
 
-cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream) {
+namespace {
+
+template <bool SINGLE>
+cudaError_t launch_tc_any(const DecodeParams &p, int head_dim, cudaStream_t stream) {
     if (p.num_seqs == 0) return cudaSuccess;
-    switch (p.num_q_heads / p.num_kv_heads) {
-        case 3: return launch_tc<3, false>(p, stream);
-        case 4: return launch_tc<4, false>(p, stream);
-        case 5: return launch_tc<5, false>(p, stream);
-        case 6: return launch_tc<6, false>(p, stream);
-        case 7: return launch_tc<7, false>(p, stream);
-        case 8: return launch_tc<8, false>(p, stream);
-        case 9: return launch_tc<9, false>(p, stream);
-        case 10: return launch_tc<10, false>(p, stream);
-        case 11: return launch_tc<11, false>(p, stream);
-        case 12: return launch_tc<12, false>(p, stream);
-        case 13: return launch_tc<13, false>(p, stream);
-        case 14: return launch_tc<14, false>(p, stream);
-        case 15: return launch_tc<15, false>(p, stream);
-        case 16: return launch_tc<16, false>(p, stream);
+    const int g = p.num_q_heads / p.num_kv_heads;
+    if (head_dim == 64) {
+        switch (g) {
+            case 3: return launch_tc<64, 3, SINGLE>(p, stream);
+            case 4: return launch_tc<64, 4, SINGLE>(p, stream);
+            case 5: return launch_tc<64, 5, SINGLE>(p, stream);
+            case 6: return launch_tc<64, 6, SINGLE>(p, stream);
+            case 7: return launch_tc<64, 7, SINGLE>(p, stream);
+            case 8: return launch_tc<64, 8, SINGLE>(p, stream);
+            default: return cudaErrorNotSupported;
+        }
+    }
+    switch (g) {
+        case 3: return launch_tc<kHD, 3, SINGLE>(p, stream);
+        case 4: return launch_tc<kHD, 4, SINGLE>(p, stream);
+        case 5: return launch_tc<kHD, 5, SINGLE>(p, stream);
+        case 6: return launch_tc<kHD, 6, SINGLE>(p, stream);
+        case 7: return launch_tc<kHD, 7, SINGLE>(p, stream);
+        case 8: return launch_tc<kHD, 8, SINGLE>(p, stream);
+        case 9: return launch_tc<kHD, 9, SINGLE>(p, stream);
+        case 10: return launch_tc<kHD, 10, SINGLE>(p, stream);
+        case 11: return launch_tc<kHD, 11, SINGLE>(p, stream);
+        case 12: return launch_tc<kHD, 12, SINGLE>(p, stream);
+        case 13: return launch_tc<kHD, 13, SINGLE>(p, stream);
+        case 14: return launch_tc<kHD, 14, SINGLE>(p, stream);
+        case 15: return launch_tc<kHD, 15, SINGLE>(p, stream);
+        case 16: return launch_tc<kHD, 16, SINGLE>(p, stream);
         default: return cudaErrorNotSupported;
     }
 }
 
-cudaError_t launch_decode_tc_single(const DecodeParams &p, cudaStream_t stream) {
-    if (p.num_seqs == 0) return cudaSuccess;
-    switch (p.num_q_heads / p.num_kv_heads) {
-        case 3: return launch_tc<3, true>(p, stream);
-        case 4: return launch_tc<4, true>(p, stream);
-        case 5: return launch_tc<5, true>(p, stream);
-        case 6: return launch_tc<6, true>(p, stream);
-        case 7: return launch_tc<7, true>(p, stream);
-        case 8: return launch_tc<8, true>(p, stream);
-        case 9: return launch_tc<9, true>(p, stream);
-        case 10: return launch_tc<10, true>(p, stream);
-        case 11: return launch_tc<11, true>(p, stream);
-        case 12: return launch_tc<12, true>(p, stream);
-        case 13: return launch_tc<13, true>(p, stream);
-        case 14: return launch_tc<14, true>(p, stream);
-        case 15: return launch_tc<15, true>(p, stream);
-        case 16: return launch_tc<16, true>(p, stream);
-        default: return cudaErrorNotSupported;
-    }
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecodeParams &p, int head_dim, cudaStream_t stream) {
+    return launch_tc_any<false>(p, head_dim, stream);
+}
+
+cudaError_t launch_decode_tc_single(const DecodeParams &p, int head_dim, cudaStream_t stream) {
+    return launch_tc_any<true>(p, head_dim, stream);
 }
 
 }  // namespace pa

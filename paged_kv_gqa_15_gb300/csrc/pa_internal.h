@@ -94,8 +94,9 @@ bool encode_tensor_map_u8(CUtensorMap *tm, const void *base, int rank, const cuu
 cudaError_t launch_write_cache(const WriteCacheParams &p, cudaStream_t stream);
 // Tensor-core partition pass of the split decode (head_dim 128, GQA group 4 or 8).
 bool decode_tc_supported(const DecodeParams &p, int head_dim);
-cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
-cudaError_t launch_decode_tc_single(const DecodeParams &p, cudaStream_t stream);
+int decode_tc_max_group(int head_dim);
+cudaError_t launch_decode_tc(const DecodeParams &p, int head_dim, cudaStream_t stream);
+cudaError_t launch_decode_tc_single(const DecodeParams &p, int head_dim, cudaStream_t stream);
 // The same over an FP8 E4M3 cache (pa_decode_tc_fp8.cu).
 bool decode_tc8_supported(const DecodeParams &p, int head_dim);
 cudaError_t launch_decode_tc8(const DecodeParams &p, cudaStream_t stream);

@@ -2,15 +2,16 @@
 num_queries_per_kv = num_heads // num_kv_heads, any integer; query head h reads kv head
 h / g), through the C ABI, against the fp64 oracle on every output element.
 
-The decode kernels serve some group sizes directly (head_dim 128 on the tensor cores:
-bf16 3-16, fp8 3-8; the CUDA-core kernel 1, 2, 4 and 8).  Any other size runs as several
-kernel groups per kv head, each of a divisor of g.  The cases below reach every kind of
-dispatch:
-  - a tensor-core group of its own (bf16 3, 5, 6, 7, 11, 12, 16; fp8 3, 5, 6, 7);
-  - tensor-core groups of a divisor (bf16 32 = 2 x 16; fp8 10 = 2 x 5, 12 = 2 x 6,
-    16 = 2 x 8);
-  - CUDA-core groups of a divisor (bf16 17 = 17 x 1; fp8 11 = 11 x 1; head_dim 64 / 256
-    with 3, 6 and 12).
+The decode kernels serve some group sizes directly (on the tensor cores: bf16 3-16 at
+head_dim 128 and 3-8 at head_dim 64, fp8 3-8 at head_dim 128; the CUDA-core kernel 1, 2,
+4 and 8).  Any other size runs as several kernel groups per kv head, each of a divisor of
+g.  The cases below reach every kind of dispatch:
+  - a tensor-core group of its own (bf16 3, 5, 6, 7, 11, 12, 16 at head_dim 128, 3 and 6
+    at head_dim 64; fp8 3, 5, 6, 7);
+  - tensor-core groups of a divisor (bf16 32 = 2 x 16, 12 = 2 x 6 at head_dim 64;
+    fp8 10 = 2 x 5, 12 = 2 x 6, 16 = 2 x 8);
+  - CUDA-core groups of a divisor (bf16 17 = 17 x 1; fp8 11 = 11 x 1; head_dim 256 with
+    3, 6 and 12).
 The prefill kernel takes the group size at run time; it is checked at 3 and 6, contiguous
 and paged."""
 import numpy as np
@@ -48,7 +49,7 @@ def test_bf16_decode_group_sizes_hd128(nq, nkv, split):
 @pytest.mark.parametrize("hd", [64, 256])
 @pytest.mark.parametrize("nq,nkv", [(6, 2), (12, 2), (24, 2)])
 @pytest.mark.parametrize("split", [False, True])
-def test_bf16_decode_group_sizes_cuda_core(hd, nq, nkv, split):
+def test_bf16_decode_group_sizes_other_head_dims(hd, nq, nkv, split):
     w = W.make_decode("gqa_cc", LENS, nq, nkv, hd, seed=130 + nq + hd)
     out, ref, _, _ = _run_decode(w, split)
     assert_close_bf16(out, ref, what=f"hd{hd} g{nq // nkv} split={split}")
