@@ -53,9 +53,9 @@
  *    num_kv_heads ("paged_attn.py", num_queries_per_kv).  Query head h reads kv
  *    head h / g.  The decode kernels serve some group sizes directly (on the
  *    tensor cores bf16 3-16 at head_dim 128 and 3-8 at head_dim 64, fp8 3-8 at
- *    head_dim 128; the CUDA-core kernel
- *    1, 2, 4 and 8); any other g runs as several groups of a divisor of g per kv
- *    head, each reading that kv head's pages (through L2).
+ *    head_dim 128; the CUDA-core kernel 1, 2, 4 and 8); any other g runs as
+ *    several groups of a divisor of g per kv head, each reading that kv head's
+ *    pages (through L2).
  *    Pointers must be 16-byte aligned.
  *  - sliding_window (decode and prefill): a query at position pos attends only
  *    to keys j > pos - sliding_window, the sliding_window most recent keys
