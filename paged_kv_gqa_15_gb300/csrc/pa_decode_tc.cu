@@ -1,5 +1,6 @@
 // pa_decode_tc.cu -- split-KV paged GQA decode on the Blackwell tensor cores, for
-// head_dim 128 and GQA groups of 4 or 8 query heads per kv head.
+// head_dim 128 with GQA groups of 3 to 16 query heads per kv head, and head_dim 64 with
+// groups of 3 to 8.
 //
 // What it computes is the partition pass of the split decode ("paged_attn.py",
 // the V2 branch of forward_decode): for sequence b, kv head kh and 512-token
@@ -15,13 +16,15 @@
 //  * a partition is 4 tiles of 128 tokens; a tile is 8 pages, loaded by TMA with
 //    one box per (page, 64-column chunk) -- 128-byte swizzle, ready for the MMA;
 //  * S^T = K Q^T per tile: tcgen05.mma M = 128 tokens, N = 16 (the group's query
-//    heads, zero-padded), K = 128, accumulated in TMEM (lane = token);
+//    heads, zero-padded), K = head_dim, accumulated in TMEM (lane = token);
 //  * four warps take the partition's softmax from TMEM (one token per thread and
 //    tile), reduce max and sum over the 512 tokens, and write P (bf16) to shared
 //    memory in the MMA's K-major layout;
 //  * O^T = V^T P: tcgen05.mma M = 128 dims, N = 16, K = 128 tokens per tile, with V
 //    read as an MN-major operand straight from the TMA tile; the epilogue reads
-//    O^T from TMEM (lane = dim) and writes the partials, coalesced.
+//    O^T from TMEM (lane = dim) and writes the partials, coalesced.  At head_dim 64
+//    the V tiles' second 64-dim chunk stays zero, so M stays 128 and rows 64-127 of
+//    O^T are zero and unread.
 //  * Persistent CTAs walk the compact (sequence, partition, kv head) item list;
 //    S, P and O are double-buffered across items.  K and V tiles stream through
 //    separate rings, each filled by its own producer warp: an item's V tiles wait
