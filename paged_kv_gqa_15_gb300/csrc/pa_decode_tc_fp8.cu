@@ -1,5 +1,5 @@
 // pa_decode_tc_fp8.cu -- split-KV paged GQA decode on the Blackwell tensor cores over
-// an FP8 E4M3 KV cache, for head_dim 128 and GQA groups of 4 or 8 query heads.
+// an FP8 E4M3 KV cache, for head_dim 128 and GQA groups of 3 to 8 query heads.
 //
 // What it computes is the partition pass of the split decode ("paged_attn.py", the V2
 // branch of forward_decode, with kv_cache_dtype "fp8", k_scale and v_scale): as the
