@@ -80,3 +80,37 @@ def test_prefill_group_sizes(nq, nkv, hd):
     assert_close_bf16(o, ref, what=f"prefill g{nq // nkv} hd{hd}")
     o, ref, _ = _paged_case([64, 129], [300, 129], nq, nkv, hd, seed=170 + nq + hd)
     assert_close_bf16(o, ref, what=f"paged prefill g{nq // nkv} hd{hd}")
+
+
+@pytest.mark.parametrize("nq,nkv", [(12, 2), (14, 2), (34, 2)])
+def test_static_entry_and_graph_replay_take_any_group(nq, nkv):
+    """The fixed-scratch split entry and a captured split step (the regrouping happens
+    on the host, before the launch, so a replay repeats the same kernels)."""
+    import oracle
+    import torch
+    import paged_kv_gqa_15_gb300 as pa
+    w = W.make_decode("gqas", [1, 513, 1500, 33], nq, nkv, 128, seed=180 + nq)
+    t = w.tensors("cuda")
+    q, kc, vc = t["q"], t["k_cache"], t["v_cache"]
+    bt = torch.from_numpy(w.block_tables).to("cuda")
+    sl = torch.from_numpy(w.seq_lens).to("cuda")
+    L = w.max_seq_len
+    ref = oracle.decode(W.to_bits(q), W.to_bits(kc), W.to_bits(vc), w.block_tables,
+                        w.seq_lens, nkv, 16, w.scale)
+    out = torch.full_like(q, float("nan"))
+    pa.pa_decode_split_static(out, q, kc, vc, bt, sl, w.scale, L)
+    torch.cuda.synchronize()
+    assert_close_bf16(out, ref, what=f"static g{nq // nkv}")
+    ws = pa.alloc_workspace(pa.decode_split_workspace_size(w.batch, nq, 128, L), "cuda")
+    out2 = torch.full_like(q, float("nan"))
+    stream = torch.cuda.Stream()
+    pa.pa_decode_split(out2, q, kc, vc, bt, sl, w.scale, L, ws, stream=stream)   # warm-up
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        pa.pa_decode_split(out2, q, kc, vc, bt, sl, w.scale, L, ws, stream=stream)
+    for _ in range(2):
+        out2.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_close_bf16(out2, ref, what=f"graph g{nq // nkv}")
