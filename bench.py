@@ -66,9 +66,9 @@ PARITY_MAX_ABS, PARITY_MEAN_ABS = 2e-2, 2e-3
 # for the source file hash they were measured on (otherwise reported as null).
 TRAFFIC = {
     # ncu capture of one decode_tc_kernel<4> launch on the Llama-8B decode workload:
-    # dram__bytes_read.sum 568.34 MB + dram__bytes_write.sum 4.80 MB
+    # dram__bytes_read.sum 568.34 MB + dram__bytes_write.sum 5.08 MB
     "decode_partitions:llama8b_decode_b64_h32kv8_d128": {
-        "src": "c4bbcafeb89f2717", "bytes_per_launch": 573137920},
+        "src": "e53731200feeaa9e", "bytes_per_launch": 573424896},
     # ncu capture of one prefill_kernel<128,64,ragged> launch on the 16-request ragged
     # causal prefill: dram__bytes_read.sum 298.53 MB + dram__bytes_write.sum 108.54 MB
     "ragged_prefill:ragged_prefill_r16_h32kv8_d128": {
@@ -78,9 +78,9 @@ TRAFFIC = {
     "ragged_prefill:chunked_paged_prefill_r8_h16kv8_d256": {
         "src": "fe29602adfbe4d3a", "bytes_per_launch": 419157248},
     # ncu capture of one decode_tc8_kernel<4> launch on the Llama-8B decode workload over
-    # an FP8 cache: dram__bytes_read.sum 284.48 MB + dram__bytes_write.sum 4.30 MB
+    # an FP8 cache: dram__bytes_read.sum 284.49 MB + dram__bytes_write.sum 4.33 MB
     "decode_partitions:llama8b_decode_fp8_b64_h32kv8_d128": {
-        "src": "f290f00f270e22cc", "bytes_per_launch": 288775424},
+        "src": "c96d19f3ccc7f4f1", "bytes_per_launch": 288820224},
 }
 
 
